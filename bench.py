@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark of the row-exact few-row quantized mat-vec on GB300.
+
+Metric: achieved HBM GB/s (algorithmic weight + x + y bytes per call, over
+the device time of the calls) and us per call, m = 1..8.  One "step" is one
+pass of the whole path over the workload: one call per listed m.
+
+Default workload: Q8_0 weights n = 4096, k = 4096, batch 1, m swept 1..8
+(W ~ N(0, 0.02) quantized to Q8_0, x ~ N(0, 1)), synthetic and seeded.
+Weights are read cold: every call uses the next copy of a ring of weight
+copies totalling >= 4x the L2 size.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas: the path needs no exchange); rank 0 prints max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+# name: (format, n, k, batch, m list, token-major grouped, config index for seeds)
+WORKLOADS = {
+    "f16_n256_k512_m1": ("f16", 256, 512, 1, [1], False, 0),
+    "q8_0_n4096_k4096_m1-8": ("q8_0", 4096, 4096, 1, list(range(1, 9)), False, 1),
+    "q4_K_n14336_k4096_m1-8": ("q4_K", 14336, 4096, 1, list(range(1, 9)), False, 2),
+    "q6_K_n128256_k4096_m1,4,8": ("q6_K", 128256, 4096, 1, [1, 4, 8], False, 3),
+    "q5_0_grouped_b16_n1024_k4096_m8": ("q5_0", 1024, 4096, 16, [8], True, 4),
+    # same formats at >= 64 MB of weights
+    "f16_n8192_k4096_m1-8": ("f16", 8192, 4096, 1, list(range(1, 9)), False, 5),
+    "q8_0_n16384_k4096_m1-8": ("q8_0", 16384, 4096, 1, list(range(1, 9)), False, 6),
+    "q4_K_n28672_k4096_m1-8": ("q4_K", 28672, 4096, 1, list(range(1, 9)), False, 7),
+    "q5_0_grouped_b32_n1024_k4096_m8": ("q5_0", 1024, 4096, 32, [8], True, 8),
+}
+DEFAULT = "q8_0_n4096_k4096_m1-8"
+METRIC = "achieved HBM GB/s (% of GB300 peak) and us/call, m=1..8 quantized mat-vec"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", 2070.0)), "measured"
+    return 6800.0, 2070.0, "fallback"
+
+
+def call_bytes(fmt, n, k, batch, m, row_bytes):
+    """Algorithmic bytes of one call: every weight once, x and y once."""
+    return batch * n * row_bytes + 4 * batch * m * k + 4 * batch * m * n
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, busy_mhz_floor: float = 0.0):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if s >= busy_mhz_floor] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import quantized_few_row_gb300 as rem
+    from quantized_few_row_gb300 import inputs
+
+    fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    rem.build()
+    rem.load()
+    rb = rem.rem_row_bytes(fmt, k)
+    wbytes = rb * n * batch
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    ring = max(1, math.ceil(4 * l2 / wbytes))
+    mmax = max(ms)
+
+    # weights: N(0, 0.02) drawn on the device, quantized by the library
+    wf = inputs.torch_normal((batch * n, k), 1000 + ci, inputs.W_STD, dev)
+    w0 = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+    rem.check(rem.rem_quantize(wf, fmt, batch * n, k, w0))
+    del wf
+    wring = [w0] + [w0.clone() for _ in range(ring - 1)]
+    if grouped:   # token-major: x [m, batch*k], y [m, batch*n]
+        x = inputs.torch_normal((mmax, batch * k), 2000 + ci, inputs.X_STD, dev)
+        y = torch.empty((mmax, batch * n), dtype=torch.float32, device=dev)
+        xbs, ybs = k, n
+    else:         # batch-major: x [batch, m, k]
+        x = inputs.torch_normal((batch, mmax, k), 2000 + ci, inputs.X_STD, dev)
+        y = torch.empty((batch, mmax, n), dtype=torch.float32, device=dev)
+        xbs, ybs = mmax * k, mmax * n
+    torch.cuda.synchronize()
+
+    def call(slot, m, stream=None):
+        return rem.rem_matvec(wring[slot], fmt, n, k, batch, x, m, xbs, y, ybs, stream)
+
+    # first calls outside any capture (device set-up, schedule caches)
+    for m in ms:
+        rem.check(call(0, m))
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    C = len(ms)
+    period = ring // math.gcd(C, ring)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for sidx in range(period):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for c, m in enumerate(ms):
+                    rem.check(call((sidx * C + c) % ring, m))
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    clocks = Clocks(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            graphs[s % period].replay()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for s in range(args.steps):
+            graphs[(args.warmup + s) % period].replay()
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+        torch.distributed.barrier()
+
+    step_bytes = sum(call_bytes(fmt, n, k, batch, m, rb) for m in ms)
+    value = world * step_bytes * args.steps / elapsed / 1e9
+
+    # per-m device time (cold ring, graph of one call per ring slot)
+    per_m = {}
+    for m in ms:
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for slot in range(ring):
+                    rem.check(call(slot, m))
+            reps = max(3, int(2e-3 / max(1e-9, elapsed / max(1, args.steps) / C) / ring) + 3)
+            for _ in range(2):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * ring)
+        per_m[m] = us
+    clk = clocks.stop(busy_mhz_floor=0.0)
+
+    # end to end through the public binding: x host->device, call, y device->host
+    xh = torch.empty_like(x, device="cpu").pin_memory()
+    xh.copy_(x.cpu())
+    yh = torch.empty_like(y, device="cpu").pin_memory()
+    h2d = sum(4 * batch * m * k for m in ms)
+    d2h = sum(4 * batch * m * n for m in ms)
+    e2e_steps = max(1, min(args.steps, 200))
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(cur)
+    slot = 0
+    for s in range(e2e_steps):
+        for m in ms:
+            if grouped:
+                x[:m].copy_(xh[:m], non_blocking=True)
+            else:
+                x[:, :m].copy_(xh[:, :m], non_blocking=True)
+            rem.check(call(slot % ring, m, cur))
+            slot += 1
+            if grouped:
+                yh[:m].copy_(y[:m], non_blocking=True)
+            else:
+                yh[:, :m].copy_(y[:, :m], non_blocking=True)
+    t1.record(cur)
+    torch.cuda.synchronize()
+    e2e_elapsed = t0.elapsed_time(t1) / 1e3
+    e2e_value = world * step_bytes * e2e_steps / e2e_elapsed / 1e9
+
+    hbm, sm_max, peak_kind = peaks()
+    fp32_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12   # TFLOP/s, plain FMA pipe
+    per_m_out = {}
+    for m in ms:
+        b = call_bytes(fmt, n, k, batch, m, rb)
+        gbs = b / (per_m[m] * 1e-6) / 1e9
+        tfl = 2.0 * m * batch * n * k / (per_m[m] * 1e-6) / 1e12
+        per_m_out[str(m)] = {"us": round(per_m[m], 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+                             "fp32_tflops": round(tfl, 2), "fp32_frac": round(tfl / fp32_peak, 4)}
+    launches = args.steps * C
+    avg_launch_s = elapsed / launches
+    achieved = (step_bytes / C) / avg_launch_s / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed / args.steps * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 accumulate over %s weights" % fmt,
+        "data": "synthetic (seeded W ~ N(0,0.02) quantized on device, x ~ N(0,1))",
+        "config": {"workload": args.workload, "format": fmt, "n": n, "k": k, "batch": batch, "m": ms,
+                   "token_major": grouped, "l2": f"cold: weight ring of {ring} copies x {wbytes} B (>= 4x L2)",
+                   "timed": "CUDA graphs of one step each, events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "per_m_us": {str(m): round(per_m[m], 3) for m in ms},
+        "per_m": per_m_out,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "rem_mv_kernel (all m of the step)",
+                     "fp32_peak_tflops": round(fp32_peak, 1)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "path": "pinned x -> device, rem_matvec, y -> pinned host, per call, un-captured"},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    return res
+
+
+# ---------------------------------------------------------------- the oracle on host cores
+
+def oracle_sample(fmt, n, k, batch, ms, grouped, ci, seconds: float):
+    """Time the oracle on a bounded sample of weight rows; returns
+    (GB/s of algorithmic bytes, cores, description)."""
+    import numpy as np
+
+    import oracle
+    from quantized_few_row_gb300 import inputs
+
+    oracle.build()
+    rows_total = batch * n
+
+    def run(rows):
+        wf = inputs.weights(rows, k, 1000 + ci)
+        w = oracle.quantize(wf, fmt)
+        mmax = max(ms)
+        x = inputs.activations(mmax, k, 2000 + ci)
+        idx = np.arange(rows, dtype=np.uint64)
+        t0 = time.perf_counter()
+        for m in ms:
+            oracle.matvec_rows(w, fmt, rows, k, x, m, k, 0, idx)
+        dt = time.perf_counter() - t0
+        nbytes = sum(rows * oracle.row_bytes(fmt, k) + 4 * m * k + 4 * m * rows for m in ms)
+        return dt, nbytes
+
+    rows = min(rows_total, 64)
+    dt, nb = run(rows)
+    while dt < seconds / 4 and rows < rows_total:
+        rows = min(rows_total, rows * 4)
+        dt, nb = run(rows)
+    return nb / dt / 1e9, oracle.threads(), f"{rows} of {rows_total} weight rows, m in {ms}, {dt:.2f} s"
+
+
+def run_reference(args):
+    fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload]
+    per_step = max(0.2, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for s in range(args.warmup + args.steps):
+        v, cores, desc = oracle_sample(fmt, n, k, batch, ms, grouped, ci, per_step)
+        if s >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 accumulate over exact f32 weights", "data": "synthetic",
+        "config": {"workload": args.workload, "format": fmt, "n": n, "k": k, "batch": batch, "m": ms},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if args.no_cpu_baseline:
+            res["cpu_baseline"] = None
+        else:
+            fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload]
+            v, cores, desc = oracle_sample(fmt, n, k, batch, ms, grouped, ci, args.cpu_seconds)
+            res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                   "sample": desc}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

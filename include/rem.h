@@ -1,0 +1,167 @@
+/*
+ * rem.h -- row-exact few-row quantized mat-vec on GB300 (sm_103a), C ABI.
+ *
+ * The operation is the one mlx-native 0.18.0 src/ops/row_exact_matvec.rs
+ * defines (module doc "Row-exact few-row mat-vec"):
+ *
+ *     y[b, j, :] = W[b] . x[b, j, :]      for b < batch, j < m, 1 <= m <= 8
+ *
+ * with F32 input rows x, F32 output y and weights W stored row-major as F16
+ * or as Q8_0 / Q4_K / Q6_K / Q5_0 blocks (RowExactWeight).  Batch b reads the
+ * weight rows b*n .. b*n+n-1, i.e. bytes from b*n*row_bytes(k)
+ * (RowExactMatvecShape, "Batched / grouped products").
+ *
+ * Row exactness (module doc "Row exactness"): output row j is bitwise
+ * identical whether it is computed alone (m = 1) or as one row of any
+ * m <= 8, on every run, as long as the split factor is the same.  The split
+ * factor is derived from (wtype, batch*n, k) alone (rem_split_factor);
+ * rows_per_cta only packs rows and never changes bits.
+ *
+ * Memory and ownership.  Every pointer passed to a compute call is a CUDA
+ * device pointer (or managed memory) owned by the caller; the library never
+ * allocates, frees, synchronises or copies to the host on these calls.
+ * `stream` is a cudaStream_t (NULL = the legacy default stream); the work is
+ * enqueued asynchronously on it and the call returns before it runs.
+ *
+ * Errors.  Every call validates its arguments before it launches anything;
+ * on an error nothing is written and a message prefixed "rem_matvec:" (or the
+ * call's name) is available from rem_last_error() on the calling thread.
+ */
+#ifndef REM_H
+#define REM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight storage (RowExactWeight); the integer values are part of the ABI. */
+typedef enum {
+    REM_F16 = 0,   /* row-major [batch*n, k] IEEE binary16, little-endian     */
+    REM_Q8_0 = 1,  /* [batch*n, k/32] blocks of 34 B: d f16 | int8 qs[32]      */
+    REM_Q4_K = 2,  /* [batch*n, k/256] blocks of 144 B: d, dmin f16 | 12 B
+                      6-bit scales/mins | 128 B nibbles                        */
+    REM_Q6_K = 3,  /* [batch*n, k/256] blocks of 210 B: 128 B low nibbles |
+                      64 B high 2-bit | int8 scales[16] | d f16                */
+    REM_Q5_0 = 4   /* [batch*n, k/32] blocks of 22 B: d f16 | u32 high bits |
+                      16 B nibbles                                             */
+} rem_wtype;
+
+/* Status codes. */
+typedef enum {
+    REM_OK = 0,
+    REM_EINVAL = -1,   /* an argument broke a validation rule; nothing launched */
+    REM_ELAUNCH = -2,  /* the schedule needs more threads per block than every
+                          kernel of the weight type can launch on this device */
+    REM_ECUDA = -3     /* a CUDA call failed (device, attribute or launch)     */
+} rem_status;
+
+#define REM_MAX_ROWS 8     /* ROW_EXACT_MATVEC_MAX_ROWS */
+#define REM_MAX_SPLIT 16   /* largest split factor a launch accepts */
+
+/*
+ * rem_matvec -- y[b, j, :] = W[b] . x[b, j, :] with the default schedule
+ * (dispatch_row_exact_matvec).
+ *
+ *   W       device pointer to batch*n weight rows of rem_row_bytes(wtype, k)
+ *           bytes each, row-major, batch-major.  Alignment: F16 8 B, Q8_0 2 B,
+ *           Q4_K 16 B, Q6_K 2 B, Q5_0 2 B.
+ *   wtype   a rem_wtype value.
+ *   n, k    output columns per batch (= weight rows per batch) and inner
+ *           dimension; k must be a multiple of 4 (F16), 32 (Q8_0, Q5_0) or
+ *           256 (Q4_K, Q6_K).
+ *   batch   independent products, >= 1.
+ *   x       device F32 input, 16-byte aligned.
+ *   m       input rows, 1..8.
+ *   x_batch_stride, y_batch_stride   elements between batches.
+ *   y       device F32 output, 4-byte aligned.
+ *
+ * Row strides are not arguments here.  They are inferred:
+ *   batch == 1                        x_row_stride = k,       y_row_stride = n
+ *   batch > 1, x_batch_stride < m*k   x_row_stride = batch*k, y_row_stride = batch*n
+ *                                     (token-major grouped projection,
+ *                                      RowExactMatvecShape::grouped_token_major)
+ *   otherwise (batch-major)           x_row_stride = k,       y_row_stride = n
+ * Use rem_matvec_ex to state them.
+ *
+ * Returns REM_OK, or REM_EINVAL / REM_ELAUNCH / REM_ECUDA (see rem_status).
+ */
+int rem_matvec(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch,
+               const float* x, uint32_t m, uint32_t x_batch_stride,
+               float* y, uint32_t y_batch_stride, void* stream);
+
+/*
+ * rem_matvec_ex -- the full form (dispatch_row_exact_matvec_scheduled with
+ * an explicit RowExactMatvecShape and RowExactMatvecSchedule).
+ *
+ *   x_row_stride, x_batch_stride   elements, multiples of 4
+ *   y_row_stride, y_batch_stride   elements; the m*batch output rows of n
+ *                                  elements must not overlap
+ *   split         K ranges per weight row, 1..REM_MAX_SPLIT, or 0 for
+ *                 rem_split_factor(wtype, batch*n, k).  Rows are bitwise
+ *                 comparable only between calls with the same split.
+ *   rows_per_cta  0 (automatic) or 32, 64, 128 or 256: weight rows one
+ *                 thread block handles.  Numerically inert.
+ *
+ * A split whose thread block would exceed the kernels' launch limit returns
+ * REM_ELAUNCH instead of launching (the page refuses such a launch rather
+ * than let Metal drop it; CUDA would fail it).
+ */
+int rem_matvec_ex(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch,
+                  const float* x, uint32_t m, uint32_t x_row_stride, uint32_t x_batch_stride,
+                  float* y, uint32_t y_row_stride, uint32_t y_batch_stride,
+                  uint32_t split, uint32_t rows_per_cta, void* stream);
+
+/*
+ * rem_row_bytes -- bytes of one weight row of k elements
+ * (RowExactWeight::row_bytes): F16 2k, Q8_0 k/32*34, Q4_K k/256*144,
+ * Q6_K k/256*210, Q5_0 k/32*22.  Returns 0 for an unknown wtype.  Host only.
+ */
+uint64_t rem_row_bytes(int wtype, uint32_t k);
+
+/*
+ * rem_split_factor -- the split factor rem_matvec uses for a weight of
+ * `rows` (= batch*n) rows of k elements (the analogue of
+ * row_exact_reduction_nsg followed by the device cap of
+ * RowExactMatvecSchedule::for_device).  It depends on (wtype, rows, k) only:
+ * a power of two so that rows/32 * split reaches about 2048 warps, at most 16
+ * and at most the number of chunks of a row.  The device cap is the largest
+ * power of two of warps every kernel of the weight type can launch; kernels
+ * are compiled for 512 threads, so it does not bind on sm_103a.  Returns 0
+ * for an unknown wtype or rows == 0 or k == 0.  Host only.
+ */
+uint32_t rem_split_factor(int wtype, uint32_t rows, uint32_t k);
+
+/*
+ * rem_dequantize -- exact F32 weights out[r, :] of `rows` weight rows
+ * (test hook for bit-exact decode checks).  Element values:
+ *   F16  the binary16 value;   Q8_0  d*q;   Q5_0  d*(q-16);
+ *   Q4_K (d*sc)*q - dmin*mn;   Q6_K  (d*sc)*(q-32)
+ * each product and the difference separately rounded to nearest even.
+ * W as for rem_matvec; out is a device F32 buffer of rows*k elements,
+ * 4-byte aligned.  Async on `stream`.
+ */
+int rem_dequantize(const void* W, int wtype, uint32_t rows, uint32_t k, float* out, void* stream);
+
+/*
+ * rem_quantize -- quantize F32 rows src[r, :] (device, rows*k elements,
+ * 4-byte aligned) into `rows` weight rows at W (device, alignment as for
+ * rem_matvec).  Round-to-nearest quantizers with fp16 scales: Q8_0
+ * d = amax/127; Q5_0 d = vmax/-16; Q4_K 6-bit sub-block scales and mins;
+ * Q6_K int8 sub-block scales; F16 rounds to nearest even.  Codes are
+ * roundf of x over the stored scale.  Async on `stream`.
+ */
+int rem_quantize(const float* src, int wtype, uint32_t rows, uint32_t k, void* W, void* stream);
+
+/* Thread-local message of the last failing call on this thread ("" if none). */
+const char* rem_last_error(void);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int rem_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REM_H */

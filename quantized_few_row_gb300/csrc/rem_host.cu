@@ -1,0 +1,498 @@
+// rem_host.cu -- host side of the C ABI declared in include/rem.h.
+//
+// The contract it enforces is the one of mlx-native 0.18.0
+// src/ops/row_exact_matvec.rs: `validate` (argument rules, output
+// non-aliasing, buffer extents), `row_exact_reduction_nsg` and
+// `RowExactMatvecSchedule::for_device` (a split factor that depends on the
+// weight shape only, capped by what every kernel of the weight type can
+// launch) and `dispatch_row_exact_matvec_scheduled` (refuse a launch above
+// the kernels' thread limit instead of launching it).  Every rule is checked
+// before anything is enqueued, so a rejected call writes nothing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/rem.h"
+#include "rem_internal.h"
+
+namespace rem {
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+bool valid_wt(int wt) { return wt >= 0 && wt < kNumWt; }
+
+const char* wt_name(int wt) {
+    static const char* names[] = {"F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0"};
+    return valid_wt(wt) ? names[wt] : "?";
+}
+
+uint64_t row_bytes_of(int wt, uint32_t k) {
+    if (!valid_wt(wt)) return 0;
+    return static_cast<uint64_t>(k / static_cast<uint32_t>(block_values(wt))) * block_bytes(wt);
+}
+
+uint32_t k_multiple(int wt) {
+    switch (wt) {
+    case kF16: return 4;
+    case kQ8_0: case kQ5_0: return 32;
+    default: return 256;
+    }
+}
+
+uint32_t w_align(int wt) {
+    switch (wt) {
+    case kF16: return 8;
+    case kQ4_K: return 16;  // 16-byte qs loads; 144-byte blocks keep it row to row
+    default: return 2;
+    }
+}
+
+uint32_t pow2_floor(uint64_t v) {
+    uint32_t p = 1;
+    while (static_cast<uint64_t>(p) * 2 <= v && p < (1u << 30)) p *= 2;
+    return p;
+}
+
+// Last element index + 1 touched by a strided [batch, rows, cols] view.
+uint64_t strided_extent(uint32_t batch, uint32_t bstride, uint32_t rows, uint32_t rstride, uint32_t cols) {
+    return static_cast<uint64_t>(batch - 1) * bstride + static_cast<uint64_t>(rows - 1) * rstride + cols;
+}
+
+// ---------------------------------------------------------------- driver entry points
+
+using PFN_encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using PFN_range = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+struct Driver {
+    PFN_encode encode = nullptr;
+    PFN_range range = nullptr;
+};
+
+const Driver& driver() {
+    static Driver d;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            d.encode = reinterpret_cast<PFN_encode>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            d.range = reinterpret_cast<PFN_range>(fn);
+        cudaGetLastError();
+    });
+    return d;
+}
+
+// ---------------------------------------------------------------- per-device state
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int smem_optin = 0;
+    uint32_t cap_warps[kNumWt] = {0, 0, 0, 0, 0};  // largest power-of-two warps every kernel can launch
+};
+
+std::mutex g_mu;
+DeviceState g_dev[64];
+std::map<std::tuple<const void*, int, int>, int> g_occ;  // (kernel, threads, smem) -> blocks per SM
+
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fail(REM_ECUDA, "rem_matvec: no current CUDA device");
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(REM_ECUDA, "rem_matvec: cannot query device %d", dev);
+        }
+        for (int wt = 0; wt < kNumWt; ++wt) {
+            int threads = kMaxWarps * 32;
+            for (int m = 1; m <= kMaxRows; ++m)
+                for (int nr0 = 1; nr0 <= 2; ++nr0) {
+                    const void* fn = mv_kernel(wt, m, nr0);
+                    cudaFuncAttributes fa;
+                    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess ||
+                        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, st.smem_optin) !=
+                            cudaSuccess) {
+                        cudaGetLastError();
+                        return fail(REM_ECUDA, "rem_matvec: cannot prepare the %s kernels on device %d (%s)",
+                                    wt_name(wt), dev, "no sm_103a image for this device?");
+                    }
+                    if (fa.maxThreadsPerBlock < threads) threads = fa.maxThreadsPerBlock;
+                }
+            st.cap_warps[wt] = threads >= 32 ? pow2_floor(static_cast<uint32_t>(threads / 32)) : 0;
+        }
+        st.ready = true;
+    }
+    *out = &st;
+    return REM_OK;
+}
+
+int blocks_per_sm(const void* fn, int threads, int smem) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(fn, threads, smem);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, static_cast<size_t>(smem)) != cudaSuccess) {
+        cudaGetLastError();
+        nb = 0;
+    }
+    g_occ[key] = nb;
+    return nb;
+}
+
+// A pointer the kernels may dereference, with at least `need` bytes after it
+// when the allocation's extent is known.
+int check_buffer(const void* p, uint64_t need, const char* what, int dev) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(REM_EINVAL, "rem_matvec: %s (%p) is not a CUDA-visible pointer", what, p);
+    }
+    if (at.type == cudaMemoryTypeUnregistered)
+        return fail(REM_EINVAL, "rem_matvec: %s (%p) is host memory not registered with CUDA", what, p);
+    if (at.type == cudaMemoryTypeHost && at.devicePointer != p)
+        return fail(REM_EINVAL, "rem_matvec: %s (%p) is pinned host memory; pass its device pointer", what, p);
+    if (at.type == cudaMemoryTypeDevice && at.device != dev)
+        return fail(REM_EINVAL, "rem_matvec: %s lives on device %d, the current device is %d", what, at.device, dev);
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+        const Driver& d = driver();
+        if (d.range) {
+            CUdeviceptr base = 0;
+            size_t size = 0;
+            if (d.range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) == CUDA_SUCCESS) {
+                const uint64_t avail = static_cast<uint64_t>(base) + size - reinterpret_cast<uint64_t>(p);
+                if (avail < need)
+                    return fail(REM_EINVAL, "rem_matvec: %s holds %llu bytes past the pointer, needs %llu", what,
+                                static_cast<unsigned long long>(avail), static_cast<unsigned long long>(need));
+            }
+        }
+    }
+    return REM_OK;
+}
+
+struct Shape {
+    uint32_t m, n, k, batch, xrs, xbs, yrs, ybs;
+};
+
+// The argument rules (validate), in the page's order.  Host-only: no CUDA call.
+int validate_args(const void* W, int wt, const float* x, const float* y, const Shape& s, uint32_t split,
+                  uint32_t rows_per_cta) {
+    if (!valid_wt(wt)) return fail(REM_EINVAL, "rem_matvec: unknown weight type %d", wt);
+    if (s.m == 0 || s.m > kMaxRows) return fail(REM_EINVAL, "rem_matvec: m (%u) must be in 1..=8", s.m);
+    if (s.n == 0 || s.k == 0 || s.batch == 0)
+        return fail(REM_EINVAL, "rem_matvec: n (%u), k (%u) and batch (%u) must be > 0", s.n, s.k, s.batch);
+    if (split > REM_MAX_SPLIT)
+        return fail(REM_EINVAL, "rem_matvec: split (%u) must be 0 (auto) or in 1..=%d", split, REM_MAX_SPLIT);
+    if (!(rows_per_cta == 0 || rows_per_cta == 32 || rows_per_cta == 64 || rows_per_cta == 128 ||
+          rows_per_cta == 256))
+        return fail(REM_EINVAL, "rem_matvec: rows_per_cta (%u) must be 0, 32, 64, 128 or 256", rows_per_cta);
+    if (!W || !x || !y) return fail(REM_EINVAL, "rem_matvec: W, x and y must be non-null");
+    if (s.k % k_multiple(wt) != 0)
+        return fail(REM_EINVAL, "rem_matvec: k (%u) must be a multiple of %u for %s", s.k, k_multiple(wt),
+                    wt_name(wt));
+    if (s.xrs % 4 != 0 || s.xbs % 4 != 0 || reinterpret_cast<uintptr_t>(x) % 16 != 0)
+        return fail(REM_EINVAL,
+                    "rem_matvec: input strides (%u, %u) must be multiples of 4 and the input pointer 16-byte aligned",
+                    s.xrs, s.xbs);
+    if (reinterpret_cast<uintptr_t>(W) % w_align(wt) != 0 || reinterpret_cast<uintptr_t>(y) % 4 != 0)
+        return fail(REM_EINVAL, "rem_matvec: weight pointer must be %u-byte and output pointer 4-byte aligned",
+                    w_align(wt));
+    // Output elements must not alias: rows of one product and the products of
+    // one call write disjoint ranges (either layout order is accepted).
+    const bool rows_disjoint = s.m == 1 || s.yrs >= s.n;
+    bool disjoint;
+    if (s.batch == 1) {
+        disjoint = rows_disjoint;
+    } else if (s.m == 1) {
+        disjoint = s.ybs >= s.n;
+    } else if (s.yrs >= s.ybs) {
+        disjoint = s.ybs >= s.n &&
+                   static_cast<uint64_t>(s.yrs) >= static_cast<uint64_t>(s.batch - 1) * s.ybs + s.n;
+    } else {
+        disjoint = rows_disjoint && static_cast<uint64_t>(s.ybs) >= static_cast<uint64_t>(s.m - 1) * s.yrs + s.n;
+    }
+    if (!disjoint)
+        return fail(REM_EINVAL,
+                    "rem_matvec: output strides overlap: y_row_stride %u, y_batch_stride %u, m %u, n %u, batch %u",
+                    s.yrs, s.ybs, s.m, s.n, s.batch);
+    if (static_cast<uint64_t>(s.m - 1) * s.yrs + s.n > 0xFFFFFFFFull)
+        return fail(REM_EINVAL, "rem_matvec: output row extent exceeds u32");
+    return REM_OK;
+}
+
+uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
+    const uint64_t nchunk = (k + chunk_values(wt) - 1) / chunk_values(wt);
+    const uint64_t groups = (rows + kLanes - 1) / kLanes;
+    const uint64_t per = groups >= 2048 ? 1 : 2048 / groups;
+    uint32_t s = pow2_floor(per);
+    if (s > static_cast<uint32_t>(kMaxSplit)) s = kMaxSplit;
+    const uint32_t cmax = pow2_floor(nchunk == 0 ? 1 : nchunk);
+    return s < cmax ? s : cmax;
+}
+
+struct Plan {
+    int nr0, g, stages, warps, smem;
+    uint32_t grid;
+    bool aligned;
+};
+
+int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& s, uint32_t split,
+                  uint32_t rows_per_cta, void* stream) {
+    int rc = validate_args(W, wt, x, y, s, split, rows_per_cta);
+    if (rc != REM_OK) return rc;
+    const uint64_t rb = row_bytes_of(wt, s.k);
+    const uint64_t rows = static_cast<uint64_t>(s.batch) * s.n;
+    DeviceState* ds = nullptr;
+    if ((rc = device_state(&ds)) != REM_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if ((rc = check_buffer(W, rb * rows, "weight", dev)) != REM_OK) return rc;
+    if ((rc = check_buffer(x, 4 * strided_extent(s.batch, s.xbs, s.m, s.xrs, s.k), "input", dev)) != REM_OK)
+        return rc;
+    if ((rc = check_buffer(y, 4 * strided_extent(s.batch, s.ybs, s.m, s.yrs, s.n), "output", dev)) != REM_OK)
+        return rc;
+
+    uint32_t S = split ? split : auto_split(wt, rows, s.k);
+    if (!split && S > ds->cap_warps[wt]) S = ds->cap_warps[wt];
+    const uint32_t nchunk = (s.k + chunk_values(wt) - 1) / chunk_values(wt);
+
+    Plan p{};
+    // two rows per lane share each input load once there are >= 4 input
+    // rows; Q6_K keeps one (its 53 staged words per row would spill)
+    p.nr0 = (s.m >= 4 && wt != kQ6_K) ? 2 : 1;
+    if (rows_per_cta) {
+        if (rows_per_cta < static_cast<uint32_t>(kLanes * p.nr0)) p.nr0 = 1;
+        p.g = static_cast<int>(rows_per_cta / (kLanes * p.nr0));
+    } else {
+        p.g = static_cast<int>(S >= static_cast<uint32_t>(kMaxWarps) ? 1 : kMaxWarps / S);
+    }
+    const uint64_t warps = static_cast<uint64_t>(S) * p.g;
+    if (warps * 32 > static_cast<uint64_t>(ds->cap_warps[wt]) * 32 || warps > static_cast<uint64_t>(kMaxWarps))
+        return fail(REM_ELAUNCH,
+                    "rem_matvec: split %u x %d row groups needs %llu threads per block but the %s kernels launch at "
+                    "most %u",
+                    S, p.g, static_cast<unsigned long long>(warps * 32), wt_name(wt), ds->cap_warps[wt] * 32);
+    p.warps = static_cast<int>(warps);
+
+    const uint32_t rows_per_group = static_cast<uint32_t>(kLanes * p.nr0);
+    const uint32_t gpb = (s.n + rows_per_group - 1) / rows_per_group;
+    const uint64_t total_groups = static_cast<uint64_t>(gpb) * s.batch;
+    const uint64_t grid = (total_groups + p.g - 1) / p.g;
+    if (grid > 0x7FFFFFFFull) return fail(REM_EINVAL, "rem_matvec: too many row groups (%llu)",
+                                          static_cast<unsigned long long>(total_groups));
+    p.grid = static_cast<uint32_t>(grid);
+
+    p.aligned = reinterpret_cast<uintptr_t>(W) % 16 == 0 && rb % 16 == 0 && rows < (1ull << 31) &&
+                rb / 2 < (1ull << 32) && driver().encode != nullptr;
+    const uint32_t cpw = (nchunk + S - 1) / S;  // chunks of the longest K range
+    const void* fn = mv_kernel(wt, static_cast<int>(s.m), p.nr0);
+    if (!p.aligned) {
+        p.stages = 1;
+    } else {
+        // deepest ring (<= 4, <= chunks per warp) that still lets the whole
+        // grid be resident at once when it can be; otherwise the deepest that fits
+        const int want_resident = static_cast<int>((grid + ds->sms - 1) / ds->sms);
+        int best = 1;
+        for (int d = static_cast<int>(cpw < static_cast<uint32_t>(kMaxStages) ? cpw : kMaxStages); d >= 1; --d) {
+            const int sm = static_cast<int>(mv_smem_bytes(wt, p.nr0, p.warps, d, static_cast<int>(s.m)));
+            if (sm > ds->smem_optin) continue;
+            if (best == 1) best = d;  // deepest that fits at all
+            if (blocks_per_sm(fn, p.warps * 32, sm) >= want_resident) {
+                best = d;
+                break;
+            }
+        }
+        p.stages = best;
+    }
+    p.smem = static_cast<int>(mv_smem_bytes(wt, p.nr0, p.warps, p.stages, static_cast<int>(s.m)));
+    if (p.smem > ds->smem_optin)
+        return fail(REM_ELAUNCH, "rem_matvec: needs %d bytes of shared memory, the device allows %d", p.smem,
+                    ds->smem_optin);
+
+    alignas(64) CUtensorMap tmap;
+    std::memset(&tmap, 0, sizeof(tmap));
+    if (p.aligned) {
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rb / 2), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rb)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(chunk_box(wt) / 2), rows_per_group};
+        const cuuint32_t estride[2] = {1, 1};
+        const CUresult cr = driver().encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), gdim,
+                                            gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return fail(REM_ECUDA, "rem_matvec: cuTensorMapEncodeTiled failed (%d)", (int)cr);
+    }
+
+    MvArgs a{};
+    a.w = static_cast<const uint8_t*>(W);
+    a.x = x;
+    a.y = y;
+    a.row_bytes = rb;
+    a.n = s.n;
+    a.k = s.k;
+    a.xrs = s.xrs;
+    a.xbs = s.xbs;
+    a.yrs = s.yrs;
+    a.ybs = s.ybs;
+    a.split = S;
+    a.nchunk = nchunk;
+    a.gpb = gpb;
+    a.total_groups = static_cast<uint32_t>(total_groups);
+    a.gpc = static_cast<uint32_t>(p.g);
+    a.stages = static_cast<uint32_t>(p.stages);
+    a.aligned = p.aligned ? 1u : 0u;
+    if (total_groups > 0xFFFFFFFFull) return fail(REM_EINVAL, "rem_matvec: too many row groups");
+
+    void* args[2] = {&tmap, &a};
+    const cudaError_t e = cudaLaunchKernel(fn, dim3(p.grid), dim3(p.warps * 32), args, static_cast<size_t>(p.smem),
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(REM_ECUDA, "rem_matvec: launch failed: %s", cudaGetErrorString(e));
+    }
+    return REM_OK;
+}
+
+int check_rows_buffer(const void* W, int wt, uint32_t rows, uint32_t k, const char* fn_name) {
+    if (!valid_wt(wt)) return fail(REM_EINVAL, "%s: unknown weight type %d", fn_name, wt);
+    if (rows == 0 || k == 0) return fail(REM_EINVAL, "%s: rows (%u) and k (%u) must be > 0", fn_name, rows, k);
+    if (k % k_multiple(wt) != 0)
+        return fail(REM_EINVAL, "%s: k (%u) must be a multiple of %u for %s", fn_name, k, k_multiple(wt),
+                    wt_name(wt));
+    if (!W) return fail(REM_EINVAL, "%s: null weight pointer", fn_name);
+    if (reinterpret_cast<uintptr_t>(W) % w_align(wt) != 0)
+        return fail(REM_EINVAL, "%s: weight pointer must be %u-byte aligned", fn_name, w_align(wt));
+    return REM_OK;
+}
+
+}  // namespace
+
+const void* mv_kernel(int wt, int m, int nr0) {
+    const bool lo = m <= 4;
+    switch (wt) {
+    case kF16: return lo ? mv_kernel_f16_a(m, nr0) : mv_kernel_f16_b(m, nr0);
+    case kQ8_0: return lo ? mv_kernel_q8_0_a(m, nr0) : mv_kernel_q8_0_b(m, nr0);
+    case kQ5_0: return lo ? mv_kernel_q5_0_a(m, nr0) : mv_kernel_q5_0_b(m, nr0);
+    case kQ4_K: return lo ? mv_kernel_q4_k_a(m, nr0) : mv_kernel_q4_k_b(m, nr0);
+    case kQ6_K: return lo ? mv_kernel_q6_k_a(m, nr0) : mv_kernel_q6_k_b(m, nr0);
+    default: return nullptr;
+    }
+}
+
+}  // namespace rem
+
+using namespace rem;
+
+extern "C" {
+
+int rem_matvec(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch, const float* x, uint32_t m,
+               uint32_t x_batch_stride, float* y, uint32_t y_batch_stride, void* stream) {
+    g_err[0] = '\0';
+    Shape s{m, n, k, batch, k, x_batch_stride, n, y_batch_stride};
+    if (batch > 1 && static_cast<uint64_t>(x_batch_stride) < static_cast<uint64_t>(m) * k) {
+        // token-major grouped projection: x [m, batch*k], y [m, batch*n]
+        const uint64_t xrs = static_cast<uint64_t>(batch) * k, yrs = static_cast<uint64_t>(batch) * n;
+        if (xrs > 0xFFFFFFFFull || yrs > 0xFFFFFFFFull)
+            return fail(REM_EINVAL, "rem_matvec: inferred token-major row stride exceeds u32; use rem_matvec_ex");
+        s.xrs = static_cast<uint32_t>(xrs);
+        s.yrs = static_cast<uint32_t>(yrs);
+    }
+    return launch_matvec(W, wtype, x, y, s, 0, 0, stream);
+}
+
+int rem_matvec_ex(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch, const float* x, uint32_t m,
+                  uint32_t x_row_stride, uint32_t x_batch_stride, float* y, uint32_t y_row_stride,
+                  uint32_t y_batch_stride, uint32_t split, uint32_t rows_per_cta, void* stream) {
+    g_err[0] = '\0';
+    const Shape s{m, n, k, batch, x_row_stride, x_batch_stride, y_row_stride, y_batch_stride};
+    return launch_matvec(W, wtype, x, y, s, split, rows_per_cta, stream);
+}
+
+uint64_t rem_row_bytes(int wtype, uint32_t k) { return row_bytes_of(wtype, k); }
+
+uint32_t rem_split_factor(int wtype, uint32_t rows, uint32_t k) {
+    if (!valid_wt(wtype) || rows == 0 || k == 0) return 0;
+    uint32_t s = auto_split(wtype, rows, k);
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+        DeviceState* ds = nullptr;
+        if (device_state(&ds) == REM_OK && s > ds->cap_warps[wtype]) s = ds->cap_warps[wtype];
+    }
+    cudaGetLastError();
+    g_err[0] = '\0';
+    return s;
+}
+
+int rem_dequantize(const void* W, int wtype, uint32_t rows, uint32_t k, float* out, void* stream) {
+    g_err[0] = '\0';
+    int rc = check_rows_buffer(W, wtype, rows, k, "rem_dequantize");
+    if (rc != REM_OK) return rc;
+    if (!out || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+        return fail(REM_EINVAL, "rem_dequantize: output must be non-null and 4-byte aligned");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(REM_ECUDA, "rem_dequantize: no current CUDA device");
+    }
+    const uint64_t rb = row_bytes_of(wtype, k);
+    if ((rc = check_buffer(W, rb * rows, "weight", dev)) != REM_OK) return rc;
+    if ((rc = check_buffer(out, 4ull * rows * k, "output", dev)) != REM_OK) return rc;
+    if (launch_dequantize(static_cast<const uint8_t*>(W), wtype, rows, k, rb, out, stream) != 0)
+        return fail(REM_ECUDA, "rem_dequantize: launch failed");
+    return REM_OK;
+}
+
+int rem_quantize(const float* src, int wtype, uint32_t rows, uint32_t k, void* W, void* stream) {
+    g_err[0] = '\0';
+    int rc = check_rows_buffer(W, wtype, rows, k, "rem_quantize");
+    if (rc != REM_OK) return rc;
+    if (!src || reinterpret_cast<uintptr_t>(src) % 4 != 0)
+        return fail(REM_EINVAL, "rem_quantize: input must be non-null and 4-byte aligned");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(REM_ECUDA, "rem_quantize: no current CUDA device");
+    }
+    const uint64_t rb = row_bytes_of(wtype, k);
+    if ((rc = check_buffer(src, 4ull * rows * k, "input", dev)) != REM_OK) return rc;
+    if ((rc = check_buffer(W, rb * rows, "weight", dev)) != REM_OK) return rc;
+    if (launch_quantize(src, wtype, rows, k, rb, static_cast<uint8_t*>(W), stream) != 0)
+        return fail(REM_ECUDA, "rem_quantize: launch failed");
+    return REM_OK;
+}
+
+const char* rem_last_error(void) { return g_err; }
+
+int rem_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// rem_internal.h -- declarations shared by the host library and the kernels.
+//
+// Weight formats follow mlx-native 0.18.0 src/ops/row_exact_matvec.rs
+// (RowExactWeight: F16, Q8_0, Q4_K, Q6_K, Q5_0 and their block sizes).
+#pragma once
+#include <cstdint>
+
+namespace rem {
+
+enum Wt : int { kF16 = 0, kQ8_0 = 1, kQ4_K = 2, kQ6_K = 3, kQ5_0 = 4, kNumWt = 5 };
+
+constexpr int kMaxRows = 8;        // ROW_EXACT_MATVEC_MAX_ROWS
+constexpr int kLanes = 32;         // weight rows per warp and NR0: one row per lane
+constexpr int kMaxWarps = 8;       // warps per CTA (kernels are bounded to 256 threads)
+constexpr int kMaxSplit = 8;       // K ranges per row
+constexpr int kMaxStages = 4;      // pipeline stages (mbarriers) per warp
+
+// Values and bytes of one block (the *_BLOCK_VALUES / *_BLOCK_BYTES constants).
+__host__ __device__ constexpr int block_values(int wt) {
+    return wt == kF16 ? 1 : (wt == kQ8_0 || wt == kQ5_0) ? 32 : 256;
+}
+__host__ __device__ constexpr int block_bytes(int wt) {
+    return wt == kF16 ? 2 : wt == kQ8_0 ? 34 : wt == kQ5_0 ? 22 : wt == kQ4_K ? 144 : 210;
+}
+
+// Staging geometry.  A "chunk" is the slice of one weight row a lane decodes
+// between two pipeline waits: 136 F16 values, 8 Q8_0 / Q5_0 blocks, or one
+// Q4_K / Q6_K super-block.  A warp stages the same chunk of its 32*NR0 rows
+// as one 2-D TMA box, one row every `box` bytes.  Box widths are odd
+// multiples of 16 bytes, so 32 lanes reading 16 bytes each at the same
+// offset of their own rows hit distinct bank quads (4 wavefronts, the
+// minimum).  Q6_K stages the 16-byte aligned 240-byte window around its
+// 210-byte super-block.
+__host__ __device__ constexpr int chunk_values(int wt) { return wt == kF16 ? 136 : 256; }
+__host__ __device__ constexpr int chunk_box(int wt) {
+    return (wt == kF16 || wt == kQ8_0) ? 272 : wt == kQ5_0 ? 176 : wt == kQ4_K ? 144 : 240;
+}
+
+// Kernel argument block (one launch).
+struct MvArgs {
+    const uint8_t* w;        // weight rows, batch b at b*n*row_bytes
+    const float* x;          // input, element (b, j, k) at b*xbs + j*xrs + k
+    float* y;                // output, element (b, j, i) at b*ybs + j*yrs + i
+    uint64_t row_bytes;
+    uint32_t n, k;
+    uint32_t xrs, xbs, yrs, ybs;
+    uint32_t split;          // K ranges per row (fixes the reduction order)
+    uint32_t nchunk;         // chunks per row
+    uint32_t gpb;            // row groups (of 32*NR0 rows) per batch
+    uint32_t total_groups;   // gpb * batch
+    uint32_t gpc;            // row groups per CTA
+    uint32_t stages;         // pipeline stages per warp (1..4)
+    uint32_t aligned;        // 1: 16-byte cp.async staging is legal
+    uint32_t pad;
+};
+
+// Kernel lookup: rem_mv_kernel<wt, m, nr0>, m in 1..8, nr0 in {1, 2}.
+// Each format is compiled in two units: M = 1..4 (_a) and M = 5..8 (_b).
+const void* mv_kernel(int wt, int m, int nr0);
+#define REM_DECLARE_PARTS(NAME) \
+    const void* NAME##_a(int m, int nr0); \
+    const void* NAME##_b(int m, int nr0);
+REM_DECLARE_PARTS(mv_kernel_f16)
+REM_DECLARE_PARTS(mv_kernel_q8_0)
+REM_DECLARE_PARTS(mv_kernel_q5_0)
+REM_DECLARE_PARTS(mv_kernel_q4_k)
+REM_DECLARE_PARTS(mv_kernel_q6_k)
+#undef REM_DECLARE_PARTS
+
+// Per-warp Q4_K sub-block input sums (8 sub-blocks x 8 rows of floats).
+constexpr int kXsumBytesPerWarp = 8 * kMaxRows * 4;
+
+// Dynamic shared memory of one CTA; the kernel lays it out the same way:
+// [rings (cross-warp partials reuse them)] [Q4_K input sums] [mbarriers], plus
+// slack to align the base to 128 bytes.
+inline uint32_t mv_smem_bytes(int wt, int nr0, int warps, int stages, int m) {
+    const uint32_t ring = (uint32_t)warps * (uint32_t)stages * kLanes * nr0 * chunk_box(wt);
+    const uint32_t red = (uint32_t)warps * nr0 * m * kLanes * 4u;
+    const uint32_t xs = (wt == kQ4_K) ? (uint32_t)warps * kXsumBytesPerWarp : 0u;
+    return (ring > red ? ring : red) + xs + (uint32_t)warps * kMaxStages * 8u + 128u;
+}
+
+// Auxiliary kernels (dequantize / quantize), rem_aux.cu.
+int launch_dequantize(const uint8_t* w, int wt, uint64_t rows, uint32_t k, uint64_t row_bytes,
+                      float* out, void* stream);
+int launch_quantize(const float* src, int wt, uint64_t rows, uint32_t k, uint64_t row_bytes,
+                    uint8_t* w, void* stream);
+
+}  // namespace rem

@@ -1,0 +1,139 @@
+"""The C ABI without a GPU: the library loads, exports what include/rem.h
+declares, and its host-side rules (row_bytes, split factor, argument
+validation) behave as specified.  Every call here returns before any CUDA
+call is made (invalid arguments are rejected first)."""
+import os
+import re
+
+import pytest
+
+import quantized_few_row_gb300 as rem
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rem.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rem.build()
+    return rem.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(rem_[a-z_]+)\s*\(", src))
+
+
+def test_header_declares_the_binding_names():
+    assert _declared() == set(rem.C_FUNCTIONS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert getattr(lib, name) is not None
+    assert rem.rem_version() == 1
+
+
+@pytest.mark.parametrize("wt,k,expect", [
+    ("f16", 512, 1024), ("q8_0", 4096, 4352), ("q4_K", 4096, 2304), ("q6_K", 4096, 3360),
+    ("q5_0", 4096, 2816), ("q8_0", 32, 34), ("q5_0", 32, 22), ("q4_K", 256, 144), ("q6_K", 256, 210),
+])
+def test_row_bytes(lib, wt, k, expect):
+    assert rem.rem_row_bytes(wt, k) == expect
+
+
+def test_row_bytes_unknown_type(lib):
+    assert rem.rem_row_bytes(9, 4096) == 0
+
+
+@pytest.mark.parametrize("wt,rows,k,expect", [
+    ("q8_0", 4096, 4096, 8),     # 128 row groups -> 2048/128 = 16, capped at 8
+    ("q4_K", 14336, 4096, 4),    # 448 row groups -> 4
+    ("q6_K", 128256, 4096, 1),   # 4008 row groups -> 1
+    ("q5_0", 16384, 4096, 4),    # 512 row groups -> 4
+    ("f16", 256, 512, 4),        # 8 groups -> 256, capped by 4 chunks of 136 values
+    ("q4_K", 32, 256, 1),        # one chunk per row
+])
+def test_split_factor_from_shape(lib, wt, rows, k, expect):
+    assert rem.rem_split_factor(wt, rows, k) == expect
+    assert rem.rem_split_factor(wt, rows, k) == expect   # no state, no m
+
+
+def test_split_factor_degenerate(lib):
+    assert rem.rem_split_factor("q8_0", 0, 4096) == 0
+    assert rem.rem_split_factor("q8_0", 64, 0) == 0
+    assert rem.rem_split_factor(7, 64, 256) == 0
+
+
+W, X, Y = 0x100000, 0x200000, 0x300000     # aligned fake addresses, never dereferenced
+
+
+def _ex(**kw):
+    a = dict(W=W, wtype="q8_0", n=64, k=256, batch=1, x=X, m=2, x_row_stride=256, x_batch_stride=0,
+             y=Y, y_row_stride=64, y_batch_stride=0, split=0, rows_per_cta=0)
+    a.update(kw)
+    return rem.rem_matvec_ex(a["W"], a["wtype"], a["n"], a["k"], a["batch"], a["x"], a["m"],
+                             a["x_row_stride"], a["x_batch_stride"], a["y"], a["y_row_stride"],
+                             a["y_batch_stride"], a["split"], a["rows_per_cta"], stream=0)
+
+
+CASES = [
+    ("m0", dict(m=0), "m (0) must be in 1..=8"),
+    ("m9", dict(m=9), "m (9) must be in 1..=8"),
+    ("n0", dict(n=0), "must be > 0"),
+    ("k0", dict(k=0), "must be > 0"),
+    ("batch0", dict(batch=0), "must be > 0"),
+    ("split", dict(split=17), "split (17)"),
+    ("rows_per_cta", dict(rows_per_cta=48), "rows_per_cta (48)"),
+    ("wtype", dict(wtype=7), "unknown weight type"),
+    ("nullW", dict(W=0), "non-null"),
+    ("nullx", dict(x=0), "non-null"),
+    ("nully", dict(y=0), "non-null"),
+    ("k_q8", dict(k=100, x_row_stride=100), "multiple of 32"),
+    ("k_f16", dict(wtype="f16", k=6, x_row_stride=8), "multiple of 4"),
+    ("k_q4k", dict(wtype="q4_K", k=288, x_row_stride=288), "multiple of 256"),
+    ("k_q6k", dict(wtype="q6_K", k=128, x_row_stride=128), "multiple of 256"),
+    ("k_q5", dict(wtype="q5_0", k=48, x_row_stride=48), "multiple of 32"),
+    ("xrs", dict(x_row_stride=258), "input strides"),
+    ("xbs", dict(batch=2, x_batch_stride=514, x_row_stride=256, y_batch_stride=128), "input strides"),
+    ("xalign", dict(x=X + 4), "16-byte aligned"),
+    ("walign_q4k", dict(wtype="q4_K", W=W + 8), "16-byte"),
+    ("walign_f16", dict(wtype="f16", W=W + 4), "8-byte"),
+    ("walign_q8", dict(W=W + 1), "2-byte"),
+    ("walign_q6k", dict(wtype="q6_K", W=W + 1), "2-byte"),
+    ("walign_q5", dict(wtype="q5_0", W=W + 1), "2-byte"),
+    ("yalign", dict(y=Y + 2), "output pointer 4-byte"),
+    ("rows_overlap", dict(m=2, y_row_stride=63), "overlap"),
+    ("batch_overlap_m1", dict(m=1, batch=2, x_batch_stride=256, y_batch_stride=63), "overlap"),
+    ("batch_major_overlap", dict(m=2, batch=2, x_batch_stride=512, y_row_stride=64, y_batch_stride=100),
+     "overlap"),
+    ("token_major_overlap", dict(m=2, batch=2, x_row_stride=512, x_batch_stride=256, y_row_stride=127,
+                                 y_batch_stride=64), "overlap"),
+    ("row_extent_u32", dict(m=8, y_row_stride=1 << 30), "exceeds u32"),
+]
+
+
+@pytest.mark.parametrize("name,kw,msg", CASES, ids=[c[0] for c in CASES])
+def test_validation_rejects(lib, name, kw, msg):
+    assert _ex(**kw) == rem.REM_EINVAL
+    err = rem.rem_last_error()
+    assert err.startswith("rem_matvec:"), err
+    assert msg in err, err
+
+
+def test_inferred_token_major_strides_validate(lib):
+    # rem_matvec with batch > 1 and x_batch_stride < m*k infers x_row_stride =
+    # batch*k and y_row_stride = batch*n; overlapping inferred outputs are
+    # still rejected: y_batch_stride < n
+    rc = rem.rem_matvec(W, "q8_0", 64, 256, 4, X, 2, 256, Y, 32, stream=0)
+    assert rc == rem.REM_EINVAL and "overlap" in rem.rem_last_error()
+
+
+def test_dequantize_and_quantize_validate(lib):
+    assert rem.rem_dequantize(W, "q4_K", 4, 300, Y, stream=0) == rem.REM_EINVAL
+    assert "rem_dequantize" in rem.rem_last_error()
+    assert rem.rem_dequantize(W + 8, "q4_K", 4, 256, Y, stream=0) == rem.REM_EINVAL
+    assert rem.rem_quantize(X, "q8_0", 0, 256, W, stream=0) == rem.REM_EINVAL
+    assert rem.rem_quantize(0, "q8_0", 4, 256, W, stream=0) == rem.REM_EINVAL
+    assert "rem_quantize" in rem.rem_last_error()
