@@ -25,9 +25,11 @@ __device__ __forceinline__ uint32_t rd32(const uint8_t* p) {
     return p[0] | (static_cast<uint32_t>(p[1]) << 8) | (static_cast<uint32_t>(p[2]) << 16) |
            (static_cast<uint32_t>(p[3]) << 24);
 }
+// Every 16-bit field of every format sits at an even offset of a block, and
+// blocks start at even addresses (W is at least 2-byte aligned), so a field
+// is written with one aligned 16-bit store.
 __device__ __forceinline__ void wr16(uint8_t* p, uint32_t v) {
-    p[0] = static_cast<uint8_t>(v);
-    p[1] = static_cast<uint8_t>(v >> 8);
+    *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(v & 0xFFFFu);
 }
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 __device__ __forceinline__ uint32_t h_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }

@@ -93,6 +93,10 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -627,6 +631,24 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap tmap, const MvArgs a) {
         const uint32_t c1 = static_cast<uint32_t>((static_cast<uint64_t>(s + 1) * a.nchunk) / S);
         const int nck = static_cast<int>(c1 - c0);
 
+        // Bring the input slice of chunk cc (M rows x chunk values) into L1
+        // ahead of use: every warp reads its own K range, so without this
+        // each block would wait for an L2 round trip.  Only addresses inside
+        // the slice are touched.
+        auto prefetch_x = [&](uint32_t cc) {
+            if (cc >= c1) return;
+            const uint32_t v0 = cc * Stage<WT>::kValues;
+            const uint32_t nv = min(static_cast<uint32_t>(Stage<WT>::kValues), a.k - v0);
+            const uint32_t bytes = 4u * nv;
+            const uint32_t lines = (bytes + 127u) / 128u + 1u;
+            for (uint32_t t = lane; t < static_cast<uint32_t>(M) * lines; t += 32u) {
+                const uint32_t j = t / lines, l = t - j * lines;
+                const char* base = reinterpret_cast<const char*>(xb + static_cast<uint64_t>(j) * a.xrs + v0);
+                const uint32_t off = (l + 1u == lines) ? bytes - 4u : 128u * l;
+                if (off < bytes) prefetch_l1(base + off);
+            }
+        };
+
         auto compute = [&](uint32_t cc, const uint8_t* st) {
             const uint8_t* rows[NR0];
 #pragma unroll
@@ -671,8 +693,11 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap tmap, const MvArgs a) {
             };
             if (lane == 0)
                 for (int i = 0; i < D && i < nck; ++i) issue(i);
+            prefetch_x(c0);
+            prefetch_x(c0 + 1);
             for (int i = 0; i < nck; ++i) {
                 const int t = i % D;
+                prefetch_x(c0 + static_cast<uint32_t>(i) + 2u);
                 const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8 * t, static_cast<uint32_t>((i / D) & 1)));
                 if (!ok) {
                     // chunks i .. i+D-1 may still be in flight: let them land
@@ -687,8 +712,10 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap tmap, const MvArgs a) {
                 if (lane == 0 && i + D < nck) issue(i + D);
             }
         } else {
+            prefetch_x(c0);
             for (int i = 0; i < nck; ++i) {
                 const uint32_t cc = c0 + static_cast<uint32_t>(i);
+                prefetch_x(cc + 1u);
                 stage_plain<WT, NR0>(ring, wg, a.row_bytes, nrows, cc, a.k, lane);
                 __syncwarp();
                 compute(cc, ring);

@@ -136,27 +136,36 @@ def test_rows_bitwise_equal_for_every_m(fmt):
             assert np.array_equal(y[j].view(np.uint32), alone[j].view(np.uint32)), (m, j)
 
 
+def _rows_per_warp(fmt, m, rows_per_cta):
+    """Rows per warp the library picks (two per lane from m >= 4, except Q6_K)."""
+    nr0 = 2 if (m >= 4 and fmt != "q6_K") else 1
+    if rows_per_cta and rows_per_cta < 32 * nr0:
+        nr0 = 1
+    return 32 * nr0
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_rows_inert_to_packing_path_and_runs(fmt):
-    n, k = 150, 2048
+    n, k = 300, 2048
     w, x = H.contiguous(fmt, n, k, 8, 230, 330)
-    split = rem.rem_split_factor(fmt, n, k)
+    split = 2
     base = H.run_matvec(w, fmt, n, k, 1, x, 8, k, 0, n, 0, 8 * n, split=split)
     variants = []
     for rpc in (32, 64, 128, 256):
-        if split * max(1, rpc // 64) <= 8:
+        if split * (rpc // _rows_per_warp(fmt, 8, rpc)) <= 8:
             variants.append(dict(rows_per_cta=rpc))
-    variants.append(dict(w_offset=2))               # 2-byte aligned base: plain staging path
-    if fmt in ("f16",):
-        variants[-1] = dict(w_offset=8)             # F16 needs 8-byte alignment
-    if fmt == "q4_K":
-        variants.pop()                              # Q4_K requires 16-byte alignment
+    assert len(variants) >= 2
+    if fmt == "f16":
+        variants.append(dict(w_offset=8))           # F16 needs 8-byte alignment: plain staging path
+    elif fmt != "q4_K":                             # Q4_K requires 16-byte alignment
+        variants.append(dict(w_offset=2))           # 2-byte aligned base: plain staging path
     for v in variants:
         y = H.run_matvec(w, fmt, n, k, 1, x, 8, k, 0, n, 0, 8 * n, split=split, **v)
         assert np.array_equal(y.view(np.uint32), base.view(np.uint32)), v
     for m in (1, 4):
-        ym = H.run_matvec(w, fmt, n, k, 1, x[:m], m, k, 0, n, 0, m * n, split=split, rows_per_cta=32)
-        assert np.array_equal(ym.view(np.uint32), base[:m * n].view(np.uint32)), m
+        for rpc in (32, 64):
+            ym = H.run_matvec(w, fmt, n, k, 1, x[:m], m, k, 0, n, 0, m * n, split=split, rows_per_cta=rpc)
+            assert np.array_equal(ym.view(np.uint32), base[:m * n].view(np.uint32)), (m, rpc)
     wh, wp = H.to_dev_bytes(w)
     xd = H.to_dev_f32(x)
     outs = []
@@ -265,9 +274,12 @@ def test_rejected_calls_write_nothing():
         a.update(b)
         rc = rem.rem_matvec_ex(a["wp"], "q8_0", n, a["k"], 1, xd, a["m"], k, 0, yd, a["yrs"], 0, 0, 0)
         assert rc == rem.REM_EINVAL, b
-    # a weight buffer too small for n rows
-    small = torch.zeros(10, dtype=torch.uint8, device=H.dev())
-    assert rem.rem_matvec_ex(small, "q8_0", n, k, 1, xd, m, k, 0, yd, n, 0, 0, 0) == rem.REM_EINVAL
+    # a weight pointer 64 bytes before the end of its allocation: the caching
+    # allocator gives a fresh 32 MiB request a segment of its own
+    torch.cuda.empty_cache()
+    big = torch.zeros(32 << 20, dtype=torch.uint8, device=H.dev())
+    near_end = big.data_ptr() + (32 << 20) - 64
+    assert rem.rem_matvec_ex(near_end, "q8_0", n, k, 1, xd, m, k, 0, yd, n, 0, 0, 0) == rem.REM_EINVAL
     assert "holds" in rem.rem_last_error()
     # host memory that CUDA cannot see
     host = np.zeros(m * n, np.float32)
