@@ -15,11 +15,12 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
 
-#include "../../include/rem.h"
+#include "rem.h"
 #include "rem_internal.h"
 
 namespace rem {
@@ -134,7 +135,7 @@ int device_state(DeviceState** out) {
             return fail(REM_ECUDA, "rem_matvec: cannot query device %d", dev);
         }
         for (int wt = 0; wt < kNumWt; ++wt) {
-            int threads = kMaxWarps * 32;
+            int threads = (kMaxWarps + 1) * 32;
             for (int m = 1; m <= kMaxRows; ++m)
                 for (int nr0 = 1; nr0 <= 2; ++nr0) {
                     const void* fn = mv_kernel(wt, m, nr0);
@@ -168,6 +169,27 @@ int blocks_per_sm(const void* fn, int threads, int smem) {
     }
     g_occ[key] = nb;
     return nb;
+}
+
+// Clusters of `split` blocks that can be resident at once (cached).
+uint64_t resident_clusters(const void* fn, const cudaLaunchConfig_t& cfg, uint32_t split, int sms) {
+    const int threads = static_cast<int>(cfg.blockDim.x);
+    const int smem = static_cast<int>(cfg.dynamicSmemBytes);
+    if (split <= 1) return static_cast<uint64_t>(blocks_per_sm(fn, threads, smem)) * sms;
+    static std::map<std::tuple<const void*, int, int, uint32_t>, int> cache;
+    std::lock_guard<std::mutex> lk(g_mu);
+    const auto key = std::make_tuple(fn, threads, smem, split);
+    auto it = cache.find(key);
+    if (it != cache.end()) return static_cast<uint64_t>(it->second);
+    cudaLaunchConfig_t c = cfg;
+    c.gridDim = dim3(split * 64u);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &c) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cache[key] = n;
+    return static_cast<uint64_t>(n);
 }
 
 // A pointer the kernels may dereference, with at least `need` bytes after it
@@ -261,8 +283,8 @@ uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
 }
 
 struct Plan {
-    int nr0, g, stages, warps, smem;
-    uint32_t grid;
+    int nr0, warps, stages, smem;
+    uint32_t cpb, grid;
     bool aligned;
 };
 
@@ -282,76 +304,125 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     if ((rc = check_buffer(y, 4 * strided_extent(s.batch, s.ybs, s.m, s.yrs, s.n), "output", dev)) != REM_OK)
         return rc;
 
+    // split = CTAs per cluster that share one row group's K ranges
     uint32_t S = split ? split : auto_split(wt, rows, s.k);
-    if (!split && S > ds->cap_warps[wt]) S = ds->cap_warps[wt];
+    if (!split && S > static_cast<uint32_t>(kMaxSplit)) S = kMaxSplit;
+    if (S > static_cast<uint32_t>(kMaxSplit))
+        return fail(REM_ELAUNCH,
+                    "rem_matvec: split %u needs clusters of %u thread blocks but the %s kernels launch clusters of "
+                    "at most %d",
+                    S, S, wt_name(wt), kMaxSplit);
     const uint32_t nchunk = (s.k + chunk_values(wt) - 1) / chunk_values(wt);
 
     Plan p{};
-    // two rows per lane share each input load once there are >= 4 input
-    // rows; Q6_K keeps one (its 53 staged words per row would spill)
+    // two rows per lane share every input load from m >= 4: each broadcast
+    // of x from shared memory then feeds two rows (Q6_K keeps one row: its
+    // 53 staged words per row would not fit twice in registers)
     p.nr0 = (s.m >= 4 && wt != kQ6_K) ? 2 : 1;
     if (rows_per_cta) {
         if (rows_per_cta < static_cast<uint32_t>(kLanes * p.nr0)) p.nr0 = 1;
-        p.g = static_cast<int>(rows_per_cta / (kLanes * p.nr0));
+        p.warps = static_cast<int>(rows_per_cta / (kLanes * p.nr0));
     } else {
-        p.g = static_cast<int>(S >= static_cast<uint32_t>(kMaxWarps) ? 1 : kMaxWarps / S);
+        // the widest row block (consumer warps per CTA) that still leaves at
+        // least two (row block, range) units per SM
+        p.warps = 1;
+        for (int g = 4; g >= 1; g /= 2) {
+            const uint64_t nb = static_cast<uint64_t>(s.batch) * ((s.n + kLanes * p.nr0 * g - 1) / (kLanes * p.nr0 * g));
+            if (nb * S >= 2ull * ds->sms || g == 1) {
+                p.warps = g;
+                break;
+            }
+        }
     }
-    const uint64_t warps = static_cast<uint64_t>(S) * p.g;
-    if (warps * 32 > static_cast<uint64_t>(ds->cap_warps[wt]) * 32 || warps > static_cast<uint64_t>(kMaxWarps))
-        return fail(REM_ELAUNCH,
-                    "rem_matvec: split %u x %d row groups needs %llu threads per block but the %s kernels launch at "
-                    "most %u",
-                    S, p.g, static_cast<unsigned long long>(warps * 32), wt_name(wt), ds->cap_warps[wt] * 32);
-    p.warps = static_cast<int>(warps);
+    const uint32_t rows_per_warp = static_cast<uint32_t>(kLanes * p.nr0);
+    if (p.warps > static_cast<int>(ds->cap_warps[wt]) || p.warps > kMaxWarps)
+        return fail(REM_ELAUNCH, "rem_matvec: %d warps per block exceed the %s kernels' limit of %u", p.warps,
+                    wt_name(wt), ds->cap_warps[wt]);
+    p.cpb = (s.n + rows_per_warp * p.warps - 1) / (rows_per_warp * p.warps);
+    const uint64_t nblocks = static_cast<uint64_t>(p.cpb) * s.batch;
+    if (nblocks > 0x7FFFFFFFull)
+        return fail(REM_EINVAL, "rem_matvec: too many row blocks (%llu)", static_cast<unsigned long long>(nblocks));
+    const void* fn = mv_kernel(wt, static_cast<int>(s.m), p.nr0);
+    const int threads = (p.warps + 1) * 32;
 
-    const uint32_t rows_per_group = static_cast<uint32_t>(kLanes * p.nr0);
-    const uint32_t gpb = (s.n + rows_per_group - 1) / rows_per_group;
-    const uint64_t total_groups = static_cast<uint64_t>(gpb) * s.batch;
-    const uint64_t grid = (total_groups + p.g - 1) / p.g;
-    if (grid > 0x7FFFFFFFull) return fail(REM_EINVAL, "rem_matvec: too many row groups (%llu)",
-                                          static_cast<unsigned long long>(total_groups));
-    p.grid = static_cast<uint32_t>(grid);
-
+    // TMA descriptors: weights as [rows][row_bytes/2] u16, inputs as
+    // [batch][m][k] f32 with the caller's strides
+    alignas(64) CUtensorMap wmap, xmap;
+    bool x_bm = false;
+    std::memset(&wmap, 0, sizeof(wmap));
+    std::memset(&xmap, 0, sizeof(xmap));
     p.aligned = reinterpret_cast<uintptr_t>(W) % 16 == 0 && rb % 16 == 0 && rows < (1ull << 31) &&
                 rb / 2 < (1ull << 32) && driver().encode != nullptr;
-    const uint32_t cpw = (nchunk + S - 1) / S;  // chunks of the longest K range
-    const void* fn = mv_kernel(wt, static_cast<int>(s.m), p.nr0);
+    if (p.aligned) {
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rb / 2), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rb)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(chunk_box(wt) / 2), rows_per_warp * p.warps};
+        const cuuint32_t estride[2] = {1, 1};
+        p.aligned = driver().encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), gdim, gstride,
+                                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    if (p.aligned) {
+        // dimensions ordered by increasing stride; either order stages the
+        // box as [m][chunk] in shared memory
+        const uint64_t xrs = s.m == 1 ? s.k : s.xrs;
+        const uint64_t xbs = s.batch == 1 ? xrs * s.m : s.xbs;
+        x_bm = xbs < xrs;
+        const cuuint64_t gdim[3] = {s.k, x_bm ? s.batch : s.m, x_bm ? s.m : s.batch};
+        const cuuint64_t gstride[2] = {4 * (x_bm ? xbs : xrs), 4 * (x_bm ? xrs : xbs)};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(chunk_values(wt)), x_bm ? 1u : s.m, x_bm ? s.m : 1u};
+        const cuuint32_t estride[3] = {1, 1, 1};
+        p.aligned = xrs > 0 && xbs > 0 &&
+                    driver().encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(x), gdim,
+                                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+
+    // stages: the deepest ring (<= 4) that keeps two blocks per SM, else the
+    // deepest that fits at all
     if (!p.aligned) {
         p.stages = 1;
     } else {
-        // deepest ring (<= 4, <= chunks per warp) that still lets the whole
-        // grid be resident at once when it can be; otherwise the deepest that fits
-        const int want_resident = static_cast<int>((grid + ds->sms - 1) / ds->sms);
-        int best = 1;
-        for (int d = static_cast<int>(cpw < static_cast<uint32_t>(kMaxStages) ? cpw : kMaxStages); d >= 1; --d) {
-            const int sm = static_cast<int>(mv_smem_bytes(wt, p.nr0, p.warps, d, static_cast<int>(s.m)));
+        int best = 0;
+        for (int d = kMaxStages; d >= 1; --d) {
+            const int sm = static_cast<int>(mv_smem_bytes(wt, p.nr0, p.warps, d, static_cast<int>(s.m), S));
             if (sm > ds->smem_optin) continue;
-            if (best == 1) best = d;  // deepest that fits at all
-            if (blocks_per_sm(fn, p.warps * 32, sm) >= want_resident) {
+            if (!best) best = d;
+            if (blocks_per_sm(fn, threads, sm) >= 2) {
                 best = d;
                 break;
             }
         }
-        p.stages = best;
+        p.stages = best ? best : 1;
     }
-    p.smem = static_cast<int>(mv_smem_bytes(wt, p.nr0, p.warps, p.stages, static_cast<int>(s.m)));
+    p.smem = static_cast<int>(mv_smem_bytes(wt, p.nr0, p.warps, p.stages, static_cast<int>(s.m), S));
     if (p.smem > ds->smem_optin)
         return fail(REM_ELAUNCH, "rem_matvec: needs %d bytes of shared memory, the device allows %d", p.smem,
                     ds->smem_optin);
 
-    alignas(64) CUtensorMap tmap;
-    std::memset(&tmap, 0, sizeof(tmap));
-    if (p.aligned) {
-        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rb / 2), static_cast<cuuint64_t>(rows)};
-        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rb)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(chunk_box(wt) / 2), rows_per_group};
-        const cuuint32_t estride[2] = {1, 1};
-        const CUresult cr = driver().encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), gdim,
-                                            gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (cr != CUDA_SUCCESS) return fail(REM_ECUDA, "rem_matvec: cuTensorMapEncodeTiled failed (%d)", (int)cr);
+    // persistent grid: as many clusters as can be resident, at most one per row block
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (S > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
     }
+    const uint64_t resident = resident_clusters(fn, cfg, S, ds->sms);
+    if (resident == 0)
+        return fail(REM_ELAUNCH, "rem_matvec: a cluster of %u blocks of %d threads and %d bytes does not fit",
+                    S, threads, p.smem);
+    const uint64_t ncl = std::min<uint64_t>(nblocks, resident);
+    p.grid = static_cast<uint32_t>(ncl * S);
+    cfg.gridDim = dim3(p.grid);
 
     MvArgs a{};
     a.w = static_cast<const uint8_t*>(W);
@@ -366,16 +437,14 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     a.ybs = s.ybs;
     a.split = S;
     a.nchunk = nchunk;
-    a.gpb = gpb;
-    a.total_groups = static_cast<uint32_t>(total_groups);
-    a.gpc = static_cast<uint32_t>(p.g);
+    a.cpb = p.cpb;
+    a.batch = s.batch;
     a.stages = static_cast<uint32_t>(p.stages);
     a.aligned = p.aligned ? 1u : 0u;
-    if (total_groups > 0xFFFFFFFFull) return fail(REM_EINVAL, "rem_matvec: too many row groups");
+    a.x_bm = x_bm ? 1u : 0u;
 
-    void* args[2] = {&tmap, &a};
-    const cudaError_t e = cudaLaunchKernel(fn, dim3(p.grid), dim3(p.warps * 32), args, static_cast<size_t>(p.smem),
-                                           static_cast<cudaStream_t>(stream));
+    void* args[3] = {&wmap, &xmap, &a};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(REM_ECUDA, "rem_matvec: launch failed: %s", cudaGetErrorString(e));

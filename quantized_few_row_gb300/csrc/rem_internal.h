@@ -12,7 +12,7 @@ enum Wt : int { kF16 = 0, kQ8_0 = 1, kQ4_K = 2, kQ6_K = 3, kQ5_0 = 4, kNumWt = 5
 constexpr int kMaxRows = 8;        // ROW_EXACT_MATVEC_MAX_ROWS
 constexpr int kLanes = 32;         // weight rows per warp and NR0: one row per lane
 constexpr int kMaxWarps = 8;       // warps per CTA (kernels are bounded to 256 threads)
-constexpr int kMaxSplit = 8;       // K ranges per row
+constexpr int kMaxSplit = 8;       // K ranges per row = CTAs per cluster (portable cluster limit)
 constexpr int kMaxStages = 4;      // pipeline stages (mbarriers) per warp
 
 // Values and bytes of one block (the *_BLOCK_VALUES / *_BLOCK_BYTES constants).
@@ -36,7 +36,9 @@ __host__ __device__ constexpr int chunk_box(int wt) {
     return (wt == kF16 || wt == kQ8_0) ? 272 : wt == kQ5_0 ? 176 : wt == kQ4_K ? 144 : 240;
 }
 
-// Kernel argument block (one launch).
+// Kernel argument block (one launch).  Grid: a number of clusters of
+// `split` CTAs that walk the batch * cpb row blocks; CTA rank s of a cluster
+// handles K range s.
 struct MvArgs {
     const uint8_t* w;        // weight rows, batch b at b*n*row_bytes
     const float* x;          // input, element (b, j, k) at b*xbs + j*xrs + k
@@ -44,14 +46,13 @@ struct MvArgs {
     uint64_t row_bytes;
     uint32_t n, k;
     uint32_t xrs, xbs, yrs, ybs;
-    uint32_t split;          // K ranges per row (fixes the reduction order)
+    uint32_t split;          // K ranges per row = CTAs per cluster (fixes the reduction order)
     uint32_t nchunk;         // chunks per row
-    uint32_t gpb;            // row groups (of 32*NR0 rows) per batch
-    uint32_t total_groups;   // gpb * batch
-    uint32_t gpc;            // row groups per CTA
-    uint32_t stages;         // pipeline stages per warp (1..4)
-    uint32_t aligned;        // 1: 16-byte cp.async staging is legal
-    uint32_t pad;
+    uint32_t cpb;            // row blocks per batch (each covers warps*32*NR0 rows)
+    uint32_t batch;
+    uint32_t stages;         // pipeline stages (1..4)
+    uint32_t aligned;        // 1: TMA staging (16-byte aligned rows, encodable input map)
+    uint32_t x_bm;           // input map dimension order: 1 = [k, batch, m] (token-major), 0 = [k, m, batch]
 };
 
 // Kernel lookup: rem_mv_kernel<wt, m, nr0>, m in 1..8, nr0 in {1, 2}.
@@ -67,17 +68,21 @@ REM_DECLARE_PARTS(mv_kernel_q4_k)
 REM_DECLARE_PARTS(mv_kernel_q6_k)
 #undef REM_DECLARE_PARTS
 
-// Per-warp Q4_K sub-block input sums (8 sub-blocks x 8 rows of floats).
-constexpr int kXsumBytesPerWarp = 8 * kMaxRows * 4;
-
 // Dynamic shared memory of one CTA; the kernel lays it out the same way:
-// [rings (cross-warp partials reuse them)] [Q4_K input sums] [mbarriers], plus
-// slack to align the base to 128 bytes.
-inline uint32_t mv_smem_bytes(int wt, int nr0, int warps, int stages, int m) {
-    const uint32_t ring = (uint32_t)warps * (uint32_t)stages * kLanes * nr0 * chunk_box(wt);
-    const uint32_t red = (uint32_t)warps * nr0 * m * kLanes * 4u;
-    const uint32_t xs = (wt == kQ4_K) ? (uint32_t)warps * kXsumBytesPerWarp : 0u;
-    return (ring > red ? ring : red) + xs + (uint32_t)warps * kMaxStages * 8u + 128u;
+// stages x [weight box (warps*32*NR0 rows x box) | input box (m x chunk
+// floats, padded to 128 B)], then the full and empty mbarriers of the
+// stages, then per-warp Q4_K sub-block input sums, plus slack to align the
+// base to 128 bytes.  With split > 1 two buffers of cross-range partial sums
+// (one per row-block parity) sit between the stages and the mbarriers.
+// `warps` counts consumer warps; the producer warp adds one more.
+inline uint32_t mv_stage_bytes(int wt, int nr0, int warps, int m) {
+    const uint32_t xb = (uint32_t)m * chunk_values(wt) * 4u;
+    return (uint32_t)warps * kLanes * nr0 * chunk_box(wt) + ((xb + 127u) & ~127u);
+}
+inline uint32_t mv_smem_bytes(int wt, int nr0, int warps, int stages, int m, int split) {
+    const uint32_t parts = split > 1 ? 2u * (uint32_t)warps * nr0 * m * kLanes * 4u : 0u;
+    return (uint32_t)stages * mv_stage_bytes(wt, nr0, warps, m) + parts + 16u * kMaxStages +
+           (uint32_t)(warps + 1) * 8u * kMaxRows * 4u + 128u;
 }
 
 // Auxiliary kernels (dequantize / quantize), rem_aux.cu.

@@ -5,11 +5,14 @@
 //
 // Work mapping.  A warp owns 32*NR0 consecutive weight rows, one row per lane
 // (lane l holds rows l and l+32).  All lanes of a warp work on the same K
-// positions at the same time, so every input load is a warp-wide broadcast
-// and every weight row is read from HBM exactly once for all M input rows.
-// K is cut into `split` contiguous ranges of chunks; warp s of a row group
-// handles range s, and the partial sums of the ranges are added in range
-// order through shared memory.
+// positions at the same time, so every input load is a shared-memory
+// broadcast and every weight row is read from HBM exactly once for all M
+// input rows.  K is cut into `split` contiguous ranges of chunks.  The
+// `split` CTAs of a thread-block cluster share the same rows and take one
+// range each; their partial sums are added in range order through
+// distributed shared memory by the cluster's rank-0 CTA.  Each CTA streams
+// its chunks through a ring of TMA stages: one box of weight rows and one box
+// of the matching inputs per stage, completed on one mbarrier.
 //
 // Row exactness (module doc "Row exactness").  The arithmetic of output
 // (i, j) depends only on row i's bytes, input row j and `split`:
@@ -85,16 +88,16 @@ __device__ __forceinline__ float4 ldg4(const float* p) {
     return __ldg(reinterpret_cast<const float4*>(p));
 }
 
+// Input values staged in shared memory (all lanes read the same address: a
+// broadcast).
+__device__ __forceinline__ float4 ldx4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
 __device__ __forceinline__ uint4 lds16(const uint8_t* p) {
     return *reinterpret_cast<const uint4*>(p);
 }
 
 __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -114,6 +117,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
@@ -137,6 +144,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
 
@@ -331,7 +347,7 @@ __device__ __forceinline__ void chain32(float2 (&c)[NR0][M], const float2 (&w)[N
     for (int q = 0; q < 8; ++q) {
         float4 xv[M];
 #pragma unroll
-        for (int j = 0; j < M; ++j) xv[j] = ldg4(xu + j * xrs + 4 * q);
+        for (int j = 0; j < M; ++j) xv[j] = ldx4(xu + j * xrs + 4 * q);
 #pragma unroll
         for (int i = 0; i < NR0; ++i)
 #pragma unroll
@@ -357,8 +373,8 @@ __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], con
         float4 xa[M], xb[M];
 #pragma unroll
         for (int j = 0; j < M; ++j) {
-            xa[j] = ldg4(xc + j * xrs + 8 * g);
-            xb[j] = second ? ldg4(xc + j * xrs + 8 * g + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xa[j] = ldx4(xc + j * xrs + 8 * g);
+            xb[j] = second ? ldx4(xc + j * xrs + 8 * g + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < NR0; ++i) {
@@ -417,7 +433,7 @@ __device__ __forceinline__ void chunk_q5_0(const uint8_t* const (&rows)[NR0], co
 }
 
 // Q4_K super-block.  xs[u*M + j] = sum of the 32 inputs of sub-block u for
-// input row j (computed cooperatively per chunk, see xsum_q4_k).
+// input row j (computed once per chunk for the CTA, see xsum_q4_k).
 template <int M, int NR0>
 __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], const float* xc, uint32_t xrs,
                                            const float* xs, float2 (&acc)[NR0][M]) {
@@ -465,16 +481,17 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
     }
 }
 
-// Cooperative sub-block input sums of one Q4_K chunk: lane (u = lane/4,
+// Sub-block input sums of one Q4_K chunk, per warp: lane (u = lane/4,
 // quarter = lane%4) adds 8 inputs, then two xor-shuffles combine the quarters
-// as (q0 + q1) + (q2 + q3).  The order is fixed, independent of M.
+// as (q0 + q1) + (q2 + q3).  The order is fixed and does not depend on M.
+// xc is the staged [M][256] input slice.
 template <int M>
-__device__ __forceinline__ void xsum_q4_k(const float* xc, uint32_t xrs, float* xs, int lane) {
+__device__ __forceinline__ void xsum_q4_k(const float* xc, float* xs, int lane) {
     const int u = lane >> 2, qt = lane & 3;
 #pragma unroll
     for (int j = 0; j < M; ++j) {
-        const float4 a = ldg4(xc + j * xrs + 32 * u + 8 * qt);
-        const float4 b = ldg4(xc + j * xrs + 32 * u + 8 * qt + 4);
+        const float4 a = ldx4(xc + j * 256 + 32 * u + 8 * qt);
+        const float4 b = ldx4(xc + j * 256 + 32 * u + 8 * qt + 4);
         float s = __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w)),
                             __fadd_rn(__fadd_rn(b.x, b.y), __fadd_rn(b.z, b.w)));
         s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
@@ -534,7 +551,7 @@ __device__ __forceinline__ void chunk_q6_k(const uint8_t* const (&rows)[NR0], co
                 for (int q = 0; q < 4; ++q) {
                     float4 xv[M];
 #pragma unroll
-                    for (int j = 0; j < M; ++j) xv[j] = ldg4(xu + j * xrs + 4 * q);
+                    for (int j = 0; j < M; ++j) xv[j] = ldx4(xu + j * xrs + 4 * q);
 #pragma unroll
                     for (int i = 0; i < NR0; ++i)
 #pragma unroll
@@ -549,22 +566,21 @@ __device__ __forceinline__ void chunk_q6_k(const uint8_t* const (&rows)[NR0], co
 
 // ---------------------------------------------------------------- staging
 
-// Fallback staging: copy chunk cc of the warp's rows with 2-byte loads into
-// the same positions the TMA path uses (W only needs 2-byte alignment).
-template <int WT, int NR0>
-__device__ __forceinline__ void stage_plain(uint8_t* st, const uint8_t* wg, uint64_t row_bytes, int nrows,
-                                            uint32_t cc, uint32_t k, int lane) {
-    constexpr int STRIDE = Stage<WT>::kBox;
+// Fallback staging (the TMA path needs 16-byte aligned rows): copy chunk cc
+// of one warp's rows with 2-byte loads into the positions a TMA box uses
+// (W only needs 2-byte alignment).
+template <int WT>
+__device__ __forceinline__ void stage_w_plain(uint8_t* dst_rows, const uint8_t* wrow0, uint64_t row_bytes,
+                                              int nrows, uint32_t cc, uint32_t k, int lane) {
+    constexpr int BOX = Stage<WT>::kBox;
     uint32_t first, len;  // byte range of the chunk inside the row
     if constexpr (WT == kF16) {
         first = cc * 272u;
-        const uint32_t vals = min(136u, k - cc * 136u);
-        len = 2u * vals;
+        len = 2u * min(136u, k - cc * 136u);
     } else if constexpr (WT == kQ8_0 || WT == kQ5_0) {
         constexpr uint32_t bb = (WT == kQ8_0) ? 34u : 22u;
         first = cc * 8u * bb;
-        const uint32_t nb = min(8u, k / 32u - cc * 8u);
-        len = nb * bb;
+        len = min(8u, k / 32u - cc * 8u) * bb;
     } else if constexpr (WT == kQ4_K) {
         first = cc * 144u;
         len = 144u;
@@ -575,171 +591,111 @@ __device__ __forceinline__ void stage_plain(uint8_t* st, const uint8_t* wg, uint
     const int so = Stage<WT>::sofs(cc);
     const uint32_t halves = len >> 1;
     for (int r = 0; r < nrows; ++r) {
-        const uint16_t* src = reinterpret_cast<const uint16_t*>(wg + (uint64_t)r * row_bytes + first);
-        uint16_t* dst = reinterpret_cast<uint16_t*>(st + r * STRIDE + so);
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(wrow0 + static_cast<uint64_t>(r) * row_bytes + first);
+        uint16_t* dst = reinterpret_cast<uint16_t*>(dst_rows + r * BOX + so);
         for (uint32_t h = lane; h < halves; h += 32) dst[h] = __ldg(src + h);
     }
 }
 
-// ---------------------------------------------------------------- the kernel
-
-template <int WT, int M, int NR0>
-__global__ void __launch_bounds__(kMaxWarps * 32)
-rem_mv_kernel(const __grid_constant__ CUtensorMap tmap, const MvArgs a) {
-    constexpr int STRIDE = Stage<WT>::kBox;
-    constexpr int ROWS = kLanes * NR0;
-    constexpr int STAGE = ROWS * STRIDE;
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
-    const int S = static_cast<int>(a.split);
-    const int D = static_cast<int>(a.stages);
-    const int lg = warp / S;
-    const int s = warp - lg * S;
-    const uint32_t g = blockIdx.x * a.gpc + static_cast<uint32_t>(lg);
-    const bool active = static_cast<uint32_t>(lg) < a.gpc && g < a.total_groups;
-
-    // shared layout: [rings | cross-warp partials (aliases rings)] [xsum] [mbarriers]
-    const uint32_t ring_bytes = static_cast<uint32_t>(nwarps) * D * STAGE;
-    const uint32_t red_bytes = static_cast<uint32_t>(nwarps) * NR0 * M * 32 * 4;
-    const uint32_t body = ring_bytes > red_bytes ? ring_bytes : red_bytes;
-    uint8_t* ring = smem + static_cast<uint32_t>(warp) * D * STAGE;
-    float* xs = reinterpret_cast<float*>(smem + body) + warp * (kXsumBytesPerWarp / 4);
-    const uint32_t xs_total = (WT == kQ4_K) ? static_cast<uint32_t>(nwarps) * kXsumBytesPerWarp : 0u;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + body + xs_total) + warp * kMaxStages;
-
-    float2 acc[NR0][M];
-#pragma unroll
-    for (int i = 0; i < NR0; ++i)
-#pragma unroll
-        for (int j = 0; j < M; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-
-    bool failed = false;
-    uint32_t b = 0, row0 = 0;
-    int nrows = 0;
-    if (active) {
-        b = g / a.gpb;
-        row0 = (g - b * a.gpb) * ROWS;
-        nrows = static_cast<int>(min(static_cast<uint32_t>(ROWS), a.n - row0));
-        const uint64_t grow = static_cast<uint64_t>(b) * a.n + row0;  // first global weight row
-        const uint8_t* wg = a.w + grow * a.row_bytes;
-        const float* xb = a.x + static_cast<uint64_t>(b) * a.xbs;
-        const uint32_t c0 = static_cast<uint32_t>((static_cast<uint64_t>(s) * a.nchunk) / S);
-        const uint32_t c1 = static_cast<uint32_t>((static_cast<uint64_t>(s + 1) * a.nchunk) / S);
-        const int nck = static_cast<int>(c1 - c0);
-
-        // Bring the input slice of chunk cc (M rows x chunk values) into L1
-        // ahead of use: every warp reads its own K range, so without this
-        // each block would wait for an L2 round trip.  Only addresses inside
-        // the slice are touched.
-        auto prefetch_x = [&](uint32_t cc) {
-            if (cc >= c1) return;
-            const uint32_t v0 = cc * Stage<WT>::kValues;
-            const uint32_t nv = min(static_cast<uint32_t>(Stage<WT>::kValues), a.k - v0);
-            const uint32_t bytes = 4u * nv;
-            const uint32_t lines = (bytes + 127u) / 128u + 1u;
-            for (uint32_t t = lane; t < static_cast<uint32_t>(M) * lines; t += 32u) {
-                const uint32_t j = t / lines, l = t - j * lines;
-                const char* base = reinterpret_cast<const char*>(xb + static_cast<uint64_t>(j) * a.xrs + v0);
-                const uint32_t off = (l + 1u == lines) ? bytes - 4u : 128u * l;
-                if (off < bytes) prefetch_l1(base + off);
-            }
-        };
-
-        auto compute = [&](uint32_t cc, const uint8_t* st) {
-            const uint8_t* rows[NR0];
-#pragma unroll
-            for (int i = 0; i < NR0; ++i) rows[i] = st + (lane + 32 * i) * STRIDE;
-            const float* xc = xb + static_cast<uint64_t>(cc) * Stage<WT>::kValues;
-            if constexpr (WT == kF16) {
-                const int nv = static_cast<int>(min(136u, a.k - cc * 136u));
-                if (nv == 136) chunk_f16<M, NR0, true>(rows, xc, a.xrs, nv, acc);
-                else chunk_f16<M, NR0, false>(rows, xc, a.xrs, nv, acc);
-            } else if constexpr (WT == kQ8_0 || WT == kQ5_0) {
-                const int nb = static_cast<int>(min(8u, a.k / 32u - cc * 8u));
-                if (nb == 8) {
-                    if constexpr (WT == kQ8_0) chunk_q8_0<M, NR0, true>(rows, xc, a.xrs, nb, acc);
-                    else chunk_q5_0<M, NR0, true>(rows, xc, a.xrs, nb, acc);
-                } else {
-                    if constexpr (WT == kQ8_0) chunk_q8_0<M, NR0, false>(rows, xc, a.xrs, nb, acc);
-                    else chunk_q5_0<M, NR0, false>(rows, xc, a.xrs, nb, acc);
-                }
-            } else if constexpr (WT == kQ4_K) {
-                xsum_q4_k<M>(xc, a.xrs, xs, lane);
-                __syncwarp();
-                chunk_q4_k<M, NR0>(rows, xc, a.xrs, xs, acc);
-            } else {
-                chunk_q6_k<M, NR0>(rows, xc, a.xrs, Stage<WT>::sofs(cc), acc);
-            }
-        };
-
-        if (a.aligned) {
-            // TMA path: each stage is one 2-D box of ROWS rows x STRIDE bytes.
-            const uint32_t bar0 = smem_u32(bars);
-            if (lane == 0) {
-                for (int t = 0; t < D; ++t) mbar_init(bar0 + 8 * t, 1);
-                asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-            }
-            __syncwarp();
-            auto issue = [&](int i) {  // lane 0 only
-                const uint32_t cc = c0 + static_cast<uint32_t>(i);
-                const int t = i % D;
-                mbar_expect_tx(bar0 + 8 * t, static_cast<uint32_t>(STAGE));
-                tma_load_2d(smem_u32(ring + t * STAGE), &tmap, static_cast<int32_t>(Stage<WT>::gofs(cc) / 2),
-                            static_cast<int32_t>(grow), bar0 + 8 * t);
-            };
-            if (lane == 0)
-                for (int i = 0; i < D && i < nck; ++i) issue(i);
-            prefetch_x(c0);
-            prefetch_x(c0 + 1);
-            for (int i = 0; i < nck; ++i) {
-                const int t = i % D;
-                prefetch_x(c0 + static_cast<uint32_t>(i) + 2u);
-                const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8 * t, static_cast<uint32_t>((i / D) & 1)));
-                if (!ok) {
-                    // chunks i .. i+D-1 may still be in flight: let them land
-                    // (bounded) before the CTA can exit and its smem be reused
-                    failed = true;
-                    for (int r = i; r < nck && r < i + D; ++r)
-                        (void)mbar_wait(bar0 + 8 * (r % D), static_cast<uint32_t>((r / D) & 1));
-                    break;
-                }
-                compute(c0 + static_cast<uint32_t>(i), ring + t * STAGE);
-                __syncwarp();
-                if (lane == 0 && i + D < nck) issue(i + D);
-            }
-        } else {
-            prefetch_x(c0);
-            for (int i = 0; i < nck; ++i) {
-                const uint32_t cc = c0 + static_cast<uint32_t>(i);
-                prefetch_x(cc + 1u);
-                stage_plain<WT, NR0>(ring, wg, a.row_bytes, nrows, cc, a.k, lane);
-                __syncwarp();
-                compute(cc, ring);
-                __syncwarp();
-            }
-        }
+// Fallback input staging: the [M][CV] slice of chunk cc, zero past k.
+template <int M, int CV>
+__device__ __forceinline__ void stage_x_plain(float* dst, const float* xb, uint32_t xrs, uint32_t cc, uint32_t k,
+                                              int nthreads) {
+    constexpr int Q = CV / 4;
+    for (int idx = static_cast<int>(threadIdx.x); idx < M * Q; idx += nthreads) {
+        const int j = idx / Q, q = idx - (idx / Q) * Q;
+        const uint32_t col = cc * CV + 4u * q;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < k) v = ldg4(xb + static_cast<uint64_t>(j) * xrs + col);
+        *reinterpret_cast<float4*>(dst + j * CV + 4 * q) = v;
     }
+}
 
-    // ---- cross-range reduction in range order, then the store
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    cluster_arrive();
+    cluster_wait();
+}
+
+// f32 at the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------- per-chunk and per-row-block steps
+
+// Decode + multiply one staged chunk for the warp's rows.
+template <int WT, int M, int NR0>
+__device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int warp, int lane, uint32_t cc,
+                                         uint32_t k, float* xs, float2 (&acc)[NR0][M]) {
+    constexpr int BOX = Stage<WT>::kBox;
+    constexpr int CV = Stage<WT>::kValues;
+    constexpr int ROWS = kLanes * NR0;
+    const uint8_t* rows[NR0];
+#pragma unroll
+    for (int i = 0; i < NR0; ++i) rows[i] = st + (warp * ROWS + lane + 32 * i) * BOX;
+    const float* xc = reinterpret_cast<const float*>(st + wstage);  // [M][CV]
+    if constexpr (WT == kF16) {
+        const int nv = static_cast<int>(min(136u, k - cc * 136u));
+        if (nv == 136) chunk_f16<M, NR0, true>(rows, xc, CV, nv, acc);
+        else chunk_f16<M, NR0, false>(rows, xc, CV, nv, acc);
+    } else if constexpr (WT == kQ8_0 || WT == kQ5_0) {
+        const int nb = static_cast<int>(min(8u, k / 32u - cc * 8u));
+        if (nb == 8) {
+            if constexpr (WT == kQ8_0) chunk_q8_0<M, NR0, true>(rows, xc, CV, nb, acc);
+            else chunk_q5_0<M, NR0, true>(rows, xc, CV, nb, acc);
+        } else {
+            if constexpr (WT == kQ8_0) chunk_q8_0<M, NR0, false>(rows, xc, CV, nb, acc);
+            else chunk_q5_0<M, NR0, false>(rows, xc, CV, nb, acc);
+        }
+    } else if constexpr (WT == kQ4_K) {
+        xsum_q4_k<M>(xc, xs, lane);
+        __syncwarp();
+        chunk_q4_k<M, NR0>(rows, xc, CV, xs, acc);
+    } else {
+        chunk_q6_k<M, NR0>(rows, xc, CV, Stage<WT>::sofs(cc), acc);
+    }
+}
+
+// End of a row block for one consumer warp: the range partial
+// (acc.x + acc.y), then either the store (split 1) or the in-order sum of
+// the cluster's ranges by rank 0.  Every thread of every CTA of the cluster
+// reaches the cluster barrier once per row block.
+template <int M, int NR0>
+__device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool failed, const MvArgs& a, uint32_t b,
+                                          uint32_t wrow0, bool wactive, bool consumer, int lane, int warp,
+                                          uint32_t s, uint32_t S, uint32_t t, float* parts, uint32_t part_floats) {
     float part[NR0][M];
 #pragma unroll
     for (int i = 0; i < NR0; ++i)
 #pragma unroll
         for (int j = 0; j < M; ++j)
             part[i][j] = failed ? __int_as_float(0x7FC00000) : __fadd_rn(acc[i][j].x, acc[i][j].y);
-
     auto store = [&](int i, int j, float v) {
-        const uint32_t row = row0 + static_cast<uint32_t>(lane + 32 * i);
-        if (row < a.n)
-            a.y[static_cast<uint64_t>(b) * a.ybs + static_cast<uint64_t>(j) * a.yrs + row] = v;
+        const uint32_t row = wrow0 + static_cast<uint32_t>(lane + 32 * i);
+        if (row < a.n) a.y[static_cast<uint64_t>(b) * a.ybs + static_cast<uint64_t>(j) * a.yrs + row] = v;
     };
-
     if (S == 1) {
-        if (active) {
+        if (wactive) {
 #pragma unroll
             for (int i = 0; i < NR0; ++i)
 #pragma unroll
@@ -747,23 +703,195 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap tmap, const MvArgs a) {
         }
         return;
     }
-    __syncthreads();  // every warp is done with its ring
-    float* red = reinterpret_cast<float*>(smem);
+    float* buf = parts + (t & 1u) * part_floats;
+    if (s != 0 && consumer) {
 #pragma unroll
-    for (int i = 0; i < NR0; ++i)
+        for (int i = 0; i < NR0; ++i)
 #pragma unroll
-        for (int j = 0; j < M; ++j) red[((warp * NR0 + i) * M + j) * 32 + lane] = part[i][j];
-    __syncthreads();
-    if (active && s == 0) {
+            for (int j = 0; j < M; ++j) buf[((warp * NR0 + i) * M + j) * 32 + lane] = part[i][j];
+    }
+    cluster_sync();  // phase t: the ranges' partials of this row block are published
+    if (s == 0 && wactive) {
 #pragma unroll
         for (int i = 0; i < NR0; ++i)
 #pragma unroll
             for (int j = 0; j < M; ++j) {
+                const float* slot = buf + ((warp * NR0 + i) * M + j) * 32 + lane;
                 float v = part[i][j];
-                for (int r = 1; r < S; ++r) v = __fadd_rn(v, red[(((warp + r) * NR0 + i) * M + j) * 32 + lane]);
+                for (uint32_t r = 1; r < S; ++r) v = __fadd_rn(v, ld_peer(slot, r));
                 store(i, j, v);
             }
     }
+}
+
+// ---------------------------------------------------------------- the kernel
+
+// Persistent kernel.  A cluster of `split` CTAs walks the row blocks
+// cid, cid + nclusters, ... (a row block is G row groups of ROWS = 32*NR0
+// rows of one batch); CTA rank s of the cluster handles K range s of every
+// row block.  A CTA has G consumer warps (one row group each) and one
+// producer warp.  Each pipeline stage holds one TMA box of the row block's
+// rows (G*ROWS x BOX bytes) and one box of the matching inputs (M x CV
+// floats).  The producer fills a stage once all consumer warps released it
+// (mbarrier `empty`, G arrivals) and runs on into the next row block;
+// consumers wait for the bytes (mbarrier `full`) and release each stage as
+// soon as they are done with it.  After a row block, CTAs of rank > 0 leave
+// their partial sums in shared memory (double-buffered by row-block parity),
+// one cluster barrier publishes them, and rank 0 adds them in range order
+// through distributed shared memory and stores y.  The producer takes part in
+// that barrier split-phase (arrive after issuing a row block, wait one row
+// block later), so it never stalls the stream.
+template <int WT, int M, int NR0>
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32)
+rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
+    constexpr int BOX = Stage<WT>::kBox;
+    constexpr int CV = Stage<WT>::kValues;
+    constexpr int ROWS = kLanes * NR0;
+    constexpr uint32_t XBYTES = M * CV * 4;
+    constexpr uint32_t XPAD = (XBYTES + 127u) & ~127u;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = static_cast<int>(blockDim.x >> 5) - 1;  // consumer warps; warp G produces
+    const bool producer = warp == G;
+    const uint32_t S = a.split;
+    const int D = static_cast<int>(a.stages);
+    const uint32_t s = S > 1 ? cluster_rank() : 0u;
+    const uint32_t cid = blockIdx.x / S;
+    const uint32_t ncl = gridDim.x / S;
+    const uint32_t wstage = static_cast<uint32_t>(G * ROWS * BOX);
+    const uint32_t stage_bytes = wstage + XPAD;
+    const uint32_t part_floats = static_cast<uint32_t>(G * NR0 * M * 32);
+    float* parts = reinterpret_cast<float*>(smem + D * stage_bytes);  // [2][G][NR0][M][32] when S > 1
+    uint64_t* full = reinterpret_cast<uint64_t*>(parts + (S > 1 ? 2 * part_floats : 0));
+    uint64_t* empty = full + kMaxStages;
+    float* xs = reinterpret_cast<float*>(empty + kMaxStages) + warp * (8 * kMaxRows);
+    const uint32_t c0 = static_cast<uint32_t>((static_cast<uint64_t>(s) * a.nchunk) / S);
+    const uint32_t c1 = static_cast<uint32_t>((static_cast<uint64_t>(s + 1) * a.nchunk) / S);
+    const int nck = static_cast<int>(c1 - c0);
+    const uint32_t nblocks = a.cpb * a.batch;  // row blocks of the whole launch
+
+    // row block -> (batch, first row in the batch)
+    auto block_origin = [&](uint32_t rb, uint32_t& b, uint32_t& row0) {
+        b = rb / a.cpb;
+        row0 = (rb - b * a.cpb) * static_cast<uint32_t>(G * ROWS);
+    };
+
+    bool failed = false;
+
+    if (!a.aligned) {
+        // ---- plain staging: every warp copies, consumers compute, one stage
+        const int nthreads = static_cast<int>(blockDim.x);
+        for (uint32_t rb = cid, t = 0; rb < nblocks; rb += ncl, ++t) {
+            uint32_t b, row0;
+            block_origin(rb, b, row0);
+            const uint32_t wrow0 = row0 + static_cast<uint32_t>(warp * ROWS);
+            const bool wactive = !producer && wrow0 < a.n;
+            const float* xb = a.x + static_cast<uint64_t>(b) * a.xbs;
+            const int wrows = wactive ? static_cast<int>(min(static_cast<uint32_t>(ROWS), a.n - wrow0)) : 0;
+            const uint8_t* wrow_ptr = a.w + (static_cast<uint64_t>(b) * a.n + wrow0) * a.row_bytes;
+            float2 acc[NR0][M];
+#pragma unroll
+            for (int i = 0; i < NR0; ++i)
+#pragma unroll
+                for (int j = 0; j < M; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+            for (int i = 0; i < nck; ++i) {
+                const uint32_t cc = c0 + static_cast<uint32_t>(i);
+                if (wactive) stage_w_plain<WT>(smem + warp * ROWS * BOX, wrow_ptr, a.row_bytes, wrows, cc, a.k, lane);
+                stage_x_plain<M, CV>(reinterpret_cast<float*>(smem + wstage), xb, a.xrs, cc, a.k, nthreads);
+                __syncthreads();
+                if (wactive) mv_chunk<WT, M, NR0>(smem, wstage, warp, lane, cc, a.k, xs, acc);
+                __syncthreads();
+            }
+            mv_finish<M, NR0>(acc, false, a, b, wrow0, wactive, !producer, lane, warp, s, S, t, parts, part_floats);
+        }
+        if (S > 1) cluster_sync();  // no CTA leaves while a peer may still read it
+        return;
+    }
+
+    // ---- TMA pipeline
+    const uint32_t fb = smem_u32(full), eb = smem_u32(empty);
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < D; ++t) {
+            mbar_init(fb + 8 * t, 1);
+            mbar_init(eb + 8 * t, static_cast<uint32_t>(G));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (producer) {
+        uint32_t i = 0;  // running chunk counter over all row blocks
+        bool stop = false;
+        uint32_t t = 0;
+        for (uint32_t rb = cid; rb < nblocks; rb += ncl, ++t) {
+            uint32_t b, row0;
+            block_origin(rb, b, row0);
+            const uint64_t grow0 = static_cast<uint64_t>(b) * a.n + row0;
+            if (lane == 0 && !stop) {
+                for (int q = 0; q < nck; ++q, ++i) {
+                    const int st = static_cast<int>(i % D);
+                    if (i >= static_cast<uint32_t>(D) &&
+                        !mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1))) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t cc = c0 + static_cast<uint32_t>(q);
+                    uint8_t* sp = smem + st * stage_bytes;
+                    mbar_expect_tx(fb + 8 * st, wstage + XBYTES);
+                    tma_load_2d(smem_u32(sp), &wmap, static_cast<int32_t>(Stage<WT>::gofs(cc) / 2),
+                                static_cast<int32_t>(grow0), fb + 8 * st);
+                    tma_load_3d(smem_u32(sp + wstage), &xmap, static_cast<int32_t>(cc * CV),
+                                a.x_bm ? static_cast<int32_t>(b) : 0, a.x_bm ? 0 : static_cast<int32_t>(b),
+                                fb + 8 * st);
+                }
+            }
+            __syncwarp();
+            if (S > 1) {
+                if (t > 0) cluster_wait();  // phase t-1
+                cluster_arrive();            // phase t
+            }
+        }
+        if (S > 1 && t > 0) cluster_wait();
+        // every copy issued has landed before the CTA can exit (bounded)
+        if (lane == 0) {
+            const uint32_t issued = i;
+            for (uint32_t r = issued > static_cast<uint32_t>(D) ? issued - D : 0u; r < issued; ++r)
+                (void)mbar_wait(fb + 8 * (r % D), static_cast<uint32_t>((r / D) & 1));
+        }
+        __syncwarp();
+        if (S > 1) cluster_sync();
+        return;
+    }
+
+    uint32_t i = 0;
+    for (uint32_t rb = cid, t = 0; rb < nblocks; rb += ncl, ++t) {
+        uint32_t b, row0;
+        block_origin(rb, b, row0);
+        const uint32_t wrow0 = row0 + static_cast<uint32_t>(warp * ROWS);
+        const bool wactive = wrow0 < a.n;
+        float2 acc[NR0][M];
+#pragma unroll
+        for (int r = 0; r < NR0; ++r)
+#pragma unroll
+            for (int j = 0; j < M; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
+        for (int q = 0; q < nck; ++q, ++i) {
+            const int st = static_cast<int>(i % D);
+            if (!failed &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, static_cast<uint32_t>((i / D) & 1))))
+                failed = true;
+            if (failed) continue;  // keep walking so every barrier below is still reached
+            if (wactive)
+                mv_chunk<WT, M, NR0>(smem + st * stage_bytes, wstage, warp, lane, c0 + static_cast<uint32_t>(q), a.k,
+                                     xs, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(eb + 8 * st);
+        }
+        mv_finish<M, NR0>(acc, failed, a, b, wrow0, wactive, true, lane, warp, s, S, t, parts, part_floats);
+    }
+    if (S > 1) cluster_sync();
 }
 
 }  // namespace dev

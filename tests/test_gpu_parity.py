@@ -136,25 +136,13 @@ def test_rows_bitwise_equal_for_every_m(fmt):
             assert np.array_equal(y[j].view(np.uint32), alone[j].view(np.uint32)), (m, j)
 
 
-def _rows_per_warp(fmt, m, rows_per_cta):
-    """Rows per warp the library picks (two per lane from m >= 4, except Q6_K)."""
-    nr0 = 2 if (m >= 4 and fmt != "q6_K") else 1
-    if rows_per_cta and rows_per_cta < 32 * nr0:
-        nr0 = 1
-    return 32 * nr0
-
-
 @pytest.mark.parametrize("fmt", FMTS)
 def test_rows_inert_to_packing_path_and_runs(fmt):
     n, k = 300, 2048
     w, x = H.contiguous(fmt, n, k, 8, 230, 330)
     split = 2
     base = H.run_matvec(w, fmt, n, k, 1, x, 8, k, 0, n, 0, 8 * n, split=split)
-    variants = []
-    for rpc in (32, 64, 128, 256):
-        if split * (rpc // _rows_per_warp(fmt, 8, rpc)) <= 8:
-            variants.append(dict(rows_per_cta=rpc))
-    assert len(variants) >= 2
+    variants = [dict(rows_per_cta=rpc) for rpc in (32, 64, 128, 256)]
     if fmt == "f16":
         variants.append(dict(w_offset=8))           # F16 needs 8-byte alignment: plain staging path
     elif fmt != "q4_K":                             # Q4_K requires 16-byte alignment
