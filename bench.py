@@ -299,26 +299,36 @@ def oracle_sample(fmt, n, k, batch, ms, grouped, ci, seconds: float):
 
     oracle.build()
     rows_total = batch * n
+    mmax = max(ms)
+    x = inputs.activations(mmax, k, 2000 + ci)
+    nbytes_per = lambda rows: sum(rows * oracle.row_bytes(fmt, k) + 4 * m * k + 4 * m * rows for m in ms)
 
-    def run(rows):
-        wf = inputs.weights(rows, k, 1000 + ci)
-        w = oracle.quantize(wf, fmt)
-        mmax = max(ms)
-        x = inputs.activations(mmax, k, 2000 + ci)
-        idx = np.arange(rows, dtype=np.uint64)
+    def prepare(rows):
+        w = oracle.quantize(inputs.weights(rows, k, 1000 + ci), fmt)
+        return w, np.arange(rows, dtype=np.uint64)
+
+    def sweep(w, idx, rows):
         t0 = time.perf_counter()
         for m in ms:
             oracle.matvec_rows(w, fmt, rows, k, x, m, k, 0, idx)
-        dt = time.perf_counter() - t0
-        nbytes = sum(rows * oracle.row_bytes(fmt, k) + 4 * m * k + 4 * m * rows for m in ms)
-        return dt, nbytes
+        return time.perf_counter() - t0
 
+    # grow the row sample until one sweep takes a measurable time, then
+    # repeat sweeps until about `seconds` of oracle work has been timed
     rows = min(rows_total, 64)
-    dt, nb = run(rows)
-    while dt < seconds / 4 and rows < rows_total:
+    w, idx = prepare(rows)
+    dt = sweep(w, idx, rows)
+    while dt < 0.5 and rows < rows_total:
         rows = min(rows_total, rows * 4)
-        dt, nb = run(rows)
-    return nb / dt / 1e9, oracle.threads(), f"{rows} of {rows_total} weight rows, m in {ms}, {dt:.2f} s"
+        w, idx = prepare(rows)
+        dt = sweep(w, idx, rows)
+    total, reps = dt, 1
+    while total < seconds:
+        total += sweep(w, idx, rows)
+        reps += 1
+    value = reps * nbytes_per(rows) / total / 1e9
+    return value, oracle.threads(), (f"{rows} of {rows_total} weight rows, m in {ms}, {reps} sweeps, "
+                                     f"{total:.2f} s")
 
 
 def run_reference(args):

@@ -114,6 +114,7 @@ struct DeviceState {
     int sms = 0;
     int smem_optin = 0;
     uint32_t cap_warps[kNumWt] = {0, 0, 0, 0, 0};  // largest power-of-two warps every kernel can launch
+    int max_threads[kNumWt][kMaxRows + 1][3] = {};  // per kernel <wt, m, nr0>
 };
 
 std::mutex g_mu;
@@ -139,6 +140,7 @@ int device_state(DeviceState** out) {
             for (int m = 1; m <= kMaxRows; ++m)
                 for (int nr0 = 1; nr0 <= 2; ++nr0) {
                     const void* fn = mv_kernel(wt, m, nr0);
+                    if (!fn) continue;  // NR0 = 2 exists for some m only
                     cudaFuncAttributes fa;
                     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess ||
                         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, st.smem_optin) !=
@@ -147,7 +149,8 @@ int device_state(DeviceState** out) {
                         return fail(REM_ECUDA, "rem_matvec: cannot prepare the %s kernels on device %d (%s)",
                                     wt_name(wt), dev, "no sm_103a image for this device?");
                     }
-                    if (fa.maxThreadsPerBlock < threads) threads = fa.maxThreadsPerBlock;
+                    st.max_threads[wt][m][nr0] = fa.maxThreadsPerBlock;
+                    if (nr0 == 1 && fa.maxThreadsPerBlock < threads) threads = fa.maxThreadsPerBlock;
                 }
             st.cap_warps[wt] = threads >= 32 ? pow2_floor(static_cast<uint32_t>(threads / 32)) : 0;
         }
@@ -315,38 +318,19 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     const uint32_t nchunk = (s.k + chunk_values(wt) - 1) / chunk_values(wt);
 
     Plan p{};
-    // two rows per lane share every input load from m >= 4: each broadcast
-    // of x from shared memory then feeds two rows (Q6_K keeps one row: its
-    // 53 staged words per row would not fit twice in registers)
-    p.nr0 = (s.m >= 4 && wt != kQ6_K) ? 2 : 1;
-    if (rows_per_cta) {
-        if (rows_per_cta < static_cast<uint32_t>(kLanes * p.nr0)) p.nr0 = 1;
-        p.warps = static_cast<int>(rows_per_cta / (kLanes * p.nr0));
-    } else {
-        // the widest row block (consumer warps per CTA) that still leaves at
-        // least two (row block, range) units per SM
-        p.warps = 1;
-        for (int g = 4; g >= 1; g /= 2) {
-            const uint64_t nb = static_cast<uint64_t>(s.batch) * ((s.n + kLanes * p.nr0 * g - 1) / (kLanes * p.nr0 * g));
-            if (nb * S >= 2ull * ds->sms || g == 1) {
-                p.warps = g;
-                break;
-            }
-        }
-    }
+    // Rows per lane: two rows share every input load from m >= 4 (kernels
+    // exist for those m), as long as the work still spreads over at least
+    // four warps per SM.
+    const uint64_t warps2 = static_cast<uint64_t>(s.batch) * ((s.n + 2 * kLanes - 1) / (2 * kLanes)) * S;
+    p.nr0 = (mv_kernel(wt, static_cast<int>(s.m), 2) != nullptr && warps2 >= 4ull * ds->sms) ? 2 : 1;
+    if (rows_per_cta && rows_per_cta < static_cast<uint32_t>(kLanes * p.nr0)) p.nr0 = 1;
     const uint32_t rows_per_warp = static_cast<uint32_t>(kLanes * p.nr0);
-    if (p.warps > static_cast<int>(ds->cap_warps[wt]) || p.warps > kMaxWarps)
-        return fail(REM_ELAUNCH, "rem_matvec: %d warps per block exceed the %s kernels' limit of %u", p.warps,
-                    wt_name(wt), ds->cap_warps[wt]);
-    p.cpb = (s.n + rows_per_warp * p.warps - 1) / (rows_per_warp * p.warps);
-    const uint64_t nblocks = static_cast<uint64_t>(p.cpb) * s.batch;
-    if (nblocks > 0x7FFFFFFFull)
-        return fail(REM_EINVAL, "rem_matvec: too many row blocks (%llu)", static_cast<unsigned long long>(nblocks));
     const void* fn = mv_kernel(wt, static_cast<int>(s.m), p.nr0);
-    const int threads = (p.warps + 1) * 32;
+    if (!fn) return fail(REM_ELAUNCH, "rem_matvec: no %s kernel for m %u", wt_name(wt), s.m);
 
-    // TMA descriptors: weights as [rows][row_bytes/2] u16, inputs as
-    // [batch][m][k] f32 with the caller's strides
+    // TMA staging needs 16-byte aligned rows and encodable tensor maps.
+    // Inputs: [batch][m][k] f32 with the caller's strides, dimensions ordered
+    // by increasing stride; either order stages the box as [m][chunk].
     alignas(64) CUtensorMap wmap, xmap;
     bool x_bm = false;
     std::memset(&wmap, 0, sizeof(wmap));
@@ -354,18 +338,6 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     p.aligned = reinterpret_cast<uintptr_t>(W) % 16 == 0 && rb % 16 == 0 && rows < (1ull << 31) &&
                 rb / 2 < (1ull << 32) && driver().encode != nullptr;
     if (p.aligned) {
-        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rb / 2), static_cast<cuuint64_t>(rows)};
-        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rb)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(chunk_box(wt) / 2), rows_per_warp * p.warps};
-        const cuuint32_t estride[2] = {1, 1};
-        p.aligned = driver().encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), gdim, gstride,
-                                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    }
-    if (p.aligned) {
-        // dimensions ordered by increasing stride; either order stages the
-        // box as [m][chunk] in shared memory
         const uint64_t xrs = s.m == 1 ? s.k : s.xrs;
         const uint64_t xbs = s.batch == 1 ? xrs * s.m : s.xbs;
         x_bm = xbs < xrs;
@@ -380,32 +352,12 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
 
-    // stages: the deepest ring (<= 4) that keeps two blocks per SM, else the
-    // deepest that fits at all
-    if (!p.aligned) {
-        p.stages = 1;
-    } else {
-        int best = 0;
-        for (int d = kMaxStages; d >= 1; --d) {
-            const int sm = static_cast<int>(mv_smem_bytes(wt, p.nr0, p.warps, d, static_cast<int>(s.m), S));
-            if (sm > ds->smem_optin) continue;
-            if (!best) best = d;
-            if (blocks_per_sm(fn, threads, sm) >= 2) {
-                best = d;
-                break;
-            }
-        }
-        p.stages = best ? best : 1;
-    }
-    p.smem = static_cast<int>(mv_smem_bytes(wt, p.nr0, p.warps, p.stages, static_cast<int>(s.m), S));
-    if (p.smem > ds->smem_optin)
-        return fail(REM_ELAUNCH, "rem_matvec: needs %d bytes of shared memory, the device allows %d", p.smem,
-                    ds->smem_optin);
-
-    // persistent grid: as many clusters as can be resident, at most one per row block
+    // Row-block width G (consumer warps per CTA) and ring depth D: the pair
+    // with the best score among those that fit.  Small m is bound by the
+    // bytes in flight per SM (up to ~96 KB), larger m by the warps that can
+    // issue decode and FMA work; both are scaled by the share of resident
+    // CTA slots the last wave of row blocks keeps busy.
     cudaLaunchConfig_t cfg{};
-    cfg.blockDim = dim3(static_cast<unsigned>(threads));
-    cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     if (S > 1) {
@@ -416,6 +368,68 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
+    double best = -1.0;
+    for (int g = kMaxWarps; g >= 1; g /= 2) {
+        if (rows_per_cta ? static_cast<uint32_t>(g) * rows_per_warp != rows_per_cta
+                         : (g > 4 || static_cast<uint32_t>(g) * rows_per_warp > 256u))
+            continue;
+        if ((g + 1) * 32 > ds->max_threads[wt][s.m][p.nr0]) {
+            if (!rows_per_cta) continue;
+            return fail(REM_ELAUNCH, "rem_matvec: %d warps per block exceed the %s kernel's limit of %d threads",
+                        g + 1, wt_name(wt), ds->max_threads[wt][s.m][p.nr0]);
+        }
+        const uint64_t nb = static_cast<uint64_t>(s.batch) * ((s.n + rows_per_warp * g - 1) / (rows_per_warp * g));
+        const uint64_t units = nb * S;
+        const uint64_t per_cta = ((nchunk + S - 1) / S) * ((units + 2ull * ds->sms - 1) / (2ull * ds->sms));
+        const int dmax = static_cast<int>(std::min<uint64_t>(kMaxStages, std::max<uint64_t>(2, per_cta)));
+        for (int d = 1; d <= dmax; ++d) {
+            const int sm = static_cast<int>(mv_smem_bytes(wt, p.nr0, g, d, static_cast<int>(s.m), S));
+            if (sm > ds->smem_optin) continue;
+            cfg.blockDim = dim3(static_cast<unsigned>((g + 1) * 32));
+            cfg.dynamicSmemBytes = static_cast<size_t>(sm);
+            const uint64_t slots = resident_clusters(fn, cfg, S, ds->sms) * S;
+            if (slots == 0) continue;
+            const uint64_t ctas = std::min(units, slots);
+            const uint64_t waves = (units + ctas - 1) / ctas;
+            const double eff = static_cast<double>(units) / static_cast<double>(waves * ctas);
+            const double per_sm = static_cast<double>(ctas) / ds->sms;
+            const double warps_sm = per_sm * g;
+            const double inflight =
+                per_sm * d * static_cast<double>(mv_stage_bytes(wt, p.nr0, g, static_cast<int>(s.m)));
+            double score = s.m <= 2 ? std::min(inflight, 98304.0) * 1e-3 + warps_sm + 0.01 * g
+                                    : warps_sm * (d >= 2 ? 1.0 : 0.75) + 0.05 * d;
+            score *= eff;
+            if (score > best) {
+                best = score;
+                p.warps = g;
+                p.stages = d;
+                p.smem = sm;
+            }
+        }
+    }
+    if (best < 0)
+        return fail(REM_ELAUNCH, "rem_matvec: no %s block of %u rows fits the device's shared memory",
+                    wt_name(wt), rows_per_cta ? rows_per_cta : rows_per_warp);
+    p.cpb = (s.n + rows_per_warp * p.warps - 1) / (rows_per_warp * p.warps);
+    const uint64_t nblocks = static_cast<uint64_t>(p.cpb) * s.batch;
+    if (nblocks > 0x7FFFFFFFull)
+        return fail(REM_EINVAL, "rem_matvec: too many row blocks (%llu)", static_cast<unsigned long long>(nblocks));
+    const int threads = (p.warps + 1) * 32;
+    if (p.aligned) {
+        // weights as [rows][row_bytes/2] u16, one box = the row block's rows x one chunk
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rb / 2), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rb)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(chunk_box(wt) / 2), rows_per_warp * p.warps};
+        const cuuint32_t estride[2] = {1, 1};
+        p.aligned = driver().encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), gdim, gstride,
+                                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+
+    // persistent grid: as many clusters as can be resident, at most one per row block
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
     const uint64_t resident = resident_clusters(fn, cfg, S, ds->sms);
     if (resident == 0)
         return fail(REM_ELAUNCH, "rem_matvec: a cluster of %u blocks of %d threads and %d bytes does not fit",

@@ -96,10 +96,6 @@ __device__ __forceinline__ uint4 lds16(const uint8_t* p) {
     return *reinterpret_cast<const uint4*>(p);
 }
 
-__device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -193,25 +189,52 @@ template <> struct Stage<kQ6_K> {
 
 // ---------------------------------------------------------------- decoders
 
-// Q8_0 block B of a staged chunk (34 B at byte 34*B of a 16-aligned row).
-// Yields the scale and the 16 code pairs as exact floats.
+// lop3: (a & b) | c
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// lop3: bitwise b ? (a ^ c) : c -- the bits of a under mask b with c's bits
+// flipped, c elsewhere
+__device__ __forceinline__ uint32_t lop_sel_xor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// lop3: bitwise c ? a : b
+__device__ __forceinline__ uint32_t lop_sel(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Bytes 0 and 1 of v as two exact floats: the bits under masks m0 (within
+// bits 0..7) and m1 (within bits 8..15) become mantissa bits under the
+// exponents 2^23 and 2^15, then `bias` removes 2^23 (2^15) and the code offset.
+__device__ __forceinline__ float2 bytes01_u(uint32_t v, uint32_t m0, uint32_t m1, float2 bias) {
+    return add2(make_float2(fbits(lop_and_or(v, m0, 0x4B000000u)), fbits(lop_and_or(v, m1, 0x47000000u))), bias);
+}
+// Bytes 0 and 1 of v read as int8: the sign bit is flipped on the way in
+// (q + 128 in 0..255), and the bias removes 2^23 + 128 (2^15 + 128).
+__device__ __forceinline__ float2 bytes01_s(uint32_t v) {
+    return add2(make_float2(fbits(lop_sel_xor(v, 0xFFu, 0x4B000080u)), fbits(lop_sel_xor(v, 0xFF00u, 0x47008000u))),
+                make_float2(-8388736.0f, -32896.0f));
+}
+
+// Byte b (0..3) of w, masked to `mask` (0x3F or 0xFF), as an exact float.
 template <int B>
-__device__ __forceinline__ void dec_q8_0(const uint8_t* row, float& d, float2 (&w)[16]) {
-    constexpr int off = 34 * B, p0 = off >> 4, bo = off & 15;
-    const uint4 v0 = lds16(row + 16 * p0), v1 = lds16(row + 16 * (p0 + 1)), v2 = lds16(row + 16 * (p0 + 2));
-    const uint32_t W[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
-    const uint32_t dw = W[bo >> 2];
-    d = h2f((bo & 2) ? (dw >> 16) : dw);
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-        const int pos = bo + 2 + 2 * p;
-        uint32_t v = W[pos >> 2];
-        if (pos & 2) v >>= 16;
-        // bytes biased by 128 (q + 128 in 0..255) under exponents 2^23, 2^15
-        const float f0 = fbits(((v ^ 0x80u) & 0xFFu) | 0x4B000000u);
-        const float f1 = fbits(((v ^ 0x8000u) & 0xFF00u) | 0x47000000u);
-        w[p] = add2(make_float2(f0, f1), make_float2(-8388736.0f, -32896.0f));
-    }
+__device__ __forceinline__ float ubyte_f(uint32_t w, uint32_t mask) {
+    const uint32_t v = B >= 2 ? (w >> 16) : w;
+    if constexpr ((B & 1) == 0) return fbits(lop_and_or(v, mask, 0x4B000000u)) - 8388608.0f;
+    else return fbits(lop_and_or(v, mask << 8, 0x47000000u)) - 32768.0f;
+}
+// Byte b (0..3) of w read as int8, as an exact float.
+template <int B>
+__device__ __forceinline__ float sbyte_f(uint32_t w) {
+    const uint32_t v = B >= 2 ? (w >> 16) : w;
+    if constexpr ((B & 1) == 0) return fbits(lop_sel_xor(v, 0xFFu, 0x4B000080u)) - 8388736.0f;
+    else return fbits(lop_sel_xor(v, 0xFF00u, 0x47008000u)) - 32896.0f;
 }
 
 // 32-bit little-endian word at an even byte position of a word array.
@@ -227,64 +250,80 @@ __device__ __forceinline__ uint32_t u32_at(const uint32_t (&W)[N]) {
 // Spread the 4 low bits of h to bit 4 of each byte (bit k -> bit 8k+4).
 __device__ __forceinline__ uint32_t spread4(uint32_t h) { return (h * 0x02040810u) & 0x10101010u; }
 
-// Q5_0 block B (22 B at byte 22*B of a 16-aligned row).
+// A 32-value block of a staged chunk: load() takes its bytes from shared
+// memory, group<Q>() yields values 4Q..4Q+3 as two pairs (decoded when the
+// chain needs them, so only the block's raw words stay in registers).
+//
+// Q8_0 block B: 34 B at byte 34*B of a 16-aligned staged row; d, then 32 int8.
 template <int B>
-__device__ __forceinline__ void dec_q5_0(const uint8_t* row, float& d, float2 (&w)[16]) {
-    constexpr int off = 22 * B, p0 = off >> 4, bo = off & 15;
-    const uint4 v0 = lds16(row + 16 * p0), v1 = lds16(row + 16 * (p0 + 1));
-    uint4 v2 = make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (bo + 22 > 32) v2 = lds16(row + 16 * (p0 + 2));
-    const uint32_t W[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
-    const uint32_t dw = W[bo >> 2];
-    d = h2f((bo & 2) ? (dw >> 16) : dw);
-    const uint32_t qh = u32_at<bo + 2>(W);
-    const uint32_t qs[4] = {u32_at<bo + 6>(W), u32_at<bo + 10>(W), u32_at<bo + 14>(W), u32_at<bo + 18>(W)};
-    const float2 bias = make_float2(-8388624.0f, -32784.0f);  // 2^23 + 16, 2^15 + 16
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        // elements 4g..4g+3: low nibbles; elements 16+4g..: high nibbles
-        const uint32_t lo = (qs[g] & 0x0F0F0F0Fu) | spread4((qh >> (4 * g)) & 0xFu);
-        const uint32_t hi = ((qs[g] >> 4) & 0x0F0F0F0Fu) | spread4((qh >> (16 + 4 * g)) & 0xFu);
-        const uint32_t lo2 = lo >> 16, hi2 = hi >> 16;
-        w[2 * g] = add2(make_float2(fbits((lo & 0xFFu) | 0x4B000000u), fbits((lo & 0xFF00u) | 0x47000000u)), bias);
-        w[2 * g + 1] = add2(make_float2(fbits((lo2 & 0xFFu) | 0x4B000000u), fbits((lo2 & 0xFF00u) | 0x47000000u)), bias);
-        w[8 + 2 * g] = add2(make_float2(fbits((hi & 0xFFu) | 0x4B000000u), fbits((hi & 0xFF00u) | 0x47000000u)), bias);
-        w[9 + 2 * g] = add2(make_float2(fbits((hi2 & 0xFFu) | 0x4B000000u), fbits((hi2 & 0xFF00u) | 0x47000000u)), bias);
+struct BlkQ8 {
+    static constexpr int off = 34 * B, p0 = off >> 4, bo = off & 15;
+    uint32_t W[12];
+    float d;
+    __device__ __forceinline__ void load(const uint8_t* row) {
+        const uint4 v0 = lds16(row + 16 * p0), v1 = lds16(row + 16 * (p0 + 1)), v2 = lds16(row + 16 * (p0 + 2));
+        W[0] = v0.x; W[1] = v0.y; W[2] = v0.z; W[3] = v0.w;
+        W[4] = v1.x; W[5] = v1.y; W[6] = v1.z; W[7] = v1.w;
+        W[8] = v2.x; W[9] = v2.y; W[10] = v2.z; W[11] = v2.w;
+        const uint32_t dw = W[bo >> 2];
+        d = h2f((bo & 2) ? (dw >> 16) : dw);
     }
-}
+    template <int Q>
+    __device__ __forceinline__ void group(float2& w01, float2& w23) const {
+        const uint32_t v = u32_at<bo + 2 + 4 * Q>(W);
+        w01 = bytes01_s(v);
+        w23 = bytes01_s(v >> 16);
+    }
+};
 
-// Q4_K: 16 value pairs of sub-block 2c+H from the 8 qs words of chunk c.
-// Low nibbles (H = 0) sit at bits 0, 8, 16 and (after >> 12) 12;
-// high nibbles (H = 1) at bits 4, 12 and (after >> 12) 8, 16.
+// Q5_0 block B: 22 B at byte 22*B; d, qh (bit e = bit 4 of element e), then
+// 16 bytes whose low nibbles are elements 0..15 and high nibbles 16..31.
+template <int B>
+struct BlkQ5 {
+    static constexpr int off = 22 * B, p0 = off >> 4, bo = off & 15;
+    uint32_t qs[4];
+    uint32_t qh;
+    float d;
+    __device__ __forceinline__ void load(const uint8_t* row) {
+        const uint4 v0 = lds16(row + 16 * p0), v1 = lds16(row + 16 * (p0 + 1));
+        uint4 v2 = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (bo + 22 > 32) v2 = lds16(row + 16 * (p0 + 2));
+        const uint32_t W[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
+        const uint32_t dw = W[bo >> 2];
+        d = h2f((bo & 2) ? (dw >> 16) : dw);
+        qh = u32_at<bo + 2>(W);
+        qs[0] = u32_at<bo + 6>(W);
+        qs[1] = u32_at<bo + 10>(W);
+        qs[2] = u32_at<bo + 14>(W);
+        qs[3] = u32_at<bo + 18>(W);
+    }
+    template <int Q>
+    __device__ __forceinline__ void group(float2& w01, float2& w23) const {
+        const uint32_t nib = Q < 4 ? qs[Q & 3] : (qs[Q & 3] >> 4);
+        const uint32_t v = lop_and_or(nib, 0x0F0F0F0Fu, spread4((qh >> (4 * Q)) & 0xFu));
+        const float2 bias = make_float2(-8388624.0f, -32784.0f);  // 2^23 + 16, 2^15 + 16
+        w01 = bytes01_u(v, 0xFFu, 0xFF00u, bias);
+        w23 = bytes01_u(v >> 16, 0xFFu, 0xFF00u, bias);
+    }
+};
+
+// Q4_K: values 4Q..4Q+3 of sub-block 2c+H from qs word v = bytes 4Q..4Q+3
+// of the chunk's 32 bytes.  Low nibbles (H = 0) sit at bits 0, 8, 16, 24;
+// high nibbles (H = 1) at 4, 12, 20, 28.  A nibble at bit p is read under
+// the exponent 2^(23-p); bits 20..31 go through v >> 12 first.
 template <int H>
-__device__ __forceinline__ void dec_q4_k_sub(const uint32_t (&q)[8], float2 (&w)[16]) {
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-        const uint32_t v = q[g], s = v >> 12;
-        if constexpr (H == 0) {
-            w[2 * g] = add2(make_float2(fbits((v & 0xFu) | 0x4B000000u), fbits((v & 0xF00u) | 0x47000000u)),
-                            make_float2(-8388608.0f, -32768.0f));
-            w[2 * g + 1] = add2(make_float2(fbits((v & 0xF0000u) | 0x43000000u), fbits((s & 0xF000u) | 0x45000000u)),
-                                make_float2(-128.0f, -2048.0f));
-        } else {
-            w[2 * g] = add2(make_float2(fbits((v & 0xF0u) | 0x49000000u), fbits((v & 0xF000u) | 0x45000000u)),
-                            make_float2(-524288.0f, -2048.0f));
-            w[2 * g + 1] = add2(make_float2(fbits((s & 0xF00u) | 0x47000000u), fbits((s & 0xF0000u) | 0x43000000u)),
-                                make_float2(-32768.0f, -128.0f));
-        }
-    }
-}
-
-// 6-bit scale / min of Q4_K sub-block s from the 12 scale bytes (words s0, s1, s2).
-__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int s, uint32_t& sc,
-                                              uint32_t& mn) {
-    if (s < 4) {
-        sc = (s0 >> (8 * s)) & 63u;
-        mn = (s1 >> (8 * s)) & 63u;
+__device__ __forceinline__ void q4k_group(uint32_t v, float2& w01, float2& w23) {
+    const uint32_t s = v >> 12;
+    if constexpr (H == 0) {
+        w01 = add2(make_float2(fbits(lop_and_or(v, 0xFu, 0x4B000000u)), fbits(lop_and_or(v, 0xF00u, 0x47000000u))),
+                   make_float2(-8388608.0f, -32768.0f));
+        w23 = add2(make_float2(fbits(lop_and_or(v, 0xF0000u, 0x43000000u)), fbits(lop_and_or(s, 0xF000u, 0x45000000u))),
+                   make_float2(-128.0f, -2048.0f));
     } else {
-        const uint32_t b8 = (s2 >> (8 * (s - 4))) & 0xFFu;
-        sc = (b8 & 0xFu) | (((s0 >> (8 * (s - 4) + 6)) & 3u) << 4);
-        mn = (b8 >> 4) | (((s1 >> (8 * (s - 4) + 6)) & 3u) << 4);
+        w01 = add2(make_float2(fbits(lop_and_or(v, 0xF0u, 0x49000000u)), fbits(lop_and_or(v, 0xF000u, 0x45000000u))),
+                   make_float2(-524288.0f, -2048.0f));
+        w23 = add2(make_float2(fbits(lop_and_or(s, 0xF00u, 0x47000000u)), fbits(lop_and_or(s, 0xF0000u, 0x43000000u))),
+                   make_float2(-32768.0f, -128.0f));
     }
 }
 
@@ -323,6 +362,23 @@ __device__ __forceinline__ void q6_load(const uint8_t* row, int o, uint32_t (&wd
     }
 }
 
+// Q6_K: values l = 4G..4G+3 of quarter T of half H (elements 128H + 32T + l).
+// Low nibbles come from ql word 16H + 8(T&1) + G (the low nibble for T < 2,
+// the high one for T >= 2), the two high bits from bits 2T, 2T+1 of qh word
+// 32 + 8H + G; one select puts them at bits 4..5 of each byte, and the 0x3F
+// masks drop the unused bits 6..7.
+template <int H, int T, int G>
+__device__ __forceinline__ void q6k_group(const uint32_t (&wd)[53], float2& w01, float2& w23) {
+    const uint32_t ql = wd[16 * H + 8 * (T & 1) + G];
+    const uint32_t qh = wd[32 + 8 * H + G];
+    const uint32_t lo = T < 2 ? ql : (ql >> 4);
+    const uint32_t hi = T == 0 ? (qh << 4) : T == 1 ? (qh << 2) : T == 2 ? qh : (qh >> 2);
+    const uint32_t v = lop_sel(lo, hi, 0x0F0F0F0Fu);
+    const float2 bias = make_float2(-8388640.0f, -32800.0f);  // 2^23 + 32, 2^15 + 32
+    w01 = bytes01_u(v, 0x3Fu, 0x3F00u, bias);
+    w23 = bytes01_u(v >> 16, 0x3Fu, 0x3F00u, bias);
+}
+
 // ---------------------------------------------------------------- chunk bodies
 
 // Accumulator update of one block/sub-block chain c with scale a.
@@ -335,32 +391,38 @@ __device__ __forceinline__ void apply_scale(float2 (&acc)[NR0][M], const float2 
         for (int j = 0; j < M; ++j) acc[i][j] = fma2(make_float2(a[i], a[i]), c[i][j], acc[i][j]);
 }
 
-// Chain over 16 pairs with inputs x[j][0..31] (32 consecutive floats).
-template <int M, int NR0>
-__device__ __forceinline__ void chain32(float2 (&c)[NR0][M], const float2 (&w)[NR0][16], const float* xu,
-                                        uint32_t xrs) {
+// The chain of one block / sub-block of 4*NG values: for each group Q of 4
+// values, gen(Q, i, w01, w23) yields row i's values 4Q..4Q+3 and the chain
+// takes c = fma2(w01, x[4Q..4Q+1], c), c = fma2(w23, x[4Q+2..4Q+3], c).
+// Input row j of the group sits at xu + j*XS + 4Q in shared memory.  Only the
+// group's decoded values and one input quad are live at a time.
+template <int M, int NR0, int NG, int XS, typename Gen>
+__device__ __forceinline__ void chain(float2 (&c)[NR0][M], const float* xu, Gen&& gen) {
 #pragma unroll
     for (int i = 0; i < NR0; ++i)
 #pragma unroll
         for (int j = 0; j < M; ++j) c[i][j] = make_float2(0.0f, 0.0f);
+    static_for<0, NG>([&](auto qc) {
+        constexpr int Q = decltype(qc)::value;
+        float2 w01[NR0], w23[NR0];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        float4 xv[M];
+        for (int i = 0; i < NR0; ++i) gen(qc, i, w01[i], w23[i]);
 #pragma unroll
-        for (int j = 0; j < M; ++j) xv[j] = ldx4(xu + j * xrs + 4 * q);
+        for (int j = 0; j < M; ++j) {
+            const float4 xv = ldx4(xu + j * XS + 4 * Q);
 #pragma unroll
-        for (int i = 0; i < NR0; ++i)
-#pragma unroll
-            for (int j = 0; j < M; ++j) {
-                c[i][j] = fma2(w[i][2 * q], make_float2(xv[j].x, xv[j].y), c[i][j]);
-                c[i][j] = fma2(w[i][2 * q + 1], make_float2(xv[j].z, xv[j].w), c[i][j]);
+            for (int i = 0; i < NR0; ++i) {
+                c[i][j] = fma2(w01[i], make_float2(xv.x, xv.y), c[i][j]);
+                c[i][j] = fma2(w23[i], make_float2(xv.z, xv.w), c[i][j]);
             }
-    }
+        }
+    });
 }
 
-template <int M, int NR0, bool FULL>
-__device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], const float* xc, uint32_t xrs,
-                                          int nvals, float2 (&acc)[NR0][M]) {
+// F16 chunk of 136 values (a zero-filled tail past k adds exact zeros).
+template <int M, int NR0>
+__device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], const float* xc,
+                                          float2 (&acc)[NR0][M]) {
     float2 c[NR0][M];
 #pragma unroll
     for (int i = 0; i < NR0; ++i)
@@ -368,29 +430,25 @@ __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], con
         for (int j = 0; j < M; ++j) c[i][j] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int g = 0; g < 17; ++g) {  // 8 values per step
-        if (!FULL && 8 * g >= nvals) break;
-        const bool second = FULL || (8 * g + 4 < nvals);
-        float4 xa[M], xb[M];
-#pragma unroll
-        for (int j = 0; j < M; ++j) {
-            xa[j] = ldx4(xc + j * xrs + 8 * g);
-            xb[j] = second ? ldx4(xc + j * xrs + 8 * g + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        float2 p[NR0][4];
 #pragma unroll
         for (int i = 0; i < NR0; ++i) {
             const uint4 h = lds16(rows[i] + 16 * g);
-            const float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-            const float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-            const float2 p2 = __half22float2(*reinterpret_cast<const __half2*>(&h.z));
-            const float2 p3 = __half22float2(*reinterpret_cast<const __half2*>(&h.w));
+            p[i][0] = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+            p[i][1] = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+            p[i][2] = __half22float2(*reinterpret_cast<const __half2*>(&h.z));
+            p[i][3] = __half22float2(*reinterpret_cast<const __half2*>(&h.w));
+        }
 #pragma unroll
-            for (int j = 0; j < M; ++j) {
-                c[i][j] = fma2(p0, make_float2(xa[j].x, xa[j].y), c[i][j]);
-                c[i][j] = fma2(p1, make_float2(xa[j].z, xa[j].w), c[i][j]);
-                if (second) {
-                    c[i][j] = fma2(p2, make_float2(xb[j].x, xb[j].y), c[i][j]);
-                    c[i][j] = fma2(p3, make_float2(xb[j].z, xb[j].w), c[i][j]);
-                }
+        for (int j = 0; j < M; ++j) {
+            const float4 xa = ldx4(xc + j * 136 + 8 * g);
+            const float4 xb = ldx4(xc + j * 136 + 8 * g + 4);
+#pragma unroll
+            for (int i = 0; i < NR0; ++i) {
+                c[i][j] = fma2(p[i][0], make_float2(xa.x, xa.y), c[i][j]);
+                c[i][j] = fma2(p[i][1], make_float2(xa.z, xa.w), c[i][j]);
+                c[i][j] = fma2(p[i][2], make_float2(xb.x, xb.y), c[i][j]);
+                c[i][j] = fma2(p[i][3], make_float2(xb.z, xb.w), c[i][j]);
             }
         }
     }
@@ -400,56 +458,50 @@ __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], con
         for (int j = 0; j < M; ++j) acc[i][j] = add2(acc[i][j], c[i][j]);
 }
 
-template <int M, int NR0, bool FULL>
-__device__ __forceinline__ void chunk_q8_0(const uint8_t* const (&rows)[NR0], const float* xc, uint32_t xrs,
-                                           int nblk, float2 (&acc)[NR0][M]) {
+// Eight 32-value blocks (Q8_0 or Q5_0) of one staged chunk.  Blocks past k
+// are zero-filled (scale 0, inputs 0) and add exact zeros.
+template <int M, int NR0, template <int> class Blk>
+__device__ __forceinline__ void chunk_blocks32(const uint8_t* const (&rows)[NR0], const float* xc,
+                                               float2 (&acc)[NR0][M]) {
     static_for<0, 8>([&](auto bc) {
         constexpr int B = decltype(bc)::value;
-        if (!FULL && B >= nblk) return;
+        Blk<B> blk[NR0];
         float d[NR0];
-        float2 w[NR0][16];
 #pragma unroll
-        for (int i = 0; i < NR0; ++i) dec_q8_0<B>(rows[i], d[i], w[i]);
+        for (int i = 0; i < NR0; ++i) {
+            blk[i].load(rows[i]);
+            d[i] = blk[i].d;
+        }
         float2 c[NR0][M];
-        chain32<M, NR0>(c, w, xc + 32 * B, xrs);
-        apply_scale<M, NR0>(acc, c, d);
-    });
-}
-
-template <int M, int NR0, bool FULL>
-__device__ __forceinline__ void chunk_q5_0(const uint8_t* const (&rows)[NR0], const float* xc, uint32_t xrs,
-                                           int nblk, float2 (&acc)[NR0][M]) {
-    static_for<0, 8>([&](auto bc) {
-        constexpr int B = decltype(bc)::value;
-        if (!FULL && B >= nblk) return;
-        float d[NR0];
-        float2 w[NR0][16];
-#pragma unroll
-        for (int i = 0; i < NR0; ++i) dec_q5_0<B>(rows[i], d[i], w[i]);
-        float2 c[NR0][M];
-        chain32<M, NR0>(c, w, xc + 32 * B, xrs);
+        chain<M, NR0, 8, 256>(c, xc + 32 * B, [&](auto qc, int i, float2& w01, float2& w23) {
+            blk[i].template group<decltype(qc)::value>(w01, w23);
+        });
         apply_scale<M, NR0>(acc, c, d);
     });
 }
 
 // Q4_K super-block.  xs[u*M + j] = sum of the 32 inputs of sub-block u for
-// input row j (computed once per chunk for the CTA, see xsum_q4_k).
+// input row j (computed once per chunk for the warp, see xsum_q4_k).
+// Sub-block scales and mins: s < 4 from bytes s of scales[0..3] / [4..7];
+// s >= 4 joins the low (high) nibble of scales[s+4] with the top two bits of
+// scales[s-4] (scales[s]) -- one select per word.
 template <int M, int NR0>
-__device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], const float* xc, uint32_t xrs,
-                                           const float* xs, float2 (&acc)[NR0][M]) {
+__device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], const float* xc, const float* xs,
+                                           float2 (&acc)[NR0][M]) {
     float d[NR0], dmin[NR0];
-    uint32_t s0[NR0], s1[NR0], s2[NR0];
+    uint32_t scw[NR0][2], mnw[NR0][2];
 #pragma unroll
     for (int i = 0; i < NR0; ++i) {
         const uint4 h = lds16(rows[i]);
         d[i] = h2f(h.x);
         dmin[i] = h2f(h.x >> 16);
-        s0[i] = h.y;
-        s1[i] = h.z;
-        s2[i] = h.w;
+        scw[i][0] = h.y;
+        mnw[i][0] = h.z;
+        scw[i][1] = lop_sel(h.w, h.y >> 2, 0x0F0F0F0Fu);
+        mnw[i][1] = lop_sel(h.w >> 4, h.z >> 2, 0x0F0F0F0Fu);
     }
-#pragma unroll
-    for (int cq = 0; cq < 4; ++cq) {
+    static_for<0, 4>([&](auto cqc) {
+        constexpr int cq = decltype(cqc)::value;
         uint32_t q[NR0][8];
 #pragma unroll
         for (int i = 0; i < NR0; ++i) {
@@ -457,28 +509,26 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
             q[i][0] = a.x; q[i][1] = a.y; q[i][2] = a.z; q[i][3] = a.w;
             q[i][4] = b.x; q[i][5] = b.y; q[i][6] = b.z; q[i][7] = b.w;
         }
-#pragma unroll
-        for (int H = 0; H < 2; ++H) {
-            const int u = 2 * cq + H;
+        static_for<0, 2>([&](auto hc) {
+            constexpr int H = decltype(hc)::value;
+            constexpr int u = 2 * cq + H;
             float sc[NR0], mnv[NR0];
-            float2 w[NR0][16];
 #pragma unroll
             for (int i = 0; i < NR0; ++i) {
-                uint32_t scu, mnu;
-                q4k_scale_min(s0[i], s1[i], s2[i], u, scu, mnu);
-                sc[i] = __fmul_rn(d[i], static_cast<float>(scu));
-                mnv[i] = __fmul_rn(dmin[i], static_cast<float>(mnu));
-                if (H == 0) dec_q4_k_sub<0>(q[i], w[i]); else dec_q4_k_sub<1>(q[i], w[i]);
+                sc[i] = __fmul_rn(d[i], ubyte_f<u & 3>(scw[i][u >> 2], 0x3Fu));
+                mnv[i] = __fmul_rn(dmin[i], ubyte_f<u & 3>(mnw[i][u >> 2], 0x3Fu));
             }
             float2 c[NR0][M];
-            chain32<M, NR0>(c, w, xc + 32 * u, xrs);
+            chain<M, NR0, 8, 256>(c, xc + 32 * u, [&](auto qc, int i, float2& w01, float2& w23) {
+                q4k_group<H>(q[i][decltype(qc)::value], w01, w23);
+            });
             apply_scale<M, NR0>(acc, c, sc);
 #pragma unroll
             for (int i = 0; i < NR0; ++i)
 #pragma unroll
                 for (int j = 0; j < M; ++j) acc[i][j].x = __fmaf_rn(-mnv[i], xs[u * M + j], acc[i][j].x);
-        }
-    }
+        });
+    });
 }
 
 // Sub-block input sums of one Q4_K chunk, per warp: lane (u = lane/4,
@@ -500,10 +550,11 @@ __device__ __forceinline__ void xsum_q4_k(const float* xc, float* xs, int lane) 
     }
 }
 
-// Q6_K super-block staged at byte o of each row.
+// Q6_K super-block staged at byte o of each row: 16 sub-blocks of 16
+// values, u = 8h + 2t + gh, each its own chain scaled by d * sc[u].
 template <int M, int NR0>
-__device__ __forceinline__ void chunk_q6_k(const uint8_t* const (&rows)[NR0], const float* xc, uint32_t xrs,
-                                           int o, float2 (&acc)[NR0][M]) {
+__device__ __forceinline__ void chunk_q6_k(const uint8_t* const (&rows)[NR0], const float* xc, int o,
+                                           float2 (&acc)[NR0][M]) {
     uint32_t wd[NR0][53];
     float d[NR0];
 #pragma unroll
@@ -511,64 +562,27 @@ __device__ __forceinline__ void chunk_q6_k(const uint8_t* const (&rows)[NR0], co
         q6_load(rows[i], o, wd[i]);
         d[i] = h2f(wd[i][52]);
     }
-    const float2 bias = make_float2(-8388640.0f, -32800.0f);  // 2^23 + 32, 2^15 + 32
+    static_for<0, 16>([&](auto uc) {
+        constexpr int u = decltype(uc)::value;
+        constexpr int h = u >> 3, t = (u >> 1) & 3, gh = u & 1;
+        float a[NR0];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-#pragma unroll
-            for (int gh = 0; gh < 2; ++gh) {
-                const int u = 8 * h + 2 * t + gh;  // sub-block of 16 values
-                float a[NR0];
-                float2 w[NR0][8];
-#pragma unroll
-                for (int i = 0; i < NR0; ++i) {
-                    const int scb = static_cast<int>(static_cast<int8_t>((wd[i][48 + (u >> 2)] >> (8 * (u & 3))) & 0xFFu));
-                    a[i] = __fmul_rn(d[i], static_cast<float>(scb));
-#pragma unroll
-                    for (int g4 = 0; g4 < 4; ++g4) {
-                        const int g = 4 * gh + g4;
-                        const uint32_t ql = wd[i][16 * h + 8 * (t & 1) + g];
-                        const uint32_t qh = wd[i][32 + 8 * h + g];
-                        const uint32_t lo = (t < 2 ? ql : (ql >> 4)) & 0x0F0F0F0Fu;
-                        uint32_t hi;
-                        if (t == 0) hi = (qh << 4) & 0x30303030u;
-                        else if (t == 1) hi = (qh << 2) & 0x30303030u;
-                        else if (t == 2) hi = qh & 0x30303030u;
-                        else hi = (qh >> 2) & 0x30303030u;
-                        const uint32_t v = lo | hi, v2 = v >> 16;
-                        w[i][2 * g4] = add2(make_float2(fbits((v & 0xFFu) | 0x4B000000u), fbits((v & 0xFF00u) | 0x47000000u)), bias);
-                        w[i][2 * g4 + 1] = add2(make_float2(fbits((v2 & 0xFFu) | 0x4B000000u), fbits((v2 & 0xFF00u) | 0x47000000u)), bias);
-                    }
-                }
-                float2 c[NR0][M];
-#pragma unroll
-                for (int i = 0; i < NR0; ++i)
-#pragma unroll
-                    for (int j = 0; j < M; ++j) c[i][j] = make_float2(0.0f, 0.0f);
-                const float* xu = xc + 128 * h + 32 * t + 16 * gh;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float4 xv[M];
-#pragma unroll
-                    for (int j = 0; j < M; ++j) xv[j] = ldx4(xu + j * xrs + 4 * q);
-#pragma unroll
-                    for (int i = 0; i < NR0; ++i)
-#pragma unroll
-                        for (int j = 0; j < M; ++j) {
-                            c[i][j] = fma2(w[i][2 * q], make_float2(xv[j].x, xv[j].y), c[i][j]);
-                            c[i][j] = fma2(w[i][2 * q + 1], make_float2(xv[j].z, xv[j].w), c[i][j]);
-                        }
-                }
-                apply_scale<M, NR0>(acc, c, a);
-            }
+        for (int i = 0; i < NR0; ++i) a[i] = __fmul_rn(d[i], sbyte_f<u & 3>(wd[i][48 + (u >> 2)]));
+        float2 c[NR0][M];
+        chain<M, NR0, 4, 256>(c, xc + 128 * h + 32 * t + 16 * gh, [&](auto qc, int i, float2& w01, float2& w23) {
+            q6k_group<h, t, 4 * gh + decltype(qc)::value>(wd[i], w01, w23);
+        });
+        apply_scale<M, NR0>(acc, c, a);
+    });
 }
 
 // ---------------------------------------------------------------- staging
 
-// Fallback staging (the TMA path needs 16-byte aligned rows): copy chunk cc
-// of one warp's rows with 2-byte loads into the positions a TMA box uses
-// (W only needs 2-byte alignment).
+// Fallback staging (the TMA path needs 16-byte aligned rows), done by the
+// producer warp: chunk cc of `nrows` weight rows, copied with 2-byte loads
+// (W only needs 2-byte alignment) into the positions a TMA box uses.  The
+// staged row's bytes outside the chunk read as zero, as a TMA box past the
+// row end does.
 template <int WT>
 __device__ __forceinline__ void stage_w_plain(uint8_t* dst_rows, const uint8_t* wrow0, uint64_t row_bytes,
                                               int nrows, uint32_t cc, uint32_t k, int lane) {
@@ -588,21 +602,24 @@ __device__ __forceinline__ void stage_w_plain(uint8_t* dst_rows, const uint8_t* 
         first = cc * 210u;
         len = 210u;
     }
-    const int so = Stage<WT>::sofs(cc);
-    const uint32_t halves = len >> 1;
+    const uint32_t so = static_cast<uint32_t>(Stage<WT>::sofs(cc));
     for (int r = 0; r < nrows; ++r) {
         const uint16_t* src = reinterpret_cast<const uint16_t*>(wrow0 + static_cast<uint64_t>(r) * row_bytes + first);
-        uint16_t* dst = reinterpret_cast<uint16_t*>(dst_rows + r * BOX + so);
-        for (uint32_t h = lane; h < halves; h += 32) dst[h] = __ldg(src + h);
+        uint16_t* dst = reinterpret_cast<uint16_t*>(dst_rows + r * BOX);
+        for (uint32_t h = lane; h < static_cast<uint32_t>(BOX / 2); h += 32) {
+            const uint32_t p = 2u * h;
+            dst[h] = (p >= so && p < so + len) ? __ldg(src + ((p - so) >> 1)) : static_cast<uint16_t>(0);
+        }
     }
 }
 
-// Fallback input staging: the [M][CV] slice of chunk cc, zero past k.
+// Fallback input staging by the producer warp: the [M][CV] slice of chunk
+// cc, zero past k.
 template <int M, int CV>
 __device__ __forceinline__ void stage_x_plain(float* dst, const float* xb, uint32_t xrs, uint32_t cc, uint32_t k,
-                                              int nthreads) {
+                                              int lane) {
     constexpr int Q = CV / 4;
-    for (int idx = static_cast<int>(threadIdx.x); idx < M * Q; idx += nthreads) {
+    for (int idx = lane; idx < M * Q; idx += 32) {
         const int j = idx / Q, q = idx - (idx / Q) * Q;
         const uint32_t col = cc * CV + 4u * q;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -646,33 +663,25 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
 // Decode + multiply one staged chunk for the warp's rows.
 template <int WT, int M, int NR0>
 __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int warp, int lane, uint32_t cc,
-                                         uint32_t k, float* xs, float2 (&acc)[NR0][M]) {
+                                         float* xs, float2 (&acc)[NR0][M]) {
     constexpr int BOX = Stage<WT>::kBox;
-    constexpr int CV = Stage<WT>::kValues;
     constexpr int ROWS = kLanes * NR0;
     const uint8_t* rows[NR0];
 #pragma unroll
     for (int i = 0; i < NR0; ++i) rows[i] = st + (warp * ROWS + lane + 32 * i) * BOX;
     const float* xc = reinterpret_cast<const float*>(st + wstage);  // [M][CV]
     if constexpr (WT == kF16) {
-        const int nv = static_cast<int>(min(136u, k - cc * 136u));
-        if (nv == 136) chunk_f16<M, NR0, true>(rows, xc, CV, nv, acc);
-        else chunk_f16<M, NR0, false>(rows, xc, CV, nv, acc);
-    } else if constexpr (WT == kQ8_0 || WT == kQ5_0) {
-        const int nb = static_cast<int>(min(8u, k / 32u - cc * 8u));
-        if (nb == 8) {
-            if constexpr (WT == kQ8_0) chunk_q8_0<M, NR0, true>(rows, xc, CV, nb, acc);
-            else chunk_q5_0<M, NR0, true>(rows, xc, CV, nb, acc);
-        } else {
-            if constexpr (WT == kQ8_0) chunk_q8_0<M, NR0, false>(rows, xc, CV, nb, acc);
-            else chunk_q5_0<M, NR0, false>(rows, xc, CV, nb, acc);
-        }
+        chunk_f16<M, NR0>(rows, xc, acc);
+    } else if constexpr (WT == kQ8_0) {
+        chunk_blocks32<M, NR0, BlkQ8>(rows, xc, acc);
+    } else if constexpr (WT == kQ5_0) {
+        chunk_blocks32<M, NR0, BlkQ5>(rows, xc, acc);
     } else if constexpr (WT == kQ4_K) {
         xsum_q4_k<M>(xc, xs, lane);
         __syncwarp();
-        chunk_q4_k<M, NR0>(rows, xc, CV, xs, acc);
+        chunk_q4_k<M, NR0>(rows, xc, xs, acc);
     } else {
-        chunk_q6_k<M, NR0>(rows, xc, CV, Stage<WT>::sofs(cc), acc);
+        chunk_q6_k<M, NR0>(rows, xc, Stage<WT>::sofs(cc), acc);
     }
 }
 
@@ -682,7 +691,7 @@ __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int
 // reaches the cluster barrier once per row block.
 template <int M, int NR0>
 __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool failed, const MvArgs& a, uint32_t b,
-                                          uint32_t wrow0, bool wactive, bool consumer, int lane, int warp,
+                                          uint32_t wrow0, bool wactive, int lane, int warp,
                                           uint32_t s, uint32_t S, uint32_t t, float* parts, uint32_t part_floats) {
     float part[NR0][M];
 #pragma unroll
@@ -704,7 +713,7 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool fail
         return;
     }
     float* buf = parts + (t & 1u) * part_floats;
-    if (s != 0 && consumer) {
+    if (s != 0) {
 #pragma unroll
         for (int i = 0; i < NR0; ++i)
 #pragma unroll
@@ -726,23 +735,27 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool fail
 
 // ---------------------------------------------------------------- the kernel
 
-// Persistent kernel.  A cluster of `split` CTAs walks the row blocks
+// Persistent kernel (at most 256 weight rows per CTA: 8 consumer warps with
+// one row per lane, 4 with two).  A cluster of `split` CTAs walks the row blocks
 // cid, cid + nclusters, ... (a row block is G row groups of ROWS = 32*NR0
 // rows of one batch); CTA rank s of the cluster handles K range s of every
 // row block.  A CTA has G consumer warps (one row group each) and one
-// producer warp.  Each pipeline stage holds one TMA box of the row block's
-// rows (G*ROWS x BOX bytes) and one box of the matching inputs (M x CV
-// floats).  The producer fills a stage once all consumer warps released it
-// (mbarrier `empty`, G arrivals) and runs on into the next row block;
-// consumers wait for the bytes (mbarrier `full`) and release each stage as
-// soon as they are done with it.  After a row block, CTAs of rank > 0 leave
-// their partial sums in shared memory (double-buffered by row-block parity),
-// one cluster barrier publishes them, and rank 0 adds them in range order
-// through distributed shared memory and stores y.  The producer takes part in
-// that barrier split-phase (arrive after issuing a row block, wait one row
-// block later), so it never stalls the stream.
+// producer warp.  Each pipeline stage holds one box of the row block's rows
+// (G*ROWS x BOX bytes) and one box of the matching inputs (M x CV floats).
+// The producer fills a stage once all consumer warps released it (mbarrier
+// `empty`, G arrivals) and runs on into the next row block; consumers wait
+// for the bytes (mbarrier `full`) and release each stage as soon as they are
+// done with it.  The producer fills stages with TMA copies (rows 16-byte
+// aligned) or, as a fallback, with plain loads and stores by its 32 lanes,
+// each of which then arrives on `full`; the consumers run the same code
+// either way.  After a row block, CTAs of rank > 0 leave their partial sums
+// in shared memory (double-buffered by row-block parity), one cluster
+// barrier publishes them, and rank 0 adds them in range order through
+// distributed shared memory and stores y.  The producer takes part in that
+// barrier split-phase (arrive after issuing a row block, wait one row block
+// later), so it never stalls the stream.
 template <int WT, int M, int NR0>
-__global__ void __launch_bounds__((kMaxWarps + 1) * 32)
+__global__ void __launch_bounds__((kMaxWarps / NR0 + 1) * 32)
 rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
     constexpr int BOX = Stage<WT>::kBox;
     constexpr int CV = Stage<WT>::kValues;
@@ -779,43 +792,10 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         row0 = (rb - b * a.cpb) * static_cast<uint32_t>(G * ROWS);
     };
 
-    bool failed = false;
-
-    if (!a.aligned) {
-        // ---- plain staging: every warp copies, consumers compute, one stage
-        const int nthreads = static_cast<int>(blockDim.x);
-        for (uint32_t rb = cid, t = 0; rb < nblocks; rb += ncl, ++t) {
-            uint32_t b, row0;
-            block_origin(rb, b, row0);
-            const uint32_t wrow0 = row0 + static_cast<uint32_t>(warp * ROWS);
-            const bool wactive = !producer && wrow0 < a.n;
-            const float* xb = a.x + static_cast<uint64_t>(b) * a.xbs;
-            const int wrows = wactive ? static_cast<int>(min(static_cast<uint32_t>(ROWS), a.n - wrow0)) : 0;
-            const uint8_t* wrow_ptr = a.w + (static_cast<uint64_t>(b) * a.n + wrow0) * a.row_bytes;
-            float2 acc[NR0][M];
-#pragma unroll
-            for (int i = 0; i < NR0; ++i)
-#pragma unroll
-                for (int j = 0; j < M; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
-            for (int i = 0; i < nck; ++i) {
-                const uint32_t cc = c0 + static_cast<uint32_t>(i);
-                if (wactive) stage_w_plain<WT>(smem + warp * ROWS * BOX, wrow_ptr, a.row_bytes, wrows, cc, a.k, lane);
-                stage_x_plain<M, CV>(reinterpret_cast<float*>(smem + wstage), xb, a.xrs, cc, a.k, nthreads);
-                __syncthreads();
-                if (wactive) mv_chunk<WT, M, NR0>(smem, wstage, warp, lane, cc, a.k, xs, acc);
-                __syncthreads();
-            }
-            mv_finish<M, NR0>(acc, false, a, b, wrow0, wactive, !producer, lane, warp, s, S, t, parts, part_floats);
-        }
-        if (S > 1) cluster_sync();  // no CTA leaves while a peer may still read it
-        return;
-    }
-
-    // ---- TMA pipeline
     const uint32_t fb = smem_u32(full), eb = smem_u32(empty);
     if (threadIdx.x == 0) {
         for (int t = 0; t < D; ++t) {
-            mbar_init(fb + 8 * t, 1);
+            mbar_init(fb + 8 * t, a.aligned ? 1u : 32u);
             mbar_init(eb + 8 * t, static_cast<uint32_t>(G));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -830,22 +810,41 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             uint32_t b, row0;
             block_origin(rb, b, row0);
             const uint64_t grow0 = static_cast<uint64_t>(b) * a.n + row0;
-            if (lane == 0 && !stop) {
+            if (a.aligned) {
+                if (lane == 0 && !stop) {
+                    for (int q = 0; q < nck; ++q, ++i) {
+                        const int st = static_cast<int>(i % D);
+                        if (i >= static_cast<uint32_t>(D) &&
+                            !mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1))) {
+                            stop = true;
+                            break;
+                        }
+                        const uint32_t cc = c0 + static_cast<uint32_t>(q);
+                        uint8_t* sp = smem + st * stage_bytes;
+                        mbar_expect_tx(fb + 8 * st, wstage + XBYTES);
+                        tma_load_2d(smem_u32(sp), &wmap, static_cast<int32_t>(Stage<WT>::gofs(cc) / 2),
+                                    static_cast<int32_t>(grow0), fb + 8 * st);
+                        tma_load_3d(smem_u32(sp + wstage), &xmap, static_cast<int32_t>(cc * CV),
+                                    a.x_bm ? static_cast<int32_t>(b) : 0, a.x_bm ? 0 : static_cast<int32_t>(b),
+                                    fb + 8 * st);
+                    }
+                }
+            } else if (!stop) {
+                const int nrows = static_cast<int>(min(static_cast<uint32_t>(G * ROWS), a.n - row0));
+                const uint8_t* wrow_ptr = a.w + grow0 * a.row_bytes;
+                const float* xb = a.x + static_cast<uint64_t>(b) * a.xbs;
                 for (int q = 0; q < nck; ++q, ++i) {
                     const int st = static_cast<int>(i % D);
                     if (i >= static_cast<uint32_t>(D) &&
-                        !mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1))) {
+                        !__all_sync(0xFFFFFFFFu, mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1)))) {
                         stop = true;
                         break;
                     }
                     const uint32_t cc = c0 + static_cast<uint32_t>(q);
                     uint8_t* sp = smem + st * stage_bytes;
-                    mbar_expect_tx(fb + 8 * st, wstage + XBYTES);
-                    tma_load_2d(smem_u32(sp), &wmap, static_cast<int32_t>(Stage<WT>::gofs(cc) / 2),
-                                static_cast<int32_t>(grow0), fb + 8 * st);
-                    tma_load_3d(smem_u32(sp + wstage), &xmap, static_cast<int32_t>(cc * CV),
-                                a.x_bm ? static_cast<int32_t>(b) : 0, a.x_bm ? 0 : static_cast<int32_t>(b),
-                                fb + 8 * st);
+                    stage_w_plain<WT>(sp, wrow_ptr, a.row_bytes, nrows, cc, a.k, lane);
+                    stage_x_plain<M, CV>(reinterpret_cast<float*>(sp + wstage), xb, a.xrs, cc, a.k, lane);
+                    mbar_arrive(fb + 8 * st);
                 }
             }
             __syncwarp();
@@ -856,7 +855,7 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         }
         if (S > 1 && t > 0) cluster_wait();
         // every copy issued has landed before the CTA can exit (bounded)
-        if (lane == 0) {
+        if (a.aligned && lane == 0) {
             const uint32_t issued = i;
             for (uint32_t r = issued > static_cast<uint32_t>(D) ? issued - D : 0u; r < issued; ++r)
                 (void)mbar_wait(fb + 8 * (r % D), static_cast<uint32_t>((r / D) & 1));
@@ -866,6 +865,7 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         return;
     }
 
+    bool failed = false;
     uint32_t i = 0;
     for (uint32_t rb = cid, t = 0; rb < nblocks; rb += ncl, ++t) {
         uint32_t b, row0;
@@ -884,12 +884,12 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 failed = true;
             if (failed) continue;  // keep walking so every barrier below is still reached
             if (wactive)
-                mv_chunk<WT, M, NR0>(smem + st * stage_bytes, wstage, warp, lane, c0 + static_cast<uint32_t>(q), a.k,
-                                     xs, acc);
+                mv_chunk<WT, M, NR0>(smem + st * stage_bytes, wstage, warp, lane, c0 + static_cast<uint32_t>(q), xs,
+                                     acc);
             __syncwarp();
             if (lane == 0) mbar_arrive(eb + 8 * st);
         }
-        mv_finish<M, NR0>(acc, failed, a, b, wrow0, wactive, true, lane, warp, s, S, t, parts, part_floats);
+        mv_finish<M, NR0>(acc, failed, a, b, wrow0, wactive, lane, warp, s, S, t, parts, part_floats);
     }
     if (S > 1) cluster_sync();
 }
@@ -897,16 +897,31 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 }  // namespace dev
 }  // namespace rem
 
-// Each translation unit instantiates four M values of one weight format,
-// both NR0, and exposes them through a lookup function.
-#define REM_K(WT, M) \
-    {(const void*)&::rem::dev::rem_mv_kernel<WT, M, 1>, (const void*)&::rem::dev::rem_mv_kernel<WT, M, 2>}
-#define REM_INSTANTIATE4(WT, NAME, M0)                                                             \
-    namespace rem {                                                                                \
-    const void* NAME(int m, int nr0) {                                                             \
-        static const void* const table[4][2] = {REM_K(WT, M0), REM_K(WT, M0 + 1), REM_K(WT, M0 + 2), \
-                                                REM_K(WT, M0 + 3)};                                \
-        if (m < M0 || m > M0 + 3 || nr0 < 1 || nr0 > 2) return nullptr;                           \
-        return table[m - M0][nr0 - 1];                                                             \
-    }                                                                                              \
+// Kernel pointer of one instantiation; two rows per lane (NR0 = 2) exist only
+// from M = 4 up and not for Q6_K (whose 53 staged words per row would not
+// fit twice in registers).
+namespace rem {
+template <int WT, int M, int NR0>
+inline const void* mv_kernel_ptr() {
+    if constexpr (NR0 == 2 && (M < 4 || WT == kQ6_K)) {
+        return nullptr;
+    } else {
+        return reinterpret_cast<const void*>(&dev::rem_mv_kernel<WT, M, NR0>);
+    }
+}
+}  // namespace rem
+
+// Each translation unit instantiates a range of M values of one weight
+// format and exposes them through a lookup function.
+#define REM_INSTANTIATE(WT, NAME, M0, NM)                                                           \
+    namespace rem {                                                                                 \
+    const void* NAME(int m, int nr0) {                                                              \
+        static const void* const table[4][2] = {                                                    \
+            {mv_kernel_ptr<WT, M0, 1>(), mv_kernel_ptr<WT, M0, 2>()},                               \
+            {mv_kernel_ptr<WT, (NM > 1 ? M0 + 1 : M0), 1>(), mv_kernel_ptr<WT, (NM > 1 ? M0 + 1 : M0), 2>()}, \
+            {mv_kernel_ptr<WT, (NM > 2 ? M0 + 2 : M0), 1>(), mv_kernel_ptr<WT, (NM > 2 ? M0 + 2 : M0), 2>()}, \
+            {mv_kernel_ptr<WT, (NM > 3 ? M0 + 3 : M0), 1>(), mv_kernel_ptr<WT, (NM > 3 ? M0 + 3 : M0), 2>()}}; \
+        if (m < M0 || m >= M0 + NM || nr0 < 1 || nr0 > 2) return nullptr;                          \
+        return table[m - M0][nr0 - 1];                                                              \
+    }                                                                                               \
     }
