@@ -56,6 +56,40 @@ def peaks():
     return 6800.0, 2070.0, "fallback"
 
 
+def kernel_sources_sha256() -> str:
+    """Digest of the CUDA sources and the public header (what a DRAM-traffic
+    figure measured by ncu depends on)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_few_row_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "rem.h"), "rb") as f:
+        h.update(b"rem.h\0" + f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch (read + write, averaged over one step's
+    launches) recorded under profiles/ for this workload, if the recording was
+    made from the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"rem_mv_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip().strip("`")
+            for key in ("kernel_sources_sha256", "dram_bytes_per_launch"):
+                if line.startswith(key + ":"):
+                    rec[key] = line.split(":", 1)[1].strip()
+    if rec.get("kernel_sources_sha256") != kernel_sources_sha256() or "dram_bytes_per_launch" not in rec:
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
 def call_bytes(fmt, n, k, batch, m, row_bytes):
     """Algorithmic bytes of one call: every weight once, x and y once."""
     return batch * n * row_bytes + 4 * batch * m * k + 4 * batch * m * n
@@ -275,7 +309,7 @@ def run_ours(args, rank, world, local_rank):
         "per_m_us": {str(m): round(per_m[m], 3) for m in ms},
         "per_m": per_m_out,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(args.workload),
                      "peak_source": f"{peak_kind} hbm_gbs", "kernel": "rem_mv_kernel (all m of the step)",
                      "fp32_peak_tflops": round(fp32_peak, 1)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -73,6 +74,12 @@ uint32_t pow2_floor(uint64_t v) {
 // Last element index + 1 touched by a strided [batch, rows, cols] view.
 uint64_t strided_extent(uint32_t batch, uint32_t bstride, uint32_t rows, uint32_t rstride, uint32_t cols) {
     return static_cast<uint64_t>(batch - 1) * bstride + static_cast<uint64_t>(rows - 1) * rstride + cols;
+}
+
+// REM_LOG_PLAN set in the environment: print each launch's schedule to stderr.
+bool log_plans() {
+    static const bool on = std::getenv("REM_LOG_PLAN") != nullptr;
+    return on;
 }
 
 // ---------------------------------------------------------------- driver entry points
@@ -288,7 +295,7 @@ uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
 struct Plan {
     int nr0, warps, stages, smem;
     uint32_t cpb, grid;
-    bool aligned;
+    bool aligned, pdl;
 };
 
 int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& s, uint32_t split,
@@ -318,16 +325,6 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     const uint32_t nchunk = (s.k + chunk_values(wt) - 1) / chunk_values(wt);
 
     Plan p{};
-    // Rows per lane: two rows share every input load from m >= 4 (kernels
-    // exist for those m), as long as the work still spreads over at least
-    // four warps per SM.
-    const uint64_t warps2 = static_cast<uint64_t>(s.batch) * ((s.n + 2 * kLanes - 1) / (2 * kLanes)) * S;
-    p.nr0 = (mv_kernel(wt, static_cast<int>(s.m), 2) != nullptr && warps2 >= 4ull * ds->sms) ? 2 : 1;
-    if (rows_per_cta && rows_per_cta < static_cast<uint32_t>(kLanes * p.nr0)) p.nr0 = 1;
-    const uint32_t rows_per_warp = static_cast<uint32_t>(kLanes * p.nr0);
-    const void* fn = mv_kernel(wt, static_cast<int>(s.m), p.nr0);
-    if (!fn) return fail(REM_ELAUNCH, "rem_matvec: no %s kernel for m %u", wt_name(wt), s.m);
-
     // TMA staging needs 16-byte aligned rows and encodable tensor maps.
     // Inputs: [batch][m][k] f32 with the caller's strides, dimensions ordered
     // by increasing stride; either order stages the box as [m][chunk].
@@ -352,64 +349,81 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
 
-    // Row-block width G (consumer warps per CTA) and ring depth D: the pair
-    // with the best score among those that fit.  Small m is bound by the
-    // bytes in flight per SM (up to ~96 KB), larger m by the warps that can
-    // issue decode and FMA work; both are scaled by the share of resident
-    // CTA slots the last wave of row blocks keeps busy.
+    // Rows per lane NR0, row-block width G (consumer warps per CTA) and ring
+    // depth D: the fitting triple with the best score.  The score models a
+    // kernel that is bound by how many consumer warps each SM keeps busy
+    // (latency of shared-memory loads and stage waits): the average consumer
+    // warps per SM (saturating at 8), with two rows per lane sharing every
+    // input load worth 1.8x, a single stage (no copy/compute overlap) 0.7x,
+    // the producer warp's share (G/(G+1))^2, 20% less per stage beyond two
+    // (deeper rings cost residency for no gain), all scaled by the share of
+    // resident CTA slots the last wave of row blocks keeps busy.  The weights
+    // were fitted to timings of every (NR0, G, D) on GB300 for the five
+    // formats at 4096..128256 rows.
     cudaLaunchConfig_t cfg{};
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
     if (S > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = S;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = S;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
     }
     double best = -1.0;
-    for (int g = kMaxWarps; g >= 1; g /= 2) {
-        if (rows_per_cta ? static_cast<uint32_t>(g) * rows_per_warp != rows_per_cta
-                         : (g > 4 || static_cast<uint32_t>(g) * rows_per_warp > 256u))
-            continue;
-        if ((g + 1) * 32 > ds->max_threads[wt][s.m][p.nr0]) {
-            if (!rows_per_cta) continue;
-            return fail(REM_ELAUNCH, "rem_matvec: %d warps per block exceed the %s kernel's limit of %d threads",
-                        g + 1, wt_name(wt), ds->max_threads[wt][s.m][p.nr0]);
-        }
-        const uint64_t nb = static_cast<uint64_t>(s.batch) * ((s.n + rows_per_warp * g - 1) / (rows_per_warp * g));
-        const uint64_t units = nb * S;
-        const uint64_t per_cta = ((nchunk + S - 1) / S) * ((units + 2ull * ds->sms - 1) / (2ull * ds->sms));
-        const int dmax = static_cast<int>(std::min<uint64_t>(kMaxStages, std::max<uint64_t>(2, per_cta)));
-        for (int d = 1; d <= dmax; ++d) {
-            const int sm = static_cast<int>(mv_smem_bytes(wt, p.nr0, g, d, static_cast<int>(s.m), S));
-            if (sm > ds->smem_optin) continue;
-            cfg.blockDim = dim3(static_cast<unsigned>((g + 1) * 32));
-            cfg.dynamicSmemBytes = static_cast<size_t>(sm);
-            const uint64_t slots = resident_clusters(fn, cfg, S, ds->sms) * S;
-            if (slots == 0) continue;
-            const uint64_t ctas = std::min(units, slots);
-            const uint64_t waves = (units + ctas - 1) / ctas;
-            const double eff = static_cast<double>(units) / static_cast<double>(waves * ctas);
-            const double per_sm = static_cast<double>(ctas) / ds->sms;
-            const double warps_sm = per_sm * g;
-            const double inflight =
-                per_sm * d * static_cast<double>(mv_stage_bytes(wt, p.nr0, g, static_cast<int>(s.m)));
-            double score = s.m <= 2 ? std::min(inflight, 98304.0) * 1e-3 + warps_sm + 0.01 * g
-                                    : warps_sm * (d >= 2 ? 1.0 : 0.75) + 0.05 * d;
-            score *= eff;
-            if (score > best) {
-                best = score;
-                p.warps = g;
-                p.stages = d;
-                p.smem = sm;
+    const void* fn = nullptr;
+    int last_cap = 0;
+    for (int nr0 = 2; nr0 >= 1; --nr0) {
+        const void* f = mv_kernel(wt, static_cast<int>(s.m), nr0);
+        if (!f) continue;
+        const uint32_t rpw = static_cast<uint32_t>(kLanes * nr0);
+        const int cap = ds->max_threads[wt][s.m][nr0];
+        for (int g = kMaxWarps; g >= 1; g /= 2) {
+            if (rows_per_cta ? static_cast<uint32_t>(g) * rpw != rows_per_cta
+                             : (g > 4 || static_cast<uint32_t>(g) * rpw > 256u))
+                continue;
+            if ((g + 1) * 32 > cap) {
+                last_cap = cap;
+                continue;
+            }
+            const uint64_t nb = static_cast<uint64_t>(s.batch) * ((s.n + rpw * g - 1) / (rpw * g));
+            const uint64_t units = nb * S;
+            const uint64_t per_cta = ((nchunk + S - 1) / S) * ((units + 2ull * ds->sms - 1) / (2ull * ds->sms));
+            const int dmax = static_cast<int>(std::min<uint64_t>(kMaxStages, std::max<uint64_t>(2, per_cta)));
+            for (int d = 1; d <= dmax; ++d) {
+                const int sm = static_cast<int>(mv_smem_bytes(wt, nr0, g, d, static_cast<int>(s.m), S));
+                if (sm > ds->smem_optin) continue;
+                cfg.blockDim = dim3(static_cast<unsigned>((g + 1) * 32));
+                cfg.dynamicSmemBytes = static_cast<size_t>(sm);
+                const uint64_t slots = resident_clusters(f, cfg, S, ds->sms) * S;
+                if (slots == 0) continue;
+                const uint64_t ctas = std::min(units, slots);
+                const uint64_t waves = (units + ctas - 1) / ctas;
+                const double eff = static_cast<double>(units) / static_cast<double>(waves * ctas);
+                const double warps_sm = static_cast<double>(ctas) / ds->sms * g;
+                const double gf = static_cast<double>(g) / (g + 1);
+                double score = std::min(warps_sm, 8.0) * (nr0 == 2 ? 1.8 : 1.0) * (d == 1 ? 0.7 : 1.0) * gf * gf *
+                               (1.0 - 0.2 * std::max(0, d - 2)) * eff;
+                if (score > best) {
+                    best = score;
+                    fn = f;
+                    p.nr0 = nr0;
+                    p.warps = g;
+                    p.stages = d;
+                    p.smem = sm;
+                }
             }
         }
     }
-    if (best < 0)
-        return fail(REM_ELAUNCH, "rem_matvec: no %s block of %u rows fits the device's shared memory",
-                    wt_name(wt), rows_per_cta ? rows_per_cta : rows_per_warp);
+    if (best < 0) {
+        if (last_cap)
+            return fail(REM_ELAUNCH, "rem_matvec: %u rows per block exceed the %s kernel's limit of %d threads",
+                        rows_per_cta, wt_name(wt), last_cap);
+        return fail(REM_ELAUNCH, "rem_matvec: no %s row block fits the device's shared memory", wt_name(wt));
+    }
+    const uint32_t rows_per_warp = static_cast<uint32_t>(kLanes * p.nr0);
     p.cpb = (s.n + rows_per_warp * p.warps - 1) / (rows_per_warp * p.warps);
     const uint64_t nblocks = static_cast<uint64_t>(p.cpb) * s.batch;
     if (nblocks > 0x7FFFFFFFull)
@@ -437,6 +451,27 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     const uint64_t ncl = std::min<uint64_t>(nblocks, resident);
     p.grid = static_cast<uint32_t>(ncl * S);
     cfg.gridDim = dim3(p.grid);
+    // Programmatic dependent launch: the kernel may start while the previous
+    // kernel of the stream finishes (it waits for it, griddepcontrol.wait,
+    // before reading x or W into shared memory and before writing y), and
+    // prefetches its first weights into L2 meanwhile.  That pays where the
+    // launch is short next to its start-up latency -- from m = 4 up (compute
+    // bound) below 256 MB of weights, from m = 2 up below 24 MB -- and costs
+    // throughput on long bandwidth-bound launches, which keep plain stream
+    // order.  Scheduling only: the arithmetic is the same either way.
+    const uint64_t wbytes = rb * rows;
+    p.pdl = (s.m >= 4 && wbytes <= (256ull << 20)) || (s.m >= 2 && wbytes <= (24ull << 20));
+    if (p.pdl) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
+    }
+    if (log_plans())
+        fprintf(stderr,
+                "rem_matvec plan: %s m %u n %u k %u batch %u split %u nr0 %d warps %d stages %d smem %d grid %u "
+                "row_blocks %llu tma %d pdl %d\n",
+                wt_name(wt), s.m, s.n, s.k, s.batch, S, p.nr0, p.warps, p.stages, p.smem, p.grid,
+                static_cast<unsigned long long>(nblocks), static_cast<int>(p.aligned), static_cast<int>(p.pdl));
 
     MvArgs a{};
     a.w = static_cast<const uint8_t*>(W);
@@ -456,6 +491,7 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     a.stages = static_cast<uint32_t>(p.stages);
     a.aligned = p.aligned ? 1u : 0u;
     a.x_bm = x_bm ? 1u : 0u;
+    a.pdl = p.pdl ? 1u : 0u;
 
     void* args[3] = {&wmap, &xmap, &a};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);

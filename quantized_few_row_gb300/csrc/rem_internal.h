@@ -53,6 +53,7 @@ struct MvArgs {
     uint32_t stages;         // pipeline stages (1..4)
     uint32_t aligned;        // 1: TMA staging (16-byte aligned rows, encodable input map)
     uint32_t x_bm;           // input map dimension order: 1 = [k, batch, m] (token-major), 0 = [k, m, batch]
+    uint32_t pdl;            // 1: launched as a programmatic dependent of the stream's previous kernel
 };
 
 // Kernel lookup: rem_mv_kernel<wt, m, nr0>, m in 1..8, nr0 in {1, 2}.

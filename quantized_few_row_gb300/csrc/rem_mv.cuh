@@ -102,6 +102,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 // ---------------------------------------------------------------- mbarrier / TMA
 
+// Weight bytes a CTA prefetches into L2 ahead of its dependency wait.
+constexpr uint32_t kPrefetchBytes = 64u << 10;
+
 // Bounded wait: a phase that does not complete within the limit reports
 // failure instead of spinning forever.
 constexpr uint32_t kWaitLimit = 1u << 20;
@@ -151,6 +154,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
+
+// Prefetch one TMA box of weights into L2 (no shared-memory destination, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel of the stream start its
+// prologue, and wait until every kernel this one depends on has completed
+// and its writes are visible (returns at once without such a dependency).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------- format traits
 
@@ -800,6 +820,21 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // Launched as a programmatic dependent (a.pdl): the first row block's
+    // weights go to L2 before the wait for the previous kernel (a prefetch
+    // only fills L2, which every later write also goes through, so it cannot
+    // make a later load stale); everything that reads x or W into shared
+    // memory, or writes y, comes after the wait.  Without such a launch the
+    // wait returns at once.
+    if (a.pdl && a.aligned && producer && lane == 0 && cid < nblocks) {
+        uint32_t b, row0;
+        block_origin(cid, b, row0);
+        const int32_t grow = static_cast<int32_t>(static_cast<uint64_t>(b) * a.n + row0);
+        const int npf = min(nck, static_cast<int>(kPrefetchBytes / wstage) + 1);
+        for (int q = 0; q < npf; ++q)
+            tma_prefetch_2d(&wmap, static_cast<int32_t>(Stage<WT>::gofs(c0 + static_cast<uint32_t>(q)) / 2), grow);
+    }
+    pdl_wait();
     __syncthreads();
 
     if (producer) {
@@ -853,6 +888,9 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 cluster_arrive();            // phase t
             }
         }
+        // all of this CTA's copies are issued: the next kernel of the stream
+        // may start its prologue (it waits for this one before using memory)
+        pdl_launch_dependents();
         if (S > 1 && t > 0) cluster_wait();
         // every copy issued has landed before the CTA can exit (bounded)
         if (a.aligned && lane == 0) {

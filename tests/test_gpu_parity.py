@@ -276,3 +276,60 @@ def test_rejected_calls_write_nothing():
     assert rem.rem_matvec_ex(wp, "q8_0", n, k, 1, xd, m, k, 0, yd, n, 0, 16, 0) == rem.REM_ELAUNCH
     torch.cuda.synchronize()
     assert np.all(yd.cpu().numpy() == H.CANARY)
+
+
+# ---------------------------------------------------------------- dependent launches
+
+def _alternating_sequence(fmt, n, k, m, stream, W, x, srcs, xs, outs):
+    """rem_quantize -> input copy -> rem_matvec -> output copy, three times
+    per source, on one stream with no synchronisation in between."""
+    for it in range(len(outs)):
+        i = it % 2
+        rem.check(rem.rem_quantize(srcs[i], fmt, n, k, W, stream))
+        x.copy_(xs[i])
+        rem.check(rem.rem_matvec(W, fmt, n, k, 1, x, m, 0, outs[it], 0, stream))
+        outs[it].mul_(1.0)   # a kernel that reads y right after the call
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("graph", [False, True])
+def test_back_to_back_calls_see_previous_writes(fmt, graph):
+    """Each call may start while the previous kernel of its stream is still
+    running (it only prefetches weights into L2 before waiting for it): weights
+    just rewritten by rem_quantize, inputs just rewritten by a copy, and an
+    output read by the next kernel give exactly the synchronised result."""
+    n, k, m = 640, 2048, 4
+    dev = H.dev()
+    wf = [inputs.weights(n, k, 260), inputs.weights(n, k, 261)]
+    xf = [inputs.activations(m, k, 360), inputs.activations(m, k, 361)]
+    q = [oracle.quantize(w, fmt) for w in wf]
+    ref = [H.run_matvec(q[i], fmt, n, k, 1, xf[i], m, k, 0, n, 0, m * n, use_ex=False) for i in range(2)]
+    for i in range(2):
+        y_ref, a_ref = oracle.matvec(q[i], fmt, n, k, 1, xf[i], m, k, 0)
+        H.assert_close_to_oracle(ref[i].reshape(1, m, n), y_ref, a_ref, fmt)
+    srcs = [torch.from_numpy(w).to(dev) for w in wf]
+    xs = [H.to_dev_f32(x) for x in xf]
+    W = torch.zeros(n * oracle.row_bytes(fmt, k), dtype=torch.uint8, device=dev)
+    x = torch.zeros_like(xs[0])
+    outs = [H.canary(m * n) for _ in range(6)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=dev)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                _alternating_sequence(fmt, n, k, m, s, W, x, srcs, xs, outs)
+        for _ in range(2):
+            for o in outs:
+                o.fill_(float(H.CANARY))
+            with torch.cuda.stream(s):
+                g.replay()
+            s.synchronize()
+            for it, o in enumerate(outs):
+                assert np.array_equal(o.cpu().numpy().view(np.uint32), ref[it % 2].view(np.uint32)), it
+    else:
+        with torch.cuda.stream(s):
+            _alternating_sequence(fmt, n, k, m, s, W, x, srcs, xs, outs)
+        s.synchronize()
+        for it, o in enumerate(outs):
+            assert np.array_equal(o.cpu().numpy().view(np.uint32), ref[it % 2].view(np.uint32)), it
