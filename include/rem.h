@@ -21,7 +21,11 @@
  * device pointer (or managed memory) owned by the caller; the library never
  * allocates, frees, synchronises or copies to the host on these calls.
  * `stream` is a cudaStream_t (NULL = the legacy default stream); the work is
- * enqueued asynchronously on it and the call returns before it runs.
+ * enqueued asynchronously on it and the call returns before it runs.  It
+ * keeps stream order: it sees every earlier write of the stream and later
+ * work sees its output (the kernel may start early and prefetch weights into
+ * L2, but reads x and W into the SM and writes y only once the previous
+ * kernel of the stream has completed).
  *
  * Errors.  Every call validates its arguments before it launches anything;
  * on an error nothing is written and a message prefixed "rem_matvec:" (or the

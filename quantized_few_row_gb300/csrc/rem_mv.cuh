@@ -706,9 +706,14 @@ __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int
 }
 
 // End of a row block for one consumer warp: the range partial
-// (acc.x + acc.y), then either the store (split 1) or the in-order sum of
-// the cluster's ranges by rank 0.  Every thread of every CTA of the cluster
-// reaches the cluster barrier once per row block.
+// (acc.x + acc.y), then either the store (split 1) or the in-order sum of the
+// cluster's ranges.  With split S every rank publishes its partials in shared
+// memory, one cluster barrier makes them visible, and output (i, j) of the
+// warp's rows is finished by rank (i*M + j) mod S: it loads the S partials of
+// that output (its own and the peers', through distributed shared memory),
+// all loads issued before the first add, and adds them in rank order.  Every
+// thread of every CTA of the cluster reaches the cluster barrier once per row
+// block.
 template <int M, int NR0>
 __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool failed, const MvArgs& a, uint32_t b,
                                           uint32_t wrow0, bool wactive, int lane, int warp,
@@ -733,21 +738,26 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool fail
         return;
     }
     float* buf = parts + (t & 1u) * part_floats;
-    if (s != 0) {
 #pragma unroll
-        for (int i = 0; i < NR0; ++i)
+    for (int i = 0; i < NR0; ++i)
 #pragma unroll
-            for (int j = 0; j < M; ++j) buf[((warp * NR0 + i) * M + j) * 32 + lane] = part[i][j];
-    }
+        for (int j = 0; j < M; ++j) buf[((warp * NR0 + i) * M + j) * 32 + lane] = part[i][j];
     cluster_sync();  // phase t: the ranges' partials of this row block are published
-    if (s == 0 && wactive) {
+    if (wactive) {
 #pragma unroll
         for (int i = 0; i < NR0; ++i)
 #pragma unroll
             for (int j = 0; j < M; ++j) {
+                if (static_cast<uint32_t>(i * M + j) % S != s) continue;
                 const float* slot = buf + ((warp * NR0 + i) * M + j) * 32 + lane;
-                float v = part[i][j];
-                for (uint32_t r = 1; r < S; ++r) v = __fadd_rn(v, ld_peer(slot, r));
+                float p[kMaxSplit];
+#pragma unroll
+                for (int r = 0; r < kMaxSplit; ++r)
+                    if (static_cast<uint32_t>(r) < S) p[r] = static_cast<uint32_t>(r) == s ? part[i][j] : ld_peer(slot, r);
+                float v = p[0];
+#pragma unroll
+                for (int r = 1; r < kMaxSplit; ++r)
+                    if (static_cast<uint32_t>(r) < S) v = __fadd_rn(v, p[r]);
                 store(i, j, v);
             }
     }
