@@ -62,7 +62,8 @@ typedef enum {
 } rem_status;
 
 #define REM_MAX_ROWS 8     /* ROW_EXACT_MATVEC_MAX_ROWS */
-#define REM_MAX_SPLIT 16   /* largest split factor a launch accepts */
+#define REM_MAX_SPLIT 16   /* largest split factor the argument rules accept */
+#define REM_MAX_CLUSTER_SPLIT 8  /* largest split the kernels launch (cluster size); above: REM_ELAUNCH */
 
 /*
  * rem_matvec -- y[b, j, :] = W[b] . x[b, j, :] with the default schedule
@@ -105,8 +106,8 @@ int rem_matvec(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch,
  *   split         K ranges per weight row, 1..REM_MAX_SPLIT, or 0 for
  *                 rem_split_factor(wtype, batch*n, k).  Rows are bitwise
  *                 comparable only between calls with the same split.
- *   rows_per_cta  0 (automatic) or 32, 64, 128 or 256: weight rows one
- *                 thread block handles.  Numerically inert.
+ *   rows_per_cta  0 (automatic) or 32, 64 or 128: weight rows one thread
+ *                 block handles.  Numerically inert.
  *
  * A split whose thread block would exceed the kernels' launch limit returns
  * REM_ELAUNCH instead of launching (the page refuses such a launch rather
@@ -129,11 +130,13 @@ uint64_t rem_row_bytes(int wtype, uint32_t k);
  * `rows` (= batch*n) rows of k elements (the analogue of
  * row_exact_reduction_nsg followed by the device cap of
  * RowExactMatvecSchedule::for_device).  It depends on (wtype, rows, k) only:
- * a power of two so that rows/32 * split reaches about 2048 warps, at most 16
- * and at most the number of chunks of a row.  The device cap is the largest
- * power of two of warps every kernel of the weight type can launch; kernels
- * are compiled for 512 threads, so it does not bind on sm_103a.  Returns 0
- * for an unknown wtype or rows == 0 or k == 0.  Host only.
+ * a power of two so that rows/32 * split reaches about 2048, at most the
+ * number of chunks of a row (72 F16 values, 4 Q8_0 blocks, 8 Q5_0 blocks,
+ * one Q4_K / Q6_K super-block) and at most REM_MAX_CLUSTER_SPLIT (8): the
+ * split ranges of a row run as the thread blocks of one cluster, and 8 is
+ * the portable cluster size (the page's device cap on threads per
+ * threadgroup becomes this cap).  Returns 0 for an unknown wtype or
+ * rows == 0 or k == 0.  Host only; makes no CUDA call.
  */
 uint32_t rem_split_factor(int wtype, uint32_t rows, uint32_t k);
 

@@ -120,7 +120,7 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     int smem_optin = 0;
-    uint32_t cap_warps[kNumWt] = {0, 0, 0, 0, 0};  // largest power-of-two warps every kernel can launch
+    int smem_per_sm = 0;
     int max_threads[kNumWt][kMaxRows + 1][3] = {};  // per kernel <wt, m, nr0>
 };
 
@@ -138,12 +138,13 @@ int device_state(DeviceState** out) {
     DeviceState& st = g_dev[dev];
     if (!st.ready) {
         if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+            cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+                cudaSuccess) {
             cudaGetLastError();
             return fail(REM_ECUDA, "rem_matvec: cannot query device %d", dev);
         }
         for (int wt = 0; wt < kNumWt; ++wt) {
-            int threads = (kMaxWarps + 1) * 32;
             for (int m = 1; m <= kMaxRows; ++m)
                 for (int nr0 = 1; nr0 <= 2; ++nr0) {
                     const void* fn = mv_kernel(wt, m, nr0);
@@ -157,9 +158,7 @@ int device_state(DeviceState** out) {
                                     wt_name(wt), dev, "no sm_103a image for this device?");
                     }
                     st.max_threads[wt][m][nr0] = fa.maxThreadsPerBlock;
-                    if (nr0 == 1 && fa.maxThreadsPerBlock < threads) threads = fa.maxThreadsPerBlock;
                 }
-            st.cap_warps[wt] = threads >= 32 ? pow2_floor(static_cast<uint32_t>(threads / 32)) : 0;
         }
         st.ready = true;
     }
@@ -245,9 +244,8 @@ int validate_args(const void* W, int wt, const float* x, const float* y, const S
         return fail(REM_EINVAL, "rem_matvec: n (%u), k (%u) and batch (%u) must be > 0", s.n, s.k, s.batch);
     if (split > REM_MAX_SPLIT)
         return fail(REM_EINVAL, "rem_matvec: split (%u) must be 0 (auto) or in 1..=%d", split, REM_MAX_SPLIT);
-    if (!(rows_per_cta == 0 || rows_per_cta == 32 || rows_per_cta == 64 || rows_per_cta == 128 ||
-          rows_per_cta == 256))
-        return fail(REM_EINVAL, "rem_matvec: rows_per_cta (%u) must be 0, 32, 64, 128 or 256", rows_per_cta);
+    if (!(rows_per_cta == 0 || rows_per_cta == 32 || rows_per_cta == 64 || rows_per_cta == 128))
+        return fail(REM_EINVAL, "rem_matvec: rows_per_cta (%u) must be 0, 32, 64 or 128", rows_per_cta);
     if (!W || !x || !y) return fail(REM_EINVAL, "rem_matvec: W, x and y must be non-null");
     if (s.k % k_multiple(wt) != 0)
         return fail(REM_EINVAL, "rem_matvec: k (%u) must be a multiple of %u for %s", s.k, k_multiple(wt),
@@ -449,6 +447,21 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
         return fail(REM_ELAUNCH, "rem_matvec: a cluster of %u blocks of %d threads and %d bytes does not fit",
                     S, threads, p.smem);
     const uint64_t ncl = std::min<uint64_t>(nblocks, resident);
+    // When fewer CTAs run than can be resident, the block scheduler fills SMs
+    // to their occupancy limit and leaves others idle.  Asking for more
+    // (unused) shared memory per CTA caps the CTAs per SM at the even share,
+    // ceil(ctas / SMs), which spreads the grid over the SMs -- kept only if
+    // the whole grid still fits at once.
+    if (ncl < resident) {
+        const uint64_t per_sm = (ncl * S + ds->sms - 1) / ds->sms;
+        const int cap = static_cast<int>(std::min<uint64_t>(static_cast<uint64_t>(ds->smem_optin),
+                                                            static_cast<uint64_t>(ds->smem_per_sm) / per_sm - 1024));
+        if (cap > p.smem && blocks_per_sm(fn, threads, p.smem) > static_cast<int>(per_sm)) {
+            cfg.dynamicSmemBytes = static_cast<size_t>(cap);
+            if (resident_clusters(fn, cfg, S, ds->sms) >= ncl) p.smem = cap;
+            cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+        }
+    }
     p.grid = static_cast<uint32_t>(ncl * S);
     cfg.gridDim = dim3(p.grid);
     // Programmatic dependent launch: the kernel may start while the previous
@@ -561,15 +574,8 @@ uint64_t rem_row_bytes(int wtype, uint32_t k) { return row_bytes_of(wtype, k); }
 
 uint32_t rem_split_factor(int wtype, uint32_t rows, uint32_t k) {
     if (!valid_wt(wtype) || rows == 0 || k == 0) return 0;
-    uint32_t s = auto_split(wtype, rows, k);
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) {
-        DeviceState* ds = nullptr;
-        if (device_state(&ds) == REM_OK && s > ds->cap_warps[wtype]) s = ds->cap_warps[wtype];
-    }
-    cudaGetLastError();
     g_err[0] = '\0';
-    return s;
+    return auto_split(wtype, rows, k);
 }
 
 int rem_dequantize(const void* W, int wtype, uint32_t rows, uint32_t k, float* out, void* stream) {

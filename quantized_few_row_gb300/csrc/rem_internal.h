@@ -11,7 +11,7 @@ enum Wt : int { kF16 = 0, kQ8_0 = 1, kQ4_K = 2, kQ6_K = 3, kQ5_0 = 4, kNumWt = 5
 
 constexpr int kMaxRows = 8;        // ROW_EXACT_MATVEC_MAX_ROWS
 constexpr int kLanes = 32;         // weight rows per warp and NR0: one row per lane
-constexpr int kMaxWarps = 8;       // warps per CTA (kernels are bounded to 256 threads)
+constexpr int kMaxWarps = 4;       // consumer warps per CTA (kernels are bounded to 5 warps)
 constexpr int kMaxSplit = 8;       // K ranges per row = CTAs per cluster (portable cluster limit)
 constexpr int kMaxStages = 4;      // pipeline stages (mbarriers) per warp
 
@@ -24,16 +24,18 @@ __host__ __device__ constexpr int block_bytes(int wt) {
 }
 
 // Staging geometry.  A "chunk" is the slice of one weight row a lane decodes
-// between two pipeline waits: 136 F16 values, 8 Q8_0 / Q5_0 blocks, or one
-// Q4_K / Q6_K super-block.  A warp stages the same chunk of its 32*NR0 rows
-// as one 2-D TMA box, one row every `box` bytes.  Box widths are odd
+// between two pipeline waits: 72 F16 values, 4 Q8_0 blocks, 8 Q5_0 blocks, or
+// one Q4_K / Q6_K super-block.  A warp stages the same chunk of its 32*NR0
+// rows as one 2-D TMA box, one row every `box` bytes.  Box widths are odd
 // multiples of 16 bytes, so 32 lanes reading 16 bytes each at the same
 // offset of their own rows hit distinct bank quads (4 wavefronts, the
-// minimum).  Q6_K stages the 16-byte aligned 240-byte window around its
-// 210-byte super-block.
-__host__ __device__ constexpr int chunk_values(int wt) { return wt == kF16 ? 136 : 256; }
+// minimum).  Q8_0 and Q6_K stage the 16-byte aligned window (144 / 240
+// bytes) around their 136 / 210 chunk bytes.
+__host__ __device__ constexpr int chunk_values(int wt) {
+    return wt == kF16 ? 72 : wt == kQ8_0 ? 128 : 256;
+}
 __host__ __device__ constexpr int chunk_box(int wt) {
-    return (wt == kF16 || wt == kQ8_0) ? 272 : wt == kQ5_0 ? 176 : wt == kQ4_K ? 144 : 240;
+    return (wt == kF16 || wt == kQ8_0 || wt == kQ4_K) ? 144 : wt == kQ5_0 ? 176 : 240;
 }
 
 // Kernel argument block (one launch).  Grid: a number of clusters of

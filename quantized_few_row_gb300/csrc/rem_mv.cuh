@@ -178,14 +178,16 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // staged row where chunk `cc` starts.
 template <int WT> struct Stage;
 template <> struct Stage<kF16> {
-    static constexpr int kValues = 136, kBox = 272;
-    __device__ static uint32_t gofs(uint32_t cc) { return cc * 272u; }  // global byte offset of the box
+    static constexpr int kValues = 72, kBox = 144;
+    __device__ static uint32_t gofs(uint32_t cc) { return cc * 144u; }  // global byte offset of the box
     __device__ static int sofs(uint32_t) { return 0; }
 };
+// Q8_0 chunks are 4 blocks (136 B): stage the 16-byte aligned 144-byte
+// window that contains them; they start 0 or 8 bytes into it.
 template <> struct Stage<kQ8_0> {
-    static constexpr int kValues = 256, kBox = 272;
-    __device__ static uint32_t gofs(uint32_t cc) { return cc * 272u; }
-    __device__ static int sofs(uint32_t) { return 0; }
+    static constexpr int kValues = 128, kBox = 144;
+    __device__ static uint32_t gofs(uint32_t cc) { return (cc * 136u) & ~15u; }
+    __device__ static int sofs(uint32_t cc) { return static_cast<int>((cc * 136u) & 15u); }
 };
 template <> struct Stage<kQ5_0> {
     static constexpr int kValues = 256, kBox = 176;
@@ -274,10 +276,10 @@ __device__ __forceinline__ uint32_t spread4(uint32_t h) { return (h * 0x02040810
 // memory, group<Q>() yields values 4Q..4Q+3 as two pairs (decoded when the
 // chain needs them, so only the block's raw words stay in registers).
 //
-// Q8_0 block B: 34 B at byte 34*B of a 16-aligned staged row; d, then 32 int8.
-template <int B>
+// Q8_0 block at byte POS (even) of a 16-aligned staged row; d, then 32 int8.
+template <int POS>
 struct BlkQ8 {
-    static constexpr int off = 34 * B, p0 = off >> 4, bo = off & 15;
+    static constexpr int off = POS, p0 = off >> 4, bo = off & 15;
     uint32_t W[12];
     float d;
     __device__ __forceinline__ void load(const uint8_t* row) {
@@ -296,11 +298,11 @@ struct BlkQ8 {
     }
 };
 
-// Q5_0 block B: 22 B at byte 22*B; d, qh (bit e = bit 4 of element e), then
+// Q5_0 block at byte POS (even): d, qh (bit e = bit 4 of element e), then
 // 16 bytes whose low nibbles are elements 0..15 and high nibbles 16..31.
-template <int B>
+template <int POS>
 struct BlkQ5 {
-    static constexpr int off = 22 * B, p0 = off >> 4, bo = off & 15;
+    static constexpr int off = POS, p0 = off >> 4, bo = off & 15;
     uint32_t qs[4];
     uint32_t qh;
     float d;
@@ -439,7 +441,7 @@ __device__ __forceinline__ void chain(float2 (&c)[NR0][M], const float* xu, Gen&
     });
 }
 
-// F16 chunk of 136 values (a zero-filled tail past k adds exact zeros).
+// F16 chunk of 72 values (a zero-filled tail past k adds exact zeros).
 template <int M, int NR0>
 __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], const float* xc,
                                           float2 (&acc)[NR0][M]) {
@@ -449,7 +451,7 @@ __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], con
 #pragma unroll
         for (int j = 0; j < M; ++j) c[i][j] = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int g = 0; g < 17; ++g) {  // 8 values per step
+    for (int g = 0; g < 9; ++g) {  // 8 values per step
         float2 p[NR0][4];
 #pragma unroll
         for (int i = 0; i < NR0; ++i) {
@@ -461,8 +463,8 @@ __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], con
         }
 #pragma unroll
         for (int j = 0; j < M; ++j) {
-            const float4 xa = ldx4(xc + j * 136 + 8 * g);
-            const float4 xb = ldx4(xc + j * 136 + 8 * g + 4);
+            const float4 xa = ldx4(xc + j * 72 + 8 * g);
+            const float4 xb = ldx4(xc + j * 72 + 8 * g + 4);
 #pragma unroll
             for (int i = 0; i < NR0; ++i) {
                 c[i][j] = fma2(p[i][0], make_float2(xa.x, xa.y), c[i][j]);
@@ -478,14 +480,16 @@ __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], con
         for (int j = 0; j < M; ++j) acc[i][j] = add2(acc[i][j], c[i][j]);
 }
 
-// Eight 32-value blocks (Q8_0 or Q5_0) of one staged chunk.  Blocks past k
-// are zero-filled (scale 0, inputs 0) and add exact zeros.
-template <int M, int NR0, template <int> class Blk>
+// NB 32-value blocks (Q8_0 or Q5_0) of one staged chunk, block b at byte
+// O + STRIDE*b of each staged row.  Blocks past k are zero-filled (scale 0,
+// inputs 0) and add exact zeros.
+template <int M, int NR0, template <int> class Blk, int NB, int STRIDE, int O>
 __device__ __forceinline__ void chunk_blocks32(const uint8_t* const (&rows)[NR0], const float* xc,
                                                float2 (&acc)[NR0][M]) {
-    static_for<0, 8>([&](auto bc) {
+    constexpr int CV = 32 * NB;
+    static_for<0, NB>([&](auto bc) {
         constexpr int B = decltype(bc)::value;
-        Blk<B> blk[NR0];
+        Blk<O + STRIDE * B> blk[NR0];
         float d[NR0];
 #pragma unroll
         for (int i = 0; i < NR0; ++i) {
@@ -493,7 +497,7 @@ __device__ __forceinline__ void chunk_blocks32(const uint8_t* const (&rows)[NR0]
             d[i] = blk[i].d;
         }
         float2 c[NR0][M];
-        chain<M, NR0, 8, 256>(c, xc + 32 * B, [&](auto qc, int i, float2& w01, float2& w23) {
+        chain<M, NR0, 8, CV>(c, xc + 32 * B, [&](auto qc, int i, float2& w01, float2& w23) {
             blk[i].template group<decltype(qc)::value>(w01, w23);
         });
         apply_scale<M, NR0>(acc, c, d);
@@ -522,13 +526,6 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
     }
     static_for<0, 4>([&](auto cqc) {
         constexpr int cq = decltype(cqc)::value;
-        uint32_t q[NR0][8];
-#pragma unroll
-        for (int i = 0; i < NR0; ++i) {
-            const uint4 a = lds16(rows[i] + 16 + 32 * cq), b = lds16(rows[i] + 32 + 32 * cq);
-            q[i][0] = a.x; q[i][1] = a.y; q[i][2] = a.z; q[i][3] = a.w;
-            q[i][4] = b.x; q[i][5] = b.y; q[i][6] = b.z; q[i][7] = b.w;
-        }
         static_for<0, 2>([&](auto hc) {
             constexpr int H = decltype(hc)::value;
             constexpr int u = 2 * cq + H;
@@ -539,8 +536,10 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
                 mnv[i] = __fmul_rn(dmin[i], ubyte_f<u & 3>(mnw[i][u >> 2], 0x3Fu));
             }
             float2 c[NR0][M];
+            // the qs word of group Q is read when the chain needs it
             chain<M, NR0, 8, 256>(c, xc + 32 * u, [&](auto qc, int i, float2& w01, float2& w23) {
-                q4k_group<H>(q[i][decltype(qc)::value], w01, w23);
+                const uint32_t v = *reinterpret_cast<const uint32_t*>(rows[i] + 16 + 32 * cq + 4 * decltype(qc)::value);
+                q4k_group<H>(v, w01, w23);
             });
             apply_scale<M, NR0>(acc, c, sc);
 #pragma unroll
@@ -609,12 +608,14 @@ __device__ __forceinline__ void stage_w_plain(uint8_t* dst_rows, const uint8_t* 
     constexpr int BOX = Stage<WT>::kBox;
     uint32_t first, len;  // byte range of the chunk inside the row
     if constexpr (WT == kF16) {
-        first = cc * 272u;
-        len = 2u * min(136u, k - cc * 136u);
-    } else if constexpr (WT == kQ8_0 || WT == kQ5_0) {
-        constexpr uint32_t bb = (WT == kQ8_0) ? 34u : 22u;
-        first = cc * 8u * bb;
-        len = min(8u, k / 32u - cc * 8u) * bb;
+        first = cc * 144u;
+        len = 2u * min(72u, k - cc * 72u);
+    } else if constexpr (WT == kQ8_0) {
+        first = cc * 136u;
+        len = min(4u, k / 32u - cc * 4u) * 34u;
+    } else if constexpr (WT == kQ5_0) {
+        first = cc * 176u;
+        len = min(8u, k / 32u - cc * 8u) * 22u;
     } else if constexpr (WT == kQ4_K) {
         first = cc * 144u;
         len = 144u;
@@ -693,9 +694,10 @@ __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int
     if constexpr (WT == kF16) {
         chunk_f16<M, NR0>(rows, xc, acc);
     } else if constexpr (WT == kQ8_0) {
-        chunk_blocks32<M, NR0, BlkQ8>(rows, xc, acc);
+        if (Stage<WT>::sofs(cc) == 0) chunk_blocks32<M, NR0, BlkQ8, 4, 34, 0>(rows, xc, acc);
+        else chunk_blocks32<M, NR0, BlkQ8, 4, 34, 8>(rows, xc, acc);
     } else if constexpr (WT == kQ5_0) {
-        chunk_blocks32<M, NR0, BlkQ5>(rows, xc, acc);
+        chunk_blocks32<M, NR0, BlkQ5, 8, 22, 0>(rows, xc, acc);
     } else if constexpr (WT == kQ4_K) {
         xsum_q4_k<M>(xc, xs, lane);
         __syncwarp();
@@ -765,8 +767,8 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool fail
 
 // ---------------------------------------------------------------- the kernel
 
-// Persistent kernel (at most 256 weight rows per CTA: 8 consumer warps with
-// one row per lane, 4 with two).  A cluster of `split` CTAs walks the row blocks
+// Persistent kernel (at most 4 consumer warps per CTA: 128 weight rows with
+// one row per lane, 256 with two).  A cluster of `split` CTAs walks the row blocks
 // cid, cid + nclusters, ... (a row block is G row groups of ROWS = 32*NR0
 // rows of one batch); CTA rank s of the cluster handles K range s of every
 // row block.  A CTA has G consumer warps (one row group each) and one
@@ -785,7 +787,7 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool fail
 // barrier split-phase (arrive after issuing a row block, wait one row block
 // later), so it never stalls the stream.
 template <int WT, int M, int NR0>
-__global__ void __launch_bounds__((kMaxWarps / NR0 + 1) * 32)
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32)
 rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
     constexpr int BOX = Stage<WT>::kBox;
     constexpr int CV = Stage<WT>::kValues;
@@ -848,6 +850,9 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     __syncthreads();
 
     if (producer) {
+        // the next kernel of the stream may start its prologue now (it waits
+        // for this one to complete before it touches memory this one writes)
+        pdl_launch_dependents();
         uint32_t i = 0;  // running chunk counter over all row blocks
         bool stop = false;
         uint32_t t = 0;
@@ -898,9 +903,6 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 cluster_arrive();            // phase t
             }
         }
-        // all of this CTA's copies are issued: the next kernel of the stream
-        // may start its prologue (it waits for this one before using memory)
-        pdl_launch_dependents();
         if (S > 1 && t > 0) cluster_wait();
         // every copy issued has landed before the CTA can exit (bounded)
         if (a.aligned && lane == 0) {

@@ -52,7 +52,8 @@ def test_row_bytes_unknown_type(lib):
     ("q4_K", 14336, 4096, 4),    # 448 row groups -> 4
     ("q6_K", 128256, 4096, 1),   # 4008 row groups -> 1
     ("q5_0", 16384, 4096, 4),    # 512 row groups -> 4
-    ("f16", 256, 512, 4),        # 8 groups -> 256, capped by 4 chunks of 136 values
+    ("f16", 256, 512, 8),        # 8 groups -> 256, capped at 8 (8 chunks of 72 values)
+    ("f16", 256, 144, 2),        # 2 chunks of 72 values
     ("q4_K", 32, 256, 1),        # one chunk per row
 ])
 def test_split_factor_from_shape(lib, wt, rows, k, expect):
@@ -86,6 +87,7 @@ CASES = [
     ("batch0", dict(batch=0), "must be > 0"),
     ("split", dict(split=17), "split (17)"),
     ("rows_per_cta", dict(rows_per_cta=48), "rows_per_cta (48)"),
+    ("rows_per_cta256", dict(rows_per_cta=256), "rows_per_cta (256)"),
     ("wtype", dict(wtype=7), "unknown weight type"),
     ("nullW", dict(W=0), "non-null"),
     ("nullx", dict(x=0), "non-null"),
