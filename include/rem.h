@@ -119,6 +119,26 @@ int rem_matvec_ex(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t bat
                   uint32_t split, uint32_t rows_per_cta, void* stream);
 
 /*
+ * rem_matvec_many -- the same product for any number of input rows m >= 1,
+ * the first of the next steps past the few-row limit (ROW_EXACT_MATVEC_MAX_ROWS
+ * in row_exact_matvec.rs caps one dispatch at 8 rows; the matrix-vector regime
+ * extends further, cf. qmv_batch_limit in nuvec-core 0.6.0 src/gpu.rs).  The
+ * m input rows run in groups of up to REM_MAX_ROWS, one launch per group,
+ * each reading W once (ceil(m/8) passes over W).  Rows are independent, so
+ * row j is bitwise the row an m = 1 call with the same split produces.
+ *
+ *   Arguments as rem_matvec_ex (strides in elements, split 0 = automatic from
+ *   (wtype, batch*n, k)) without rows_per_cta.  The output rules apply to all
+ *   m rows; every group is validated before the first launch, so an argument
+ *   error writes nothing.  A CUDA error in a later group leaves the earlier
+ *   groups written.
+ */
+int rem_matvec_many(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch,
+                    const float* x, uint32_t m, uint32_t x_row_stride, uint32_t x_batch_stride,
+                    float* y, uint32_t y_row_stride, uint32_t y_batch_stride,
+                    uint32_t split, void* stream);
+
+/*
  * rem_row_bytes -- bytes of one weight row of k elements
  * (RowExactWeight::row_bytes): F16 2k, Q8_0 k/32*34, Q4_K k/256*144,
  * Q6_K k/256*210, Q5_0 k/32*22.  Returns 0 for an unknown wtype.  Host only.

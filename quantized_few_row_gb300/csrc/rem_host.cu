@@ -237,9 +237,11 @@ struct Shape {
 
 // The argument rules (validate), in the page's order.  Host-only: no CUDA call.
 int validate_args(const void* W, int wt, const float* x, const float* y, const Shape& s, uint32_t split,
-                  uint32_t rows_per_cta) {
+                  uint32_t rows_per_cta, bool any_m = false) {
     if (!valid_wt(wt)) return fail(REM_EINVAL, "rem_matvec: unknown weight type %d", wt);
-    if (s.m == 0 || s.m > kMaxRows) return fail(REM_EINVAL, "rem_matvec: m (%u) must be in 1..=8", s.m);
+    if (s.m == 0 || (!any_m && s.m > kMaxRows))
+        return fail(REM_EINVAL, any_m ? "rem_matvec_many: m (%u) must be >= 1" : "rem_matvec: m (%u) must be in 1..=8",
+                    s.m);
     if (s.n == 0 || s.k == 0 || s.batch == 0)
         return fail(REM_EINVAL, "rem_matvec: n (%u), k (%u) and batch (%u) must be > 0", s.n, s.k, s.batch);
     if (split > REM_MAX_SPLIT)
@@ -469,11 +471,11 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     // before reading x or W into shared memory and before writing y), and
     // prefetches its first weights into L2 meanwhile.  That pays where the
     // launch is short next to its start-up latency -- from m = 4 up (compute
-    // bound) below 256 MB of weights, from m = 2 up below 24 MB -- and costs
+    // bound) below 256 MB of weights, at any m below 24 MB -- and costs
     // throughput on long bandwidth-bound launches, which keep plain stream
     // order.  Scheduling only: the arithmetic is the same either way.
     const uint64_t wbytes = rb * rows;
-    p.pdl = (s.m >= 4 && wbytes <= (256ull << 20)) || (s.m >= 2 && wbytes <= (24ull << 20));
+    p.pdl = (s.m >= 4 && wbytes <= (256ull << 20)) || wbytes <= (24ull << 20);
     if (p.pdl) {
         attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
@@ -568,6 +570,35 @@ int rem_matvec_ex(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t bat
     g_err[0] = '\0';
     const Shape s{m, n, k, batch, x_row_stride, x_batch_stride, y_row_stride, y_batch_stride};
     return launch_matvec(W, wtype, x, y, s, split, rows_per_cta, stream);
+}
+
+int rem_matvec_many(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch, const float* x, uint32_t m,
+                    uint32_t x_row_stride, uint32_t x_batch_stride, float* y, uint32_t y_row_stride,
+                    uint32_t y_batch_stride, uint32_t split, void* stream) {
+    g_err[0] = '\0';
+    const Shape all{m, n, k, batch, x_row_stride, x_batch_stride, y_row_stride, y_batch_stride};
+    // every rule for the whole call (output aliasing over all m rows
+    // included) and every group's rules are checked before the first launch
+    int rc = validate_args(W, wtype, x, y, all, split, 0, true);
+    if (rc != REM_OK) return rc;
+    for (uint32_t j0 = 0; j0 < m; j0 += kMaxRows) {
+        const Shape g{std::min<uint32_t>(kMaxRows, m - j0), n, k, batch, x_row_stride, x_batch_stride,
+                      y_row_stride, y_batch_stride};
+        if ((rc = validate_args(W, wtype, x + static_cast<uint64_t>(j0) * x_row_stride, y +
+                                static_cast<uint64_t>(j0) * y_row_stride, g, split, 0)) != REM_OK)
+            return rc;
+    }
+    // the split comes from the shape, so every group (and an m = 1 call)
+    // uses the same one
+    const uint32_t S = split ? split : auto_split(wtype, static_cast<uint64_t>(batch) * n, k);
+    for (uint32_t j0 = 0; j0 < m; j0 += kMaxRows) {
+        const Shape g{std::min<uint32_t>(kMaxRows, m - j0), n, k, batch, x_row_stride, x_batch_stride,
+                      y_row_stride, y_batch_stride};
+        rc = launch_matvec(W, wtype, x + static_cast<uint64_t>(j0) * x_row_stride,
+                           y + static_cast<uint64_t>(j0) * y_row_stride, g, S, 0, stream);
+        if (rc != REM_OK) return rc;
+    }
+    return REM_OK;
 }
 
 uint64_t rem_row_bytes(int wtype, uint32_t k) { return row_bytes_of(wtype, k); }

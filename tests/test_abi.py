@@ -139,3 +139,26 @@ def test_dequantize_and_quantize_validate(lib):
     assert rem.rem_quantize(X, "q8_0", 0, 256, W, stream=0) == rem.REM_EINVAL
     assert rem.rem_quantize(0, "q8_0", 4, 256, W, stream=0) == rem.REM_EINVAL
     assert "rem_quantize" in rem.rem_last_error()
+
+
+def _many(**kw):
+    a = dict(W=W, wtype="q8_0", n=64, k=256, batch=1, x=X, m=12, x_row_stride=256, x_batch_stride=0,
+             y=Y, y_row_stride=64, y_batch_stride=0, split=0)
+    a.update(kw)
+    return rem.rem_matvec_many(a["W"], a["wtype"], a["n"], a["k"], a["batch"], a["x"], a["m"],
+                               a["x_row_stride"], a["x_batch_stride"], a["y"], a["y_row_stride"],
+                               a["y_batch_stride"], a["split"], stream=0)
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(m=0), "m (0) must be >= 1"),
+    (dict(y_row_stride=63), "overlap"),             # rows 0..11 of 64 outputs overlap
+    (dict(k=100, x_row_stride=100), "multiple of 32"),
+    (dict(split=17), "split (17)"),
+    (dict(m=20, y_row_stride=1 << 28), "exceeds u32"),  # (m-1)*y_row_stride + n past 2^32
+], ids=["m0", "overlap", "k", "split", "extent"])
+def test_many_rows_validation_rejects(lib, kw, msg):
+    """rem_matvec_many checks the rules over all m rows (not only per group of
+    8) before it launches anything; fake pointers are never dereferenced."""
+    assert _many(**kw) == rem.REM_EINVAL
+    assert msg in rem.rem_last_error(), rem.rem_last_error()

@@ -333,3 +333,52 @@ def test_back_to_back_calls_see_previous_writes(fmt, graph):
         s.synchronize()
         for it, o in enumerate(outs):
             assert np.array_equal(o.cpu().numpy().view(np.uint32), ref[it % 2].view(np.uint32)), it
+
+
+# ---------------------------------------------------------------- more than 8 input rows
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_many_rows_match_oracle_and_single_rows(fmt):
+    """rem_matvec_many (groups of 8 input rows) against the oracle, and every
+    row bitwise equal to the same row computed alone and to the same row of an
+    8-row call."""
+    n, k = 200, {"f16": 1088}.get(fmt, 1024)
+    mmax = 24
+    w, x = H.contiguous(fmt, n, k, mmax, 270, 370)
+    alone = [H.run_matvec(w, fmt, n, k, 1, x[j:j + 1], 1, k, 0, n, 0, n, use_ex=False) for j in range(mmax)]
+    eight = H.run_matvec(w, fmt, n, k, 1, x[8:16], 8, k, 0, n, 0, 8 * n, use_ex=False).reshape(8, n)
+    wh, wp = H.to_dev_bytes(w)
+    xd = H.to_dev_f32(x)
+    for m in (9, 12, 16, 17, 24):
+        yd = H.canary(m * n)
+        rem.check(rem.rem_matvec_many(wp, fmt, n, k, 1, xd, m, k, 0, yd, n, 0, 0))
+        torch.cuda.synchronize()
+        y = yd.cpu().numpy().reshape(m, n)
+        y_ref, a_ref = oracle.matvec(w, fmt, n, k, 1, x[:m], m, k, 0)
+        H.assert_close_to_oracle(y.reshape(1, m, n), y_ref, a_ref, f"{fmt} m={m}")
+        for j in range(m):
+            assert np.array_equal(y[j].view(np.uint32), alone[j].view(np.uint32)), (m, j)
+        if m >= 16:
+            assert np.array_equal(y[8:16].view(np.uint32), eight.view(np.uint32)), m
+
+
+@pytest.mark.parametrize("fmt", ["q5_0", "q4_K"])
+def test_many_rows_token_major_grouped(fmt):
+    """Grouped token-major layout (x [m, G*k], y [m, G*n]) with m = 11 tokens:
+    equal to the oracle and bitwise equal to the 8 + 3 split done by hand."""
+    G, n, k, m = 3, 96, 512, 11
+    w = oracle.quantize(inputs.weights(G * n, k, 280), fmt)
+    x = inputs.activations(m, G * k, 380)
+    wh, wp = H.to_dev_bytes(w)
+    xd = H.to_dev_f32(x)
+    yd = H.canary(m * G * n)
+    rem.check(rem.rem_matvec_many(wp, fmt, n, k, G, xd, m, G * k, k, yd, G * n, n, 0))
+    torch.cuda.synchronize()
+    y = yd.cpu().numpy()
+    y_ref, a_ref = oracle.matvec(w, fmt, n, k, G, x, m, G * k, k)
+    H.assert_close_to_oracle(H.gather_y(y, G, m, n, G * n, n), y_ref, a_ref, f"{fmt} grouped m={m}")
+    split = rem.rem_split_factor(fmt, G * n, k)
+    head = H.run_matvec(w, fmt, n, k, G, x[:8], 8, G * k, k, G * n, n, 8 * G * n, split=split)
+    tail = H.run_matvec(w, fmt, n, k, G, x[8:], 3, G * k, k, G * n, n, 3 * G * n, split=split)
+    assert np.array_equal(y[:8 * G * n].view(np.uint32), head.view(np.uint32))
+    assert np.array_equal(y[8 * G * n:].view(np.uint32), tail.view(np.uint32))
