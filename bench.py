@@ -44,7 +44,11 @@ WORKLOADS = {
     "q5_0_grouped_b32_n1024_k4096_m8": ("q5_0", 1024, 4096, 32, [8], True, 8),
     # more than 8 input rows (rem_matvec_many: groups of 8, one pass over W each)
     "q4_K_n14336_k4096_m16,32": ("q4_K", 14336, 4096, 1, [16, 32], False, 9),
+    # fused epilogue y = W.x + bias (rem_matvec_axpby, one bias vector for all rows)
+    "q8_0_n4096_k4096_m1-8_bias": ("q8_0", 4096, 4096, 1, list(range(1, 9)), False, 10),
 }
+# workloads that run the epilogue alpha * W.x + beta * c with c a bias vector
+EPILOGUE = {"q8_0_n4096_k4096_m1-8_bias": (1.0, 1.0)}
 DEFAULT = "q8_0_n4096_k4096_m1-8"
 METRIC = "achieved HBM GB/s (% of GB300 peak) and us/call, m=1..8 quantized mat-vec"
 
@@ -180,7 +184,13 @@ def run_ours(args, rank, world, local_rank):
         xbs, ybs = mmax * k, mmax * n
     torch.cuda.synchronize()
 
+    epi = EPILOGUE.get(args.workload)
+    bias = inputs.torch_normal((batch, n), 3000 + ci, inputs.X_STD, dev) if epi else None
+
     def call(slot, m, stream=None):
+        if epi:
+            return rem.rem_matvec_axpby(wring[slot], fmt, n, k, batch, x, m, k, xbs, y, n, ybs, epi[0], epi[1],
+                                        bias, 0, n, stream)
         if m > 8:
             xrs, yrs = (batch * k, batch * n) if grouped else (k, n)
             return rem.rem_matvec_many(wring[slot], fmt, n, k, batch, x, m, xrs, xbs, y, yrs, ybs, 0, stream)
@@ -228,7 +238,8 @@ def run_ours(args, rank, world, local_rank):
         elapsed = float(t.item())
         torch.distributed.barrier()
 
-    step_bytes = sum(call_bytes(fmt, n, k, batch, m, rb) for m in ms)
+    extra = 4 * batch * n if epi else 0     # the bias vector, read once per call
+    step_bytes = sum(call_bytes(fmt, n, k, batch, m, rb) + extra for m in ms)
     value = world * step_bytes * args.steps / elapsed / 1e9
 
     # per-m device time (cold ring, graph of one call per ring slot)
@@ -286,7 +297,7 @@ def run_ours(args, rank, world, local_rank):
     fp32_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12   # TFLOP/s, plain FMA pipe
     per_m_out = {}
     for m in ms:
-        b = call_bytes(fmt, n, k, batch, m, rb)
+        b = call_bytes(fmt, n, k, batch, m, rb) + extra
         gbs = b / (per_m[m] * 1e-6) / 1e9
         tfl = 2.0 * m * batch * n * k / (per_m[m] * 1e-6) / 1e12
         per_m_out[str(m)] = {"us": round(per_m[m], 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),

@@ -119,6 +119,29 @@ int rem_matvec_ex(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t bat
                   uint32_t split, uint32_t rows_per_cta, void* stream);
 
 /*
+ * rem_matvec_axpby -- y[b, j, :] = alpha * (W[b] . x[b, j, :]) + beta * c[b, j, :],
+ * the fused epilogue of the gemv with an addend (nuvec-core 0.6.0
+ * src/gpu.rs, the gemv "axpby" variant: alpha, beta and the addend's strides
+ * along the output).  Each output is fma(alpha, acc, beta * c) with beta * c
+ * rounded first; with beta == 0 c is not read and y = alpha * acc (so
+ * alpha = 1, beta = 0 is bitwise rem_matvec_ex with split 0).  The epilogue
+ * acts on every output after the fixed reduction, so rows stay exact.
+ *
+ *   x, y, strides   as rem_matvec_ex (automatic split and packing)
+ *   c               F32 addend, element (b, j, i) at
+ *                   b*c_batch_stride + j*c_row_stride + i; c_row_stride = 0
+ *                   broadcasts one bias vector over the m rows,
+ *                   c_batch_stride = 0 over the batch.  c may be y itself
+ *                   with the same strides (y = alpha*W.x + beta*y); any other
+ *                   overlap of c and y is refused.  Ignored when beta == 0.
+ */
+int rem_matvec_axpby(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch,
+                     const float* x, uint32_t m, uint32_t x_row_stride, uint32_t x_batch_stride,
+                     float* y, uint32_t y_row_stride, uint32_t y_batch_stride,
+                     float alpha, float beta, const float* c, uint32_t c_row_stride,
+                     uint32_t c_batch_stride, void* stream);
+
+/*
  * rem_matvec_many -- the same product for any number of input rows m >= 1,
  * the first of the next steps past the few-row limit (ROW_EXACT_MATVEC_MAX_ROWS
  * in row_exact_matvec.rs caps one dispatch at 8 rows; the matrix-vector regime

@@ -18,7 +18,8 @@ import os
 
 __all__ = [
     "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "WTYPES", "REM_OK", "REM_EINVAL", "REM_ELAUNCH", "REM_ECUDA",
-    "RemError", "build", "library_path", "load", "rem_matvec", "rem_matvec_ex", "rem_matvec_many", "rem_row_bytes",
+    "RemError", "build", "library_path", "load", "rem_matvec", "rem_matvec_ex", "rem_matvec_many",
+    "rem_matvec_axpby", "rem_row_bytes",
     "rem_split_factor", "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version", "check",
     "C_FUNCTIONS",
 ]
@@ -26,7 +27,8 @@ __all__ = [
 F16, Q8_0, Q4_K, Q6_K, Q5_0 = 0, 1, 2, 3, 4
 WTYPES = {"f16": F16, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q5_0": Q5_0}
 REM_OK, REM_EINVAL, REM_ELAUNCH, REM_ECUDA = 0, -1, -2, -3
-C_FUNCTIONS = ("rem_matvec", "rem_matvec_ex", "rem_matvec_many", "rem_row_bytes", "rem_split_factor",
+C_FUNCTIONS = ("rem_matvec", "rem_matvec_ex", "rem_matvec_many", "rem_matvec_axpby", "rem_row_bytes",
+               "rem_split_factor",
                "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -66,6 +68,10 @@ def load():
     lib.rem_matvec_ex.restype = i32
     lib.rem_matvec_many.argtypes = [vp, i32, u32, u32, u32, vp, u32, u32, u32, vp, u32, u32, u32, vp]
     lib.rem_matvec_many.restype = i32
+    f32 = ctypes.c_float
+    lib.rem_matvec_axpby.argtypes = [vp, i32, u32, u32, u32, vp, u32, u32, u32, vp, u32, u32, f32, f32, vp, u32,
+                                     u32, vp]
+    lib.rem_matvec_axpby.restype = i32
     lib.rem_row_bytes.argtypes = [i32, u32]
     lib.rem_row_bytes.restype = u64
     lib.rem_split_factor.argtypes = [i32, u32, u32]
@@ -128,6 +134,14 @@ def rem_matvec_many(W, wtype, n: int, k: int, batch: int, x, m: int, x_row_strid
                     y, y_row_stride: int, y_batch_stride: int, split: int = 0, stream=None) -> int:
     return load().rem_matvec_many(_ptr(W), _wt(wtype), n, k, batch, _ptr(x), m, x_row_stride, x_batch_stride,
                                   _ptr(y), y_row_stride, y_batch_stride, split, _stream(stream))
+
+
+def rem_matvec_axpby(W, wtype, n: int, k: int, batch: int, x, m: int, x_row_stride: int, x_batch_stride: int,
+                     y, y_row_stride: int, y_batch_stride: int, alpha: float, beta: float, c=None,
+                     c_row_stride: int = 0, c_batch_stride: int = 0, stream=None) -> int:
+    return load().rem_matvec_axpby(_ptr(W), _wt(wtype), n, k, batch, _ptr(x), m, x_row_stride, x_batch_stride,
+                                   _ptr(y), y_row_stride, y_batch_stride, alpha, beta, _ptr(c), c_row_stride,
+                                   c_batch_stride, _stream(stream))
 
 
 def rem_row_bytes(wtype, k: int) -> int:

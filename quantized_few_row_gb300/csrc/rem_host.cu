@@ -298,8 +298,16 @@ struct Plan {
     bool aligned, pdl;
 };
 
+// Optional epilogue of a launch: y = alpha * acc + beta * c.
+struct Epilogue {
+    uint32_t mode = 0;  // 0 none, 1 alpha only, 2 alpha and beta * c
+    float alpha = 1.0f, beta = 0.0f;
+    const float* c = nullptr;
+    uint32_t crs = 0, cbs = 0;
+};
+
 int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& s, uint32_t split,
-                  uint32_t rows_per_cta, void* stream) {
+                  uint32_t rows_per_cta, void* stream, const Epilogue& epi = Epilogue()) {
     int rc = validate_args(W, wt, x, y, s, split, rows_per_cta);
     if (rc != REM_OK) return rc;
     const uint64_t rb = row_bytes_of(wt, s.k);
@@ -507,6 +515,12 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     a.aligned = p.aligned ? 1u : 0u;
     a.x_bm = x_bm ? 1u : 0u;
     a.pdl = p.pdl ? 1u : 0u;
+    a.epi = epi.mode;
+    a.alpha = epi.alpha;
+    a.beta = epi.beta;
+    a.c = epi.c;
+    a.crs = epi.crs;
+    a.cbs = epi.cbs;
 
     void* args[3] = {&wmap, &xmap, &a};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
@@ -570,6 +584,44 @@ int rem_matvec_ex(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t bat
     g_err[0] = '\0';
     const Shape s{m, n, k, batch, x_row_stride, x_batch_stride, y_row_stride, y_batch_stride};
     return launch_matvec(W, wtype, x, y, s, split, rows_per_cta, stream);
+}
+
+int rem_matvec_axpby(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch, const float* x, uint32_t m,
+                     uint32_t x_row_stride, uint32_t x_batch_stride, float* y, uint32_t y_row_stride,
+                     uint32_t y_batch_stride, float alpha, float beta, const float* c, uint32_t c_row_stride,
+                     uint32_t c_batch_stride, void* stream) {
+    g_err[0] = '\0';
+    const Shape s{m, n, k, batch, x_row_stride, x_batch_stride, y_row_stride, y_batch_stride};
+    Epilogue e;
+    e.alpha = alpha;
+    e.beta = beta;
+    if (beta != 0.0f) {
+        if (!c || reinterpret_cast<uintptr_t>(c) % 4 != 0)
+            return fail(REM_EINVAL, "rem_matvec: c must be non-null and 4-byte aligned when beta != 0");
+        // c may be y itself (same strides: each element is read, then written, by one thread);
+        // any other overlap between c and y is refused
+        const uint64_t cext = 4 * strided_extent(batch, c_batch_stride, m, c_row_stride, n);
+        const uint64_t yext = 4 * strided_extent(batch, y_batch_stride, m, y_row_stride, n);
+        const uintptr_t c0 = reinterpret_cast<uintptr_t>(c), y0 = reinterpret_cast<uintptr_t>(y);
+        const bool same = c0 == y0 && c_row_stride == y_row_stride && c_batch_stride == y_batch_stride;
+        if (!same && c0 < y0 + yext && y0 < c0 + cext)
+            return fail(REM_EINVAL, "rem_matvec: c overlaps y (only c == y with the same strides is allowed)");
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(REM_ECUDA, "rem_matvec: no current CUDA device");
+        }
+        int rc = validate_args(W, wtype, x, y, s, 0, 0);
+        if (rc != REM_OK) return rc;
+        if ((rc = check_buffer(c, cext, "addend c", dev)) != REM_OK) return rc;
+        e.mode = 2;
+        e.c = c;
+        e.crs = c_row_stride;
+        e.cbs = c_batch_stride;
+    } else if (alpha != 1.0f) {
+        e.mode = 1;
+    }
+    return launch_matvec(W, wtype, x, y, s, 0, 0, stream, e);
 }
 
 int rem_matvec_many(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch, const float* x, uint32_t m,

@@ -56,6 +56,11 @@ struct MvArgs {
     uint32_t aligned;        // 1: TMA staging (16-byte aligned rows, encodable input map)
     uint32_t x_bm;           // input map dimension order: 1 = [k, batch, m] (token-major), 0 = [k, m, batch]
     uint32_t pdl;            // 1: launched as a programmatic dependent of the stream's previous kernel
+    // epilogue: 0 = y = acc; 1 = y = alpha*acc; 2 = y = fma(alpha, acc, beta*c)
+    uint32_t epi;
+    float alpha, beta;
+    const float* c;          // addend, element (b, j, i) at b*cbs + j*crs + i (read only when epi == 2)
+    uint32_t crs, cbs;
 };
 
 // Kernel lookup: rem_mv_kernel<wt, m, nr0>, m in 1..8, nr0 in {1, 2}.

@@ -726,9 +726,18 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool fail
 #pragma unroll
         for (int j = 0; j < M; ++j)
             part[i][j] = failed ? __int_as_float(0x7FC00000) : __fadd_rn(acc[i][j].x, acc[i][j].y);
+    // the store, with the optional epilogue alpha * acc + beta * c (each output
+    // element on its own, after the fixed reduction: row exactness is kept)
     auto store = [&](int i, int j, float v) {
         const uint32_t row = wrow0 + static_cast<uint32_t>(lane + 32 * i);
-        if (row < a.n) a.y[static_cast<uint64_t>(b) * a.ybs + static_cast<uint64_t>(j) * a.yrs + row] = v;
+        if (row >= a.n) return;
+        if (a.epi == 1) {
+            v = __fmul_rn(a.alpha, v);
+        } else if (a.epi == 2) {
+            const float cv = a.c[static_cast<uint64_t>(b) * a.cbs + static_cast<uint64_t>(j) * a.crs + row];
+            v = __fmaf_rn(a.alpha, v, __fmul_rn(a.beta, cv));
+        }
+        a.y[static_cast<uint64_t>(b) * a.ybs + static_cast<uint64_t>(j) * a.yrs + row] = v;
     };
     if (S == 1) {
         if (wactive) {

@@ -162,3 +162,28 @@ def test_many_rows_validation_rejects(lib, kw, msg):
     8) before it launches anything; fake pointers are never dereferenced."""
     assert _many(**kw) == rem.REM_EINVAL
     assert msg in rem.rem_last_error(), rem.rem_last_error()
+
+
+def _axpby(**kw):
+    a = dict(W=W, wtype="q8_0", n=64, k=256, batch=1, x=X, m=2, x_row_stride=256, x_batch_stride=0,
+             y=Y, y_row_stride=64, y_batch_stride=0, alpha=2.0, beta=0.5, c=0x400000, c_row_stride=64,
+             c_batch_stride=0)
+    a.update(kw)
+    return rem.rem_matvec_axpby(a["W"], a["wtype"], a["n"], a["k"], a["batch"], a["x"], a["m"],
+                                a["x_row_stride"], a["x_batch_stride"], a["y"], a["y_row_stride"],
+                                a["y_batch_stride"], a["alpha"], a["beta"], a["c"], a["c_row_stride"],
+                                a["c_batch_stride"], stream=0)
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(c=0), "c must be non-null"),
+    (dict(c=0x400002), "c must be non-null and 4-byte aligned"),
+    (dict(c=Y + 4), "c overlaps y"),                       # shifted by one element
+    (dict(c=Y, c_row_stride=0), "c overlaps y"),           # same base, other strides
+], ids=["null", "misaligned", "shifted", "strides"])
+def test_axpby_addend_rules(lib, kw, msg):
+    """The addend is checked before anything else happens: non-null and
+    aligned when beta != 0, and either disjoint from y or y itself with the
+    same strides."""
+    assert _axpby(**kw) == rem.REM_EINVAL
+    assert msg in rem.rem_last_error(), rem.rem_last_error()

@@ -382,3 +382,78 @@ def test_many_rows_token_major_grouped(fmt):
     tail = H.run_matvec(w, fmt, n, k, G, x[8:], 3, G * k, k, G * n, n, 3 * G * n, split=split)
     assert np.array_equal(y[:8 * G * n].view(np.uint32), head.view(np.uint32))
     assert np.array_equal(y[8 * G * n:].view(np.uint32), tail.view(np.uint32))
+
+
+# ---------------------------------------------------------------- fused epilogue alpha * W.x + beta * c
+
+def _fma_f32(a, b, c):
+    """Correctly rounded binary32 fma(a, b, c) from exact rational arithmetic."""
+    from fractions import Fraction
+    r = Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c))
+    f = np.float32(float(r))
+    cands = [np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))]
+    return min(cands, key=lambda v: (abs(Fraction(float(v)) - r), int(np.float32(v).view(np.uint32)) & 1))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_axpby_matches_oracle_and_exact_epilogue(fmt):
+    n, k, m = 150, {"f16": 1088}.get(fmt, 1024), 5
+    w, x = H.contiguous(fmt, n, k, m, 290, 390)
+    c = inputs.activations(m, n, 490)
+    alpha, beta = np.float32(-1.75), np.float32(0.3)
+    wh, wp = H.to_dev_bytes(w)
+    xd = H.to_dev_f32(x)
+    cd = H.to_dev_f32(c)
+    plain = H.canary(m * n)
+    rem.check(rem.rem_matvec_ex(wp, fmt, n, k, 1, xd, m, k, 0, plain, n, 0, 0, 0))
+    yd = H.canary(m * n)
+    rem.check(rem.rem_matvec_axpby(wp, fmt, n, k, 1, xd, m, k, 0, yd, n, 0, float(alpha), float(beta), cd, n, 0))
+    torch.cuda.synchronize()
+    y = yd.cpu().numpy().reshape(m, n)
+    p = plain.cpu().numpy().reshape(m, n)
+    # against the oracle: alpha * y_ref + beta * c in f64, the product's tolerance scaled
+    # by |alpha| plus two binary32 roundings of the epilogue
+    y_ref, a_ref = oracle.matvec(w, fmt, n, k, 1, x, m, k, 0)
+    ref = float(alpha) * y_ref[0] + float(beta) * c.astype(np.float64)
+    tol = abs(float(alpha)) * (1e-4 * a_ref[0] + 1e-7) + 2.0 ** -22 * (np.abs(float(alpha) * y_ref[0]) +
+                                                                       np.abs(float(beta) * c))
+    assert np.all(np.abs(y - ref) <= tol), np.max(np.abs(y - ref) - tol)
+    # the epilogue is exactly fma(alpha, acc, fl(beta * c)) on the plain result
+    g = np.random.Generator(np.random.PCG64(7))
+    for j, i in zip(g.integers(0, m, 200), g.integers(0, n, 200)):
+        expect = _fma_f32(alpha, p[j, i], np.float32(beta) * np.float32(c[j, i]))
+        assert y[j, i].view(np.uint32) == np.float32(expect).view(np.uint32), (j, i)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_K", "f16"])
+def test_axpby_special_cases(fmt):
+    """alpha = 1, beta = 0 is the plain call bitwise; beta = 0 reads no c;
+    c == y accumulates in place; c_row_stride = 0 broadcasts one bias vector."""
+    n, k, m = 130, {"f16": 1088}.get(fmt, 1024), 3
+    w, x = H.contiguous(fmt, n, k, m, 291, 391)
+    wh, wp = H.to_dev_bytes(w)
+    xd = H.to_dev_f32(x)
+    plain = H.canary(m * n)
+    rem.check(rem.rem_matvec_ex(wp, fmt, n, k, 1, xd, m, k, 0, plain, n, 0, 0, 0))
+    nan_c = torch.full((m * n,), float("nan"), device=H.dev())
+    y1 = H.canary(m * n)
+    rem.check(rem.rem_matvec_axpby(wp, fmt, n, k, 1, xd, m, k, 0, y1, n, 0, 1.0, 0.0, nan_c, n, 0))
+    y2 = H.canary(m * n)
+    rem.check(rem.rem_matvec_axpby(wp, fmt, n, k, 1, xd, m, k, 0, y2, n, 0, 0.5, 0.0, None, 0, 0))
+    bias = inputs.activations(1, n, 492)[0]
+    bd = H.to_dev_f32(bias)
+    y3 = H.canary(m * n)
+    rem.check(rem.rem_matvec_axpby(wp, fmt, n, k, 1, xd, m, k, 0, y3, n, 0, 1.0, 1.0, bd, 0, 0))
+    acc = H.to_dev_f32(inputs.activations(m, n, 493))
+    acc0 = acc.cpu().numpy().reshape(m, n)
+    rem.check(rem.rem_matvec_axpby(wp, fmt, n, k, 1, xd, m, k, 0, acc, n, 0, 2.0, -1.0, acc, n, 0))
+    torch.cuda.synchronize()
+    p = plain.cpu().numpy().reshape(m, n)
+    assert np.array_equal(y1.cpu().numpy().view(np.uint32), plain.cpu().numpy().view(np.uint32))
+    assert np.array_equal(y2.cpu().numpy().reshape(m, n), p * np.float32(0.5))
+    assert np.array_equal(y3.cpu().numpy().reshape(m, n), p + bias[None, :])   # fma(1, acc, b) = acc + b
+    g = np.random.Generator(np.random.PCG64(8))
+    got = acc.cpu().numpy().reshape(m, n)
+    for j, i in zip(g.integers(0, m, 100), g.integers(0, n, 100)):
+        expect = _fma_f32(np.float32(2.0), p[j, i], -acc0[j, i])
+        assert got[j, i].view(np.uint32) == np.float32(expect).view(np.uint32), (j, i)
