@@ -29,8 +29,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "rem_oracle.c")
 _LIB = os.path.join(_HERE, "librem_oracle.so")
 
-F16, Q8_0, Q4_K, Q6_K, Q5_0 = 0, 1, 2, 3, 4
-WTYPES = {"f16": F16, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q5_0": Q5_0}
+F16, Q8_0, Q4_K, Q6_K, Q5_0, F32, BF16 = 0, 1, 2, 3, 4, 5, 6
+WTYPES = {"f16": F16, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q5_0": Q5_0, "f32": F32, "bf16": BF16}
 
 _lib = None
 
@@ -71,6 +71,10 @@ def _load():
     lib.rem_oracle_h2f_array.restype = None
     lib.rem_oracle_f2h_array.argtypes = [f32p, u16p, ctypes.c_uint64, ctypes.c_int]
     lib.rem_oracle_f2h_array.restype = None
+    lib.rem_oracle_bf2f_array.argtypes = [u16p, f32p, ctypes.c_uint64]
+    lib.rem_oracle_bf2f_array.restype = None
+    lib.rem_oracle_f2bf_array.argtypes = [f32p, u16p, ctypes.c_uint64]
+    lib.rem_oracle_f2bf_array.restype = None
     lib.rem_oracle_dequantize.argtypes = [u8p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint32, f32p]
     lib.rem_oracle_dequantize.restype = ctypes.c_int
     lib.rem_oracle_quantize.argtypes = [f32p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint32, u8p]
@@ -123,6 +127,22 @@ def f2h(f: np.ndarray, mode: str = "rn") -> np.ndarray:
     out = np.empty(f.shape, dtype=np.uint16)
     _load().rem_oracle_f2h_array(_ptr(f, ctypes.c_float), _ptr(out, ctypes.c_uint16), f.size,
                                  {"rn": 0, "ru": 1}[mode])
+    return out
+
+
+def bf2f(b: np.ndarray) -> np.ndarray:
+    """Exact bfloat16 -> binary32 widening of uint16 bit patterns."""
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float32)
+    _load().rem_oracle_bf2f_array(_ptr(b, ctypes.c_uint16), _ptr(out, ctypes.c_float), b.size)
+    return out
+
+
+def f2bf(f: np.ndarray) -> np.ndarray:
+    """binary32 -> bfloat16 bit patterns, round to nearest even."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.empty(f.shape, dtype=np.uint16)
+    _load().rem_oracle_f2bf_array(_ptr(f, ctypes.c_float), _ptr(out, ctypes.c_uint16), f.size)
     return out
 
 
@@ -194,6 +214,6 @@ def within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, a_ref: np.ndarray,
     return ok
 
 
-__all__ = ["build", "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "WTYPES", "block_values", "block_bytes",
-           "row_bytes", "threads", "h2f", "f2h", "quantize", "dequantize", "matvec", "matvec_rows",
+__all__ = ["build", "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16", "WTYPES", "block_values", "block_bytes",
+           "row_bytes", "threads", "h2f", "f2h", "bf2f", "f2bf", "quantize", "dequantize", "matvec", "matvec_rows",
            "within_tolerance", "wtype_of"]

@@ -28,6 +28,12 @@
  * Quantizers (test-data generators, reading 3) round x/d with roundf (ties
  * away from zero) against the stored fp16 scale.  Parity only depends on
  * the bytes they produce.
+ *
+ * Dense weights (the row-independent gemv of nuvec-core 0.6.0 src/gpu.rs,
+ * gemv_rows: F32, F16 and BF16 matrices under the same row contract):
+ *   F32   4 B : one binary32 per element
+ *   BF16  2 B : the upper 16 bits of a binary32 (widening is exact; the
+ *               "quantizer" rounds binary32 to nearest even)
  */
 #include <math.h>
 #include <stdint.h>
@@ -37,7 +43,7 @@
 #include <omp.h>
 #endif
 
-enum { W_F16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_Q6_K = 3, W_Q5_0 = 4 };
+enum { W_F16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_Q6_K = 3, W_Q5_0 = 4, W_F32 = 5, W_BF16 = 6 };
 
 /* ------------------------------------------------------------------ */
 /* Block constants (row_exact_matvec.rs, the *_BLOCK_* constants).     */
@@ -46,6 +52,8 @@ enum { W_F16 = 0, W_Q8_0 = 1, W_Q4_K = 2, W_Q6_K = 3, W_Q5_0 = 4 };
 int rem_oracle_block_values(int wtype) {
     switch (wtype) {
     case W_F16: return 1;
+    case W_F32: return 1;
+    case W_BF16: return 1;
     case W_Q8_0: return 32;
     case W_Q5_0: return 32;
     case W_Q4_K: return 256;
@@ -57,6 +65,8 @@ int rem_oracle_block_values(int wtype) {
 int rem_oracle_block_bytes(int wtype) {
     switch (wtype) {
     case W_F16: return 2;
+    case W_F32: return 4;
+    case W_BF16: return 2;
     case W_Q8_0: return 34;
     case W_Q5_0: return 22;
     case W_Q4_K: return 144;
@@ -157,6 +167,29 @@ static uint16_t f2h_mode(float f, int mode) {
 }
 
 uint16_t rem_oracle_f2h_rn(float f) { return f2h_mode(f, 0); }
+
+/* bfloat16: the upper half of a binary32 bit pattern. */
+static uint32_t f2u(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return u;
+}
+static float u2f(uint32_t u) {
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+float rem_oracle_bf2f(uint16_t b) { return u2f((uint32_t)b << 16); }
+
+/* binary32 -> bfloat16, round to nearest, ties to even on the 16 dropped
+ * bits; NaN stays NaN (quiet bit set), infinities stay infinite. */
+uint16_t rem_oracle_f2bf_rn(float f) {
+    uint32_t u = f2u(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0) return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep = u >> 16, rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;  /* carries into the exponent */
+    return (uint16_t)keep;
+}
 uint16_t rem_oracle_f2h_ru(float f) { return f2h_mode(f, 1); }
 
 static uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
@@ -245,6 +278,15 @@ static void deq_row(int wtype, const uint8_t* row, uint32_t k, float* out) {
     switch (wtype) {
     case W_F16:
         for (uint32_t e = 0; e < k; ++e) out[e] = rem_oracle_h2f(rd16(row + 2 * e));
+        break;
+    case W_BF16:
+        for (uint32_t e = 0; e < k; ++e) out[e] = rem_oracle_bf2f(rd16(row + 2 * e));
+        break;
+    case W_F32:
+        for (uint32_t e = 0; e < k; ++e) {
+            const uint8_t* p = row + 4 * e;
+            out[e] = u2f((uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24));
+        }
         break;
     case W_Q8_0:
         for (uint32_t blk = 0; blk < k / 32; ++blk) deq_q8_0(row + 34 * blk, out + 32 * blk);
@@ -433,6 +475,13 @@ int rem_oracle_quantize(const float* src, int wtype, uint32_t rows, uint32_t k, 
             const float* vb = v + (uint64_t)blk * bv;
             switch (wtype) {
             case W_F16: wr16(row + 2 * blk, rem_oracle_f2h_rn(vb[0])); break;
+            case W_BF16: wr16(row + 2 * blk, rem_oracle_f2bf_rn(vb[0])); break;
+            case W_F32: {
+                uint32_t u = f2u(vb[0]);
+                uint8_t* p = row + 4 * blk;
+                p[0] = (uint8_t)u; p[1] = (uint8_t)(u >> 8); p[2] = (uint8_t)(u >> 16); p[3] = (uint8_t)(u >> 24);
+                break;
+            }
             case W_Q8_0: quant_q8_0(vb, row + 34 * blk); break;
             case W_Q5_0: quant_q5_0(vb, row + 22 * blk); break;
             case W_Q4_K: quant_q4_k(vb, row + 144 * blk); break;
@@ -508,4 +557,10 @@ void rem_oracle_h2f_array(const uint16_t* h, float* out, uint64_t count) {
 }
 void rem_oracle_f2h_array(const float* f, uint16_t* out, uint64_t count, int mode) {
     for (uint64_t i = 0; i < count; ++i) out[i] = f2h_mode(f[i], mode);
+}
+void rem_oracle_bf2f_array(const uint16_t* b, float* out, uint64_t count) {
+    for (uint64_t i = 0; i < count; ++i) out[i] = rem_oracle_bf2f(b[i]);
+}
+void rem_oracle_f2bf_array(const float* f, uint16_t* out, uint64_t count) {
+    for (uint64_t i = 0; i < count; ++i) out[i] = rem_oracle_f2bf_rn(f[i]);
 }

@@ -340,3 +340,61 @@ def test_sampled_rows_equal_full_rows(orc):
         b, i = divmod(int(r), n)
         assert np.array_equal(ys[c], yf[b, :, i])
         assert np.array_equal(as_[c], af[b, :, i])
+
+
+# ---------------------------------------------------------------- dense BF16 / F32 weights
+
+def test_dense_row_bytes(orc):
+    # one IEEE binary32 (4 B) or bfloat16 (2 B) per element
+    for k in (4, 256, 4096):
+        assert orc.row_bytes("f32", k) == 4 * k
+        assert orc.row_bytes("bf16", k) == 2 * k
+    assert orc.block_values("bf16") == 1 and orc.block_bytes("bf16") == 2
+    assert orc.block_values("f32") == 1 and orc.block_bytes("f32") == 4
+
+
+def test_bf2f_all_patterns_match_library(orc):
+    import torch
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = orc.bf2f(b)
+    ref = torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_f2bf_nearest_even_matches_library(orc):
+    import torch
+    g = np.random.Generator(np.random.PCG64(11))
+    b = g.integers(0, 0x7F7F, 20000).astype(np.uint16)
+    lo = orc.bf2f(b).astype(np.float64)
+    hi = orc.bf2f((b + 1).astype(np.uint16)).astype(np.float64)
+    halfway = ((lo + hi) / 2).astype(np.float32)     # exact in binary32: ties to even decide
+    v = np.concatenate([_f32_probe_values(), halfway, -halfway,
+                        np.array([3.4e38, -3.4e38, 1e-40, -1e-40], np.float32)])
+    ours = orc.f2bf(v)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    nan_bits = orc.f2bf(np.array([np.nan], np.float32))
+    assert np.isnan(orc.bf2f(nan_bits))[0]
+
+
+def test_dense_quantize_dequantize(orc):
+    v = inputs.weights(3, 64, 50)
+    assert np.array_equal(orc.dequantize(orc.quantize(v, "f32"), "f32", 3, 64).view(np.uint32), v.view(np.uint32))
+    bf = orc.dequantize(orc.quantize(v, "bf16"), "bf16", 3, 64)
+    assert np.array_equal(orc.f2bf(bf), orc.f2bf(v))            # bf16 values, re-rounding is exact
+    assert np.all(np.abs(bf - v) <= np.abs(v) * 2.0 ** -8)      # half an ulp of an 8-bit significand
+
+
+@pytest.mark.parametrize("fmt,k", [("f32", 64), ("bf16", 96)])
+def test_dense_brute_force_rational(orc, fmt, k):
+    n, m = 3, 4
+    blocks = orc.quantize(inputs.weights(n, k, 42), fmt)
+    wf = orc.dequantize(blocks, fmt, n, k)
+    x = inputs.activations(m, k, 43)
+    y, a = orc.matvec(blocks, fmt, n, k, 1, x, m, k, 0)
+    for i in range(n):
+        for j in range(m):
+            exact = sum(Fraction(float(wf[i, kk])) * Fraction(float(x[j, kk])) for kk in range(k))
+            assert abs(Fraction(y[0, j, i]) - exact) <= Fraction(k * 2.0 ** -52) * Fraction(a[0, j, i])
