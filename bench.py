@@ -44,6 +44,9 @@ WORKLOADS = {
     "q5_0_grouped_b32_n1024_k4096_m8": ("q5_0", 1024, 4096, 32, [8], True, 8),
     # more than 8 input rows (rem_matvec_many: groups of 8, one pass over W each)
     "q4_K_n14336_k4096_m16,32": ("q4_K", 14336, 4096, 1, [16, 32], False, 9),
+    # dense weights under the same row contract
+    "bf16_n8192_k4096_m1-8": ("bf16", 8192, 4096, 1, list(range(1, 9)), False, 11),
+    "f32_n4096_k4096_m1-8": ("f32", 4096, 4096, 1, list(range(1, 9)), False, 12),
     # fused epilogue y = W.x + bias (rem_matvec_axpby, one bias vector for all rows)
     "q8_0_n4096_k4096_m1-8_bias": ("q8_0", 4096, 4096, 1, list(range(1, 9)), False, 10),
 }

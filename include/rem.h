@@ -48,8 +48,12 @@ typedef enum {
                       6-bit scales/mins | 128 B nibbles                        */
     REM_Q6_K = 3,  /* [batch*n, k/256] blocks of 210 B: 128 B low nibbles |
                       64 B high 2-bit | int8 scales[16] | d f16                */
-    REM_Q5_0 = 4   /* [batch*n, k/32] blocks of 22 B: d f16 | u32 high bits |
+    REM_Q5_0 = 4,  /* [batch*n, k/32] blocks of 22 B: d f16 | u32 high bits |
                       16 B nibbles                                             */
+    /* dense weights under the same row contract (the row-independent gemv of
+       nuvec-core 0.6.0 src/gpu.rs, gemv_rows over F32 / F16 / BF16 matrices) */
+    REM_F32 = 5,   /* row-major [batch*n, k] IEEE binary32, little-endian     */
+    REM_BF16 = 6   /* row-major [batch*n, k] bfloat16 (upper half of binary32) */
 } rem_wtype;
 
 /* Status codes. */
@@ -71,11 +75,11 @@ typedef enum {
  *
  *   W       device pointer to batch*n weight rows of rem_row_bytes(wtype, k)
  *           bytes each, row-major, batch-major.  Alignment: F16 8 B, Q8_0 2 B,
- *           Q4_K 16 B, Q6_K 2 B, Q5_0 2 B.
+ *           Q4_K 16 B, Q6_K 2 B, Q5_0 2 B, F32 4 B, BF16 8 B.
  *   wtype   a rem_wtype value.
  *   n, k    output columns per batch (= weight rows per batch) and inner
- *           dimension; k must be a multiple of 4 (F16), 32 (Q8_0, Q5_0) or
- *           256 (Q4_K, Q6_K).
+ *           dimension; k must be a multiple of 4 (F16, F32, BF16), 32 (Q8_0,
+ *           Q5_0) or 256 (Q4_K, Q6_K).
  *   batch   independent products, >= 1.
  *   x       device F32 input, 16-byte aligned.
  *   m       input rows, 1..8.
@@ -164,7 +168,8 @@ int rem_matvec_many(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t b
 /*
  * rem_row_bytes -- bytes of one weight row of k elements
  * (RowExactWeight::row_bytes): F16 2k, Q8_0 k/32*34, Q4_K k/256*144,
- * Q6_K k/256*210, Q5_0 k/32*22.  Returns 0 for an unknown wtype.  Host only.
+ * Q6_K k/256*210, Q5_0 k/32*22; F32 4k, BF16 2k.  Returns 0 for an unknown
+ * wtype.  Host only.
  */
 uint64_t rem_row_bytes(int wtype, uint32_t k);
 
@@ -174,8 +179,8 @@ uint64_t rem_row_bytes(int wtype, uint32_t k);
  * row_exact_reduction_nsg followed by the device cap of
  * RowExactMatvecSchedule::for_device).  It depends on (wtype, rows, k) only:
  * a power of two so that rows/32 * split reaches about 2048, at most the
- * number of chunks of a row (72 F16 values, 4 Q8_0 blocks, 8 Q5_0 blocks,
- * one Q4_K / Q6_K super-block) and at most REM_MAX_CLUSTER_SPLIT (8): the
+ * number of chunks of a row (72 F16 or BF16 values, 36 F32 values, 4 Q8_0
+ * blocks, 8 Q5_0 blocks, one Q4_K / Q6_K super-block) and at most REM_MAX_CLUSTER_SPLIT (8): the
  * split ranges of a row run as the thread blocks of one cluster, and 8 is
  * the portable cluster size (the page's device cap on threads per
  * threadgroup becomes this cap).  Returns 0 for an unknown wtype or

@@ -17,15 +17,15 @@ import ctypes
 import os
 
 __all__ = [
-    "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "WTYPES", "REM_OK", "REM_EINVAL", "REM_ELAUNCH", "REM_ECUDA",
+    "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16", "WTYPES", "REM_OK", "REM_EINVAL", "REM_ELAUNCH", "REM_ECUDA",
     "RemError", "build", "library_path", "load", "rem_matvec", "rem_matvec_ex", "rem_matvec_many",
     "rem_matvec_axpby", "rem_row_bytes",
     "rem_split_factor", "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version", "check",
     "C_FUNCTIONS",
 ]
 
-F16, Q8_0, Q4_K, Q6_K, Q5_0 = 0, 1, 2, 3, 4
-WTYPES = {"f16": F16, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q5_0": Q5_0}
+F16, Q8_0, Q4_K, Q6_K, Q5_0, F32, BF16 = 0, 1, 2, 3, 4, 5, 6
+WTYPES = {"f16": F16, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q5_0": Q5_0, "f32": F32, "bf16": BF16}
 REM_OK, REM_EINVAL, REM_ELAUNCH, REM_ECUDA = 0, -1, -2, -3
 C_FUNCTIONS = ("rem_matvec", "rem_matvec_ex", "rem_matvec_many", "rem_matvec_axpby", "rem_row_bytes",
                "rem_split_factor",

@@ -1,11 +1,13 @@
 // rem_aux.cu -- exact dequantization and round-to-nearest quantization of
 // the weight formats of mlx-native 0.18.0 src/ops/row_exact_matvec.rs
-// (RowExactWeight: F16, Q8_0, Q4_K, Q6_K, Q5_0), on the GPU.
+// (RowExactWeight: F16, Q8_0, Q4_K, Q6_K, Q5_0) and of the dense F32 / BF16
+// weights of the row-independent gemv (nuvec-core 0.6.0 src/gpu.rs), on the GPU.
 //
 // Every floating-point step is an explicitly rounded intrinsic
 // (__fmul_rn, __fsub_rn, __fdiv_rn, __fadd_rn), so the results do not depend
 // on contraction or on the compiler: a dequantized value is
 //   F16  the binary16 value          Q8_0  d*q          Q5_0  d*(q-16)
+//   F32  the binary32 value          BF16  the upper half of a binary32
 //   Q4_K (d*sc)*q - dmin*mn          Q6_K  (d*sc)*(q-32)
 // and a quantized code is roundf(x / stored_scale), clamped.
 #include <cuda_fp16.h>
@@ -34,11 +36,21 @@ __device__ __forceinline__ void wr16(uint8_t* p, uint32_t v) {
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 __device__ __forceinline__ uint32_t h_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }
 __device__ __forceinline__ uint32_t h_ru(float f) { return __half_as_ushort(__float2half_ru(f)); }
+// binary32 -> bfloat16 bits, round to nearest even on the 16 dropped bits;
+// a NaN keeps its upper bits with the quiet bit set.
+__device__ __forceinline__ uint32_t bf_rn(float f) {
+    const uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u) return (u >> 16) | 0x0040u;
+    uint32_t keep = u >> 16;
+    const uint32_t rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;
+    return keep & 0xFFFFu;
+}
 
 // ---------------------------------------------------------------- dequantize
 
 // One thread per group of 32 values (a Q8_0 / Q5_0 block, a Q4_K sub-block,
-// two Q6_K sub-blocks, or 32 F16 values).
+// two Q6_K sub-blocks, or 32 F16 / F32 / BF16 values).
 __global__ void dequant_kernel(const uint8_t* __restrict__ w, int wt, uint64_t rows, uint32_t k,
                                uint64_t row_bytes, float* __restrict__ out) {
     const uint64_t groups_per_row = (k + 31u) / 32u;  // F16 rows may end in a partial group
@@ -51,6 +63,12 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ w, int wt, uint64_t r
     if (wt == kF16) {
         const uint32_t nv = min(32u, k - 32u * gi);
         for (uint32_t e = 0; e < nv; ++e) o[e] = h2f(rd16(row + 2u * (32u * gi + e)));
+    } else if (wt == kBF16) {
+        const uint32_t nv = min(32u, k - 32u * gi);
+        for (uint32_t e = 0; e < nv; ++e) o[e] = __uint_as_float(rd16(row + 2u * (32u * gi + e)) << 16);
+    } else if (wt == kF32) {
+        const uint32_t nv = min(32u, k - 32u * gi);
+        for (uint32_t e = 0; e < nv; ++e) o[e] = __uint_as_float(rd32(row + 4u * (32u * gi + e)));
     } else if (wt == kQ8_0) {
         const uint8_t* b = row + 34u * gi;
         const float d = h2f(rd16(b));
@@ -243,7 +261,7 @@ __device__ void quant_q6_k(const float* v, uint8_t* b) {
     wr16(b + 208, dh);
 }
 
-// One thread per block (per value for F16).
+// One thread per block (per value for F16, F32 and BF16).
 __global__ void quant_kernel(const float* __restrict__ src, int wt, uint64_t rows, uint32_t k, uint64_t row_bytes,
                              uint8_t* __restrict__ w) {
     const uint32_t bv = static_cast<uint32_t>(block_values(wt));
@@ -256,6 +274,8 @@ __global__ void quant_kernel(const float* __restrict__ src, int wt, uint64_t row
     uint8_t* b = w + r * row_bytes + static_cast<uint64_t>(bi) * block_bytes(wt);
     switch (wt) {
     case kF16: wr16(b, h_rn(v[0])); break;
+    case kBF16: wr16(b, bf_rn(v[0])); break;
+    case kF32: *reinterpret_cast<uint32_t*>(b) = __float_as_uint(v[0]); break;
     case kQ8_0: quant_q8_0(v, b); break;
     case kQ5_0: quant_q5_0(v, b); break;
     case kQ4_K: quant_q4_k(v, b); break;

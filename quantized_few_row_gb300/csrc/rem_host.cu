@@ -40,7 +40,7 @@ int fail(int code, const char* fmt, ...) {
 bool valid_wt(int wt) { return wt >= 0 && wt < kNumWt; }
 
 const char* wt_name(int wt) {
-    static const char* names[] = {"F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0"};
+    static const char* names[] = {"F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16"};
     return valid_wt(wt) ? names[wt] : "?";
 }
 
@@ -51,7 +51,7 @@ uint64_t row_bytes_of(int wt, uint32_t k) {
 
 uint32_t k_multiple(int wt) {
     switch (wt) {
-    case kF16: return 4;
+    case kF16: case kF32: case kBF16: return 4;
     case kQ8_0: case kQ5_0: return 32;
     default: return 256;
     }
@@ -59,7 +59,8 @@ uint32_t k_multiple(int wt) {
 
 uint32_t w_align(int wt) {
     switch (wt) {
-    case kF16: return 8;
+    case kF16: case kBF16: return 8;
+    case kF32: return 4;
     case kQ4_K: return 16;  // 16-byte qs loads; 144-byte blocks keep it row to row
     default: return 2;
     }
@@ -553,6 +554,8 @@ const void* mv_kernel(int wt, int m, int nr0) {
     case kQ5_0: return lo ? mv_kernel_q5_0_a(m, nr0) : mv_kernel_q5_0_b(m, nr0);
     case kQ4_K: return lo ? mv_kernel_q4_k_a(m, nr0) : mv_kernel_q4_k_b(m, nr0);
     case kQ6_K: return lo ? mv_kernel_q6_k_a(m, nr0) : mv_kernel_q6_k_b(m, nr0);
+    case kF32: return lo ? mv_kernel_f32_a(m, nr0) : mv_kernel_f32_b(m, nr0);
+    case kBF16: return lo ? mv_kernel_bf16_a(m, nr0) : mv_kernel_bf16_b(m, nr0);
     default: return nullptr;
     }
 }

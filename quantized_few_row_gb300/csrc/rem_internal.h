@@ -7,7 +7,7 @@
 
 namespace rem {
 
-enum Wt : int { kF16 = 0, kQ8_0 = 1, kQ4_K = 2, kQ6_K = 3, kQ5_0 = 4, kNumWt = 5 };
+enum Wt : int { kF16 = 0, kQ8_0 = 1, kQ4_K = 2, kQ6_K = 3, kQ5_0 = 4, kF32 = 5, kBF16 = 6, kNumWt = 7 };
 
 constexpr int kMaxRows = 8;        // ROW_EXACT_MATVEC_MAX_ROWS
 constexpr int kLanes = 32;         // weight rows per warp and NR0: one row per lane
@@ -17,25 +17,27 @@ constexpr int kMaxStages = 4;      // pipeline stages (mbarriers) per warp
 
 // Values and bytes of one block (the *_BLOCK_VALUES / *_BLOCK_BYTES constants).
 __host__ __device__ constexpr int block_values(int wt) {
-    return wt == kF16 ? 1 : (wt == kQ8_0 || wt == kQ5_0) ? 32 : 256;
+    return (wt == kF16 || wt == kF32 || wt == kBF16) ? 1 : (wt == kQ8_0 || wt == kQ5_0) ? 32 : 256;
 }
 __host__ __device__ constexpr int block_bytes(int wt) {
-    return wt == kF16 ? 2 : wt == kQ8_0 ? 34 : wt == kQ5_0 ? 22 : wt == kQ4_K ? 144 : 210;
+    return (wt == kF16 || wt == kBF16) ? 2 : wt == kF32 ? 4 : wt == kQ8_0 ? 34 : wt == kQ5_0 ? 22
+           : wt == kQ4_K ? 144 : 210;
 }
 
 // Staging geometry.  A "chunk" is the slice of one weight row a lane decodes
-// between two pipeline waits: 72 F16 values, 4 Q8_0 blocks, 8 Q5_0 blocks, or
-// one Q4_K / Q6_K super-block.  A warp stages the same chunk of its 32*NR0
+// between two pipeline waits: 72 F16 or BF16 values, 36 F32 values, 4 Q8_0
+// blocks, 8 Q5_0 blocks, or one Q4_K / Q6_K super-block.  A warp stages the same chunk of its 32*NR0
 // rows as one 2-D TMA box, one row every `box` bytes.  Box widths are odd
 // multiples of 16 bytes, so 32 lanes reading 16 bytes each at the same
 // offset of their own rows hit distinct bank quads (4 wavefronts, the
 // minimum).  Q8_0 and Q6_K stage the 16-byte aligned window (144 / 240
 // bytes) around their 136 / 210 chunk bytes.
 __host__ __device__ constexpr int chunk_values(int wt) {
-    return wt == kF16 ? 72 : wt == kQ8_0 ? 128 : 256;
+    return (wt == kF16 || wt == kBF16) ? 72 : wt == kF32 ? 36 : wt == kQ8_0 ? 128 : 256;
 }
 __host__ __device__ constexpr int chunk_box(int wt) {
-    return (wt == kF16 || wt == kQ8_0 || wt == kQ4_K) ? 144 : wt == kQ5_0 ? 176 : 240;
+    return (wt == kF16 || wt == kBF16 || wt == kF32 || wt == kQ8_0 || wt == kQ4_K) ? 144 : wt == kQ5_0 ? 176
+           : 240;
 }
 
 // Kernel argument block (one launch).  Grid: a number of clusters of
@@ -74,6 +76,8 @@ REM_DECLARE_PARTS(mv_kernel_q8_0)
 REM_DECLARE_PARTS(mv_kernel_q5_0)
 REM_DECLARE_PARTS(mv_kernel_q4_k)
 REM_DECLARE_PARTS(mv_kernel_q6_k)
+REM_DECLARE_PARTS(mv_kernel_f32)
+REM_DECLARE_PARTS(mv_kernel_bf16)
 #undef REM_DECLARE_PARTS
 
 // Dynamic shared memory of one CTA; the kernel lays it out the same way:

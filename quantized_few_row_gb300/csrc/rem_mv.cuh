@@ -182,6 +182,16 @@ template <> struct Stage<kF16> {
     __device__ static uint32_t gofs(uint32_t cc) { return cc * 144u; }  // global byte offset of the box
     __device__ static int sofs(uint32_t) { return 0; }
 };
+template <> struct Stage<kBF16> {
+    static constexpr int kValues = 72, kBox = 144;
+    __device__ static uint32_t gofs(uint32_t cc) { return cc * 144u; }
+    __device__ static int sofs(uint32_t) { return 0; }
+};
+template <> struct Stage<kF32> {
+    static constexpr int kValues = 36, kBox = 144;
+    __device__ static uint32_t gofs(uint32_t cc) { return cc * 144u; }
+    __device__ static int sofs(uint32_t) { return 0; }
+};
 // Q8_0 chunks are 4 blocks (136 B): stage the 16-byte aligned 144-byte
 // window that contains them; they start 0 or 8 bytes into it.
 template <> struct Stage<kQ8_0> {
@@ -480,6 +490,57 @@ __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], con
         for (int j = 0; j < M; ++j) acc[i][j] = add2(acc[i][j], c[i][j]);
 }
 
+// BF16 pair from a 32-bit word: the two halves are the upper 16 bits of
+// binary32 values (exact).
+__device__ __forceinline__ float2 bf16x2(uint32_t v) { return make_float2(fbits(v << 16), fbits(v & 0xFFFF0000u)); }
+
+// BF16 chunk of 72 values, F32 chunk of 36 values: the same chain as F16
+// (pairs in order, then acc = acc + c per chunk).
+template <int M, int NR0, int WT>
+__device__ __forceinline__ void chunk_dense(const uint8_t* const (&rows)[NR0], const float* xc,
+                                            float2 (&acc)[NR0][M]) {
+    constexpr int CV = Stage<WT>::kValues;
+    constexpr int PER = WT == kF32 ? 4 : 8;  // values per 16-byte load
+    float2 c[NR0][M];
+#pragma unroll
+    for (int i = 0; i < NR0; ++i)
+#pragma unroll
+        for (int j = 0; j < M; ++j) c[i][j] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int g = 0; g < CV / PER; ++g) {
+        float2 p[NR0][PER / 2];
+#pragma unroll
+        for (int i = 0; i < NR0; ++i) {
+            const uint4 h = lds16(rows[i] + 16 * g);
+            if constexpr (WT == kF32) {
+                p[i][0] = make_float2(fbits(h.x), fbits(h.y));
+                p[i][1] = make_float2(fbits(h.z), fbits(h.w));
+            } else {
+                p[i][0] = bf16x2(h.x);
+                p[i][1] = bf16x2(h.y);
+                p[i][2] = bf16x2(h.z);
+                p[i][3] = bf16x2(h.w);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+#pragma unroll
+            for (int q = 0; q < PER / 4; ++q) {
+                const float4 xv = ldx4(xc + j * CV + PER * g + 4 * q);
+#pragma unroll
+                for (int i = 0; i < NR0; ++i) {
+                    c[i][j] = fma2(p[i][2 * q], make_float2(xv.x, xv.y), c[i][j]);
+                    c[i][j] = fma2(p[i][2 * q + 1], make_float2(xv.z, xv.w), c[i][j]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NR0; ++i)
+#pragma unroll
+        for (int j = 0; j < M; ++j) acc[i][j] = add2(acc[i][j], c[i][j]);
+}
+
 // NB 32-value blocks (Q8_0 or Q5_0) of one staged chunk, block b at byte
 // O + STRIDE*b of each staged row.  Blocks past k are zero-filled (scale 0,
 // inputs 0) and add exact zeros.
@@ -607,9 +668,12 @@ __device__ __forceinline__ void stage_w_plain(uint8_t* dst_rows, const uint8_t* 
                                               int nrows, uint32_t cc, uint32_t k, int lane) {
     constexpr int BOX = Stage<WT>::kBox;
     uint32_t first, len;  // byte range of the chunk inside the row
-    if constexpr (WT == kF16) {
+    if constexpr (WT == kF16 || WT == kBF16) {
         first = cc * 144u;
         len = 2u * min(72u, k - cc * 72u);
+    } else if constexpr (WT == kF32) {
+        first = cc * 144u;
+        len = 4u * min(36u, k - cc * 36u);
     } else if constexpr (WT == kQ8_0) {
         first = cc * 136u;
         len = min(4u, k / 32u - cc * 4u) * 34u;
@@ -693,6 +757,8 @@ __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int
     const float* xc = reinterpret_cast<const float*>(st + wstage);  // [M][CV]
     if constexpr (WT == kF16) {
         chunk_f16<M, NR0>(rows, xc, acc);
+    } else if constexpr (WT == kBF16 || WT == kF32) {
+        chunk_dense<M, NR0, WT>(rows, xc, acc);
     } else if constexpr (WT == kQ8_0) {
         if (Stage<WT>::sofs(cc) == 0) chunk_blocks32<M, NR0, BlkQ8, 4, 34, 0>(rows, xc, acc);
         else chunk_blocks32<M, NR0, BlkQ8, 4, 34, 8>(rows, xc, acc);

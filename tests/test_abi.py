@@ -38,6 +38,7 @@ def test_exports_every_declared_symbol(lib):
 @pytest.mark.parametrize("wt,k,expect", [
     ("f16", 512, 1024), ("q8_0", 4096, 4352), ("q4_K", 4096, 2304), ("q6_K", 4096, 3360),
     ("q5_0", 4096, 2816), ("q8_0", 32, 34), ("q5_0", 32, 22), ("q4_K", 256, 144), ("q6_K", 256, 210),
+    ("f32", 4096, 16384), ("bf16", 4096, 8192), ("f32", 4, 16), ("bf16", 4, 8),
 ])
 def test_row_bytes(lib, wt, k, expect):
     assert rem.rem_row_bytes(wt, k) == expect
@@ -94,6 +95,9 @@ CASES = [
     ("nully", dict(y=0), "non-null"),
     ("k_q8", dict(k=100, x_row_stride=100), "multiple of 32"),
     ("k_f16", dict(wtype="f16", k=6, x_row_stride=8), "multiple of 4"),
+    ("k_f32", dict(wtype="f32", k=6, x_row_stride=8), "multiple of 4"),
+    ("k_bf16", dict(wtype="bf16", k=10, x_row_stride=12), "multiple of 4"),
+    ("w_f32", dict(wtype="f32", W=W + 2), "4-byte"),
     ("k_q4k", dict(wtype="q4_K", k=288, x_row_stride=288), "multiple of 256"),
     ("k_q6k", dict(wtype="q6_K", k=128, x_row_stride=128), "multiple of 256"),
     ("k_q5", dict(wtype="q5_0", k=48, x_row_stride=48), "multiple of 32"),

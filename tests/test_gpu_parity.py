@@ -22,7 +22,7 @@ from tests import gpu_harness as H
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["f16", "q8_0", "q5_0", "q4_K", "q6_K"]
+FMTS = ["f16", "q8_0", "q5_0", "q4_K", "q6_K", "bf16", "f32"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,6 +44,14 @@ def _adversarial_blocks(fmt, rows, k, seed):
         h = b.view(np.uint16)
         h[(h & 0x7C00) == 0x7C00] &= 0x3FFF   # no inf / NaN
         return b
+    if fmt == "bf16":
+        h = b.view(np.uint16)
+        h[(h & 0x7F80) == 0x7F80] &= 0xBFFF   # no inf / NaN
+        return b
+    if fmt == "f32":
+        u = b.view(np.uint32)
+        u[(u & 0x7F800000) == 0x7F800000] &= 0xBFFFFFFF
+        return b
     g = np.random.Generator(np.random.PCG64(seed + 1))
     bb = oracle.block_bytes(fmt)
     nb = rb // bb
@@ -59,7 +67,7 @@ def _adversarial_blocks(fmt, rows, k, seed):
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_dequantize_bit_exact(fmt):
-    k = {"f16": 520, "q8_0": 1024, "q5_0": 1024, "q4_K": 1024, "q6_K": 1024}[fmt]
+    k = {"f16": 520, "q8_0": 1024, "q5_0": 1024, "q4_K": 1024, "q6_K": 1024, "bf16": 520, "f32": 520}[fmt]
     rows = 37
     for w in (oracle.quantize(inputs.weights(rows, k, 101), fmt), _adversarial_blocks(fmt, rows, k, 102)):
         ref = oracle.dequantize(w, fmt, rows, k)
@@ -97,6 +105,8 @@ SHAPES = {  # (n, k): several row groups, several chunks, ragged row tail
     "q5_0": [(103, 1024), (40, 160), (77, 2048)],
     "q4_K": [(103, 1024), (33, 256), (150, 4096)],
     "q6_K": [(103, 1024), (33, 256), (150, 4096)],
+    "bf16": [(103, 520), (64, 72), (7, 4096)],
+    "f32": [(103, 520), (64, 36), (7, 4096)],
 }
 
 
@@ -143,8 +153,10 @@ def test_rows_inert_to_packing_path_and_runs(fmt):
     split = 2
     base = H.run_matvec(w, fmt, n, k, 1, x, 8, k, 0, n, 0, 8 * n, split=split)
     variants = [dict(rows_per_cta=rpc) for rpc in (32, 64, 128)]
-    if fmt == "f16":
-        variants.append(dict(w_offset=8))           # F16 needs 8-byte alignment: plain staging path
+    if fmt in ("f16", "bf16"):
+        variants.append(dict(w_offset=8))           # 8-byte alignment required: plain staging path
+    elif fmt == "f32":
+        variants.append(dict(w_offset=4))           # 4-byte aligned base: plain staging path
     elif fmt != "q4_K":                             # Q4_K requires 16-byte alignment
         variants.append(dict(w_offset=2))           # 2-byte aligned base: plain staging path
     for v in variants:
@@ -241,7 +253,7 @@ def test_nan_in_input_row_stays_in_that_row(fmt):
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_single_row_single_chunk(fmt):
-    n, k, m = 1, {"f16": 4}.get(fmt, oracle.block_values(fmt)), 1
+    n, k, m = 1, {"f16": 4, "bf16": 4, "f32": 4}.get(fmt, oracle.block_values(fmt)), 1
     w, x = H.contiguous(fmt, n, k, m, 290, 390)
     y_ref, a_ref = oracle.matvec(w, fmt, n, k, 1, x, m, k, 0)
     y = H.run_matvec(w, fmt, n, k, 1, x, m, k, 0, n, 0, 1, use_ex=False)
