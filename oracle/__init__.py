@@ -71,6 +71,19 @@ def _load():
     lib.rem_oracle_h2f_array.restype = None
     lib.rem_oracle_f2h_array.argtypes = [f32p, u16p, ctypes.c_uint64, ctypes.c_int]
     lib.rem_oracle_f2h_array.restype = None
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    lib.rem_oracle_affine_dequantize.argtypes = [u32p, u16p, u16p, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+                                                 ctypes.c_uint32, f32p]
+    lib.rem_oracle_affine_dequantize.restype = ctypes.c_int
+    lib.rem_oracle_affine_quantize.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint32,
+                                               u32p, u16p, u16p]
+    lib.rem_oracle_affine_quantize.restype = ctypes.c_int
+    lib.rem_oracle_affine_matvec_rows.argtypes = [u32p, u16p, u16p, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+                                                  ctypes.c_uint32, f32p, ctypes.c_uint32, ctypes.c_uint64,
+                                                  ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64),
+                                                  ctypes.c_uint64, ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.POINTER(ctypes.c_double)]
+    lib.rem_oracle_affine_matvec_rows.restype = ctypes.c_int
     lib.rem_oracle_bf2f_array.argtypes = [u16p, f32p, ctypes.c_uint64]
     lib.rem_oracle_bf2f_array.restype = None
     lib.rem_oracle_f2bf_array.argtypes = [f32p, u16p, ctypes.c_uint64]
@@ -146,6 +159,64 @@ def f2bf(f: np.ndarray) -> np.ndarray:
     return out
 
 
+def affine_quantize(values: np.ndarray, bits: int, group_size: int):
+    """Affine test data: (codes uint32 [rows, k*bits/32], scales uint16 [rows, k/gs],
+    biases uint16 [rows, k/gs]) from float rows [rows, k]."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    rows, k = v.shape
+    codes = np.empty((rows, k * bits // 32), dtype=np.uint32)
+    sc = np.empty((rows, k // group_size), dtype=np.uint16)
+    bi = np.empty((rows, k // group_size), dtype=np.uint16)
+    rc = _load().rem_oracle_affine_quantize(_ptr(v, ctypes.c_float), bits, group_size, rows, k,
+                                            _ptr(codes, ctypes.c_uint32), _ptr(sc, ctypes.c_uint16),
+                                            _ptr(bi, ctypes.c_uint16))
+    if rc != 0:
+        raise ValueError(f"affine_quantize: bad bits {bits} / group size {group_size} / k {k}")
+    return codes, sc, bi
+
+
+def affine_dequantize(codes, scales, biases, bits: int, group_size: int, rows: int, k: int) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint32)
+    s = np.ascontiguousarray(scales, dtype=np.uint16)
+    b = np.ascontiguousarray(biases, dtype=np.uint16)
+    out = np.empty((rows, k), dtype=np.float32)
+    rc = _load().rem_oracle_affine_dequantize(_ptr(c, ctypes.c_uint32), _ptr(s, ctypes.c_uint16),
+                                              _ptr(b, ctypes.c_uint16), bits, group_size, rows, k,
+                                              _ptr(out, ctypes.c_float))
+    if rc != 0:
+        raise ValueError("affine_dequantize: bad arguments")
+    return out
+
+
+def affine_matvec_rows(codes, scales, biases, bits: int, group_size: int, n: int, k: int, x: np.ndarray, m: int,
+                       x_row_stride: int, x_batch_stride: int, rows):
+    """f64 y and sum|w*x| for selected global rows of an affine weight; [len(rows), m]."""
+    c = np.ascontiguousarray(codes, dtype=np.uint32).reshape(-1)
+    s = np.ascontiguousarray(scales, dtype=np.uint16).reshape(-1)
+    b = np.ascontiguousarray(biases, dtype=np.uint16).reshape(-1)
+    xf = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    r = np.ascontiguousarray(rows, dtype=np.uint64).reshape(-1)
+    y = np.empty((r.size, m), dtype=np.float64)
+    a = np.empty((r.size, m), dtype=np.float64)
+    rc = _load().rem_oracle_affine_matvec_rows(_ptr(c, ctypes.c_uint32), _ptr(s, ctypes.c_uint16),
+                                               _ptr(b, ctypes.c_uint16), bits, group_size, n, k,
+                                               _ptr(xf, ctypes.c_float), m, x_row_stride, x_batch_stride,
+                                               _ptr(r, ctypes.c_uint64), r.size, _ptr(y, ctypes.c_double),
+                                               _ptr(a, ctypes.c_double))
+    if rc != 0:
+        raise RuntimeError(f"oracle affine matvec failed ({rc})")
+    return y, a
+
+
+def affine_matvec(codes, scales, biases, bits: int, group_size: int, n: int, k: int, batch: int, x: np.ndarray,
+                  m: int, x_row_stride: int, x_batch_stride: int):
+    """f64 y[b, j, i] and A[b, j, i] for every output of an affine product."""
+    rows = np.arange(batch * n, dtype=np.uint64)
+    y, a = affine_matvec_rows(codes, scales, biases, bits, group_size, n, k, x, m, x_row_stride, x_batch_stride,
+                              rows)
+    return (y.reshape(batch, n, m).transpose(0, 2, 1).copy(), a.reshape(batch, n, m).transpose(0, 2, 1).copy())
+
+
 def quantize(values: np.ndarray, wtype) -> np.ndarray:
     """Quantize float rows [rows, k] into block bytes [rows, row_bytes]."""
     wt = wtype_of(wtype)
@@ -215,5 +286,6 @@ def within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, a_ref: np.ndarray,
 
 
 __all__ = ["build", "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16", "WTYPES", "block_values", "block_bytes",
-           "row_bytes", "threads", "h2f", "f2h", "bf2f", "f2bf", "quantize", "dequantize", "matvec", "matvec_rows",
+           "row_bytes", "threads", "h2f", "f2h", "bf2f", "f2bf", "affine_quantize", "affine_dequantize", "affine_matvec",
+           "affine_matvec_rows", "quantize", "dequantize", "matvec", "matvec_rows",
            "within_tolerance", "wtype_of"]

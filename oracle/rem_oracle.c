@@ -542,6 +542,119 @@ int rem_oracle_matvec_rows(const uint8_t* w, int wtype, uint32_t n, uint32_t k,
     return err;
 }
 
+/* ------------------------------------------------------------------ */
+/* Affine quantization (nuvec-core 0.6.0 src/gpu.rs: Quantize /         */
+/* Dequantize / QuantizedMatmul in QuantMode::Affine with (group_size,  */
+/* bits), and pack_factor: 32/bits codes per 32-bit word for 4 and 8    */
+/* bits).  The pages give no element formula or layout; the reading:    */
+/*   codes   rows x (k*bits/32) uint32 words; code i of a row sits at   */
+/*           bits [bits*(i % (32/bits)), +bits) of word i / (32/bits)   */
+/*           (lowest bits first);                                       */
+/*   scales, biases  rows x (k/group_size) binary16, one per group;     */
+/*   w = fl(fl(scale*q) + bias), the product rounded, then the add.     */
+/* ------------------------------------------------------------------ */
+
+static int affine_ok(int bits, int gs, uint32_t k) {
+    return (bits == 4 || bits == 8) && (gs == 32 || gs == 64 || gs == 128) && k > 0 && k % (uint32_t)gs == 0;
+}
+
+static void deq_affine_row(const uint32_t* codes, const uint16_t* sc, const uint16_t* bi, int bits, int gs,
+                           uint32_t k, float* out) {
+    const uint32_t per = 32u / (uint32_t)bits, mask = (1u << bits) - 1u;
+    for (uint32_t i = 0; i < k; ++i) {
+        uint32_t q = (codes[i / per] >> (bits * (i % per))) & mask;
+        float s = rem_oracle_h2f(sc[i / (uint32_t)gs]), b = rem_oracle_h2f(bi[i / (uint32_t)gs]);
+        float p = s * (float)q;
+        out[i] = p + b;
+    }
+}
+
+/* Dequantize `rows` rows of k elements into out[rows][k].  0 on success. */
+int rem_oracle_affine_dequantize(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                                 int gs, uint32_t rows, uint32_t k, float* out) {
+    if (!affine_ok(bits, gs, k)) return -1;
+    const uint64_t cw = (uint64_t)k * bits / 32, ng = k / (uint32_t)gs;
+    for (uint32_t r = 0; r < rows; ++r)
+        deq_affine_row(codes + r * cw, scales + r * ng, biases + r * ng, bits, gs, k, out + (uint64_t)r * k);
+    return 0;
+}
+
+/* Test-data quantizer: per group lo = min, hi = max, scale = fp16_rn((hi -
+ * lo) / (2^bits - 1)), bias = fp16_rn(lo), q = clamp(roundf((v - bias) /
+ * scale), 0, 2^bits - 1) against the stored scale and bias (q = 0 when the
+ * stored scale is 0).  0 on success. */
+int rem_oracle_affine_quantize(const float* src, int bits, int gs, uint32_t rows, uint32_t k, uint32_t* codes,
+                               uint16_t* scales, uint16_t* biases) {
+    if (!affine_ok(bits, gs, k)) return -1;
+    const uint32_t per = 32u / (uint32_t)bits, qmax = (1u << bits) - 1u;
+    const uint64_t cw = (uint64_t)k * bits / 32, ng = k / (uint32_t)gs;
+    for (uint32_t r = 0; r < rows; ++r) {
+        const float* v = src + (uint64_t)r * k;
+        uint32_t* cr = codes + r * cw;
+        for (uint64_t w = 0; w < cw; ++w) cr[w] = 0;
+        for (uint64_t g = 0; g < ng; ++g) {
+            const float* vg = v + g * gs;
+            float lo = vg[0], hi = vg[0];
+            for (int e = 1; e < gs; ++e) {
+                if (vg[e] < lo) lo = vg[e];
+                if (vg[e] > hi) hi = vg[e];
+            }
+            uint16_t sh = rem_oracle_f2h_rn((hi - lo) / (float)qmax), bh = rem_oracle_f2h_rn(lo);
+            scales[r * ng + g] = sh;
+            biases[r * ng + g] = bh;
+            float sf = rem_oracle_h2f(sh), bf = rem_oracle_h2f(bh);
+            for (int e = 0; e < gs; ++e) {
+                long q = 0;
+                if (sf != 0.0f) {
+                    q = (long)roundf((vg[e] - bf) / sf);
+                    if (q < 0) q = 0;
+                    if (q > (long)qmax) q = (long)qmax;
+                }
+                uint64_t i = g * gs + (uint64_t)e;
+                cr[i / per] |= (uint32_t)q << (bits * (i % per));
+            }
+        }
+    }
+    return 0;
+}
+
+/* f64 y and sum|w*x| for selected global rows of an affine weight (as
+ * rem_oracle_matvec_rows). */
+int rem_oracle_affine_matvec_rows(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                                  int gs, uint32_t n, uint32_t k, const float* x, uint32_t m, uint64_t xrs,
+                                  uint64_t xbs, const uint64_t* rows, uint64_t nrows, double* y, double* a) {
+    if (!affine_ok(bits, gs, k) || n == 0 || m == 0) return -1;
+    const uint64_t cw = (uint64_t)k * bits / 32, ng = k / (uint32_t)gs;
+    int err = 0;
+#pragma omp parallel
+    {
+        float* wf = (float*)malloc(sizeof(float) * (size_t)k);
+        if (!wf) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t c = 0; c < (int64_t)nrows; ++c) {
+            if (!wf) continue;
+            uint64_t r = rows[c], bidx = r / n;
+            deq_affine_row(codes + r * cw, scales + r * ng, biases + r * ng, bits, gs, k, wf);
+            for (uint32_t j = 0; j < m; ++j) {
+                const float* xr = x + bidx * xbs + (uint64_t)j * xrs;
+                double sum = 0.0, sa = 0.0;
+                for (uint32_t kk = 0; kk < k; ++kk) {
+                    double p = (double)wf[kk] * (double)xr[kk];
+                    sum += p;
+                    sa += fabs(p);
+                }
+                y[(uint64_t)c * m + j] = sum;
+                a[(uint64_t)c * m + j] = sa;
+            }
+        }
+        free(wf);
+    }
+    return err;
+}
+
 /* Threads the parallel region above uses. */
 int rem_oracle_threads(void) {
 #ifdef _OPENMP

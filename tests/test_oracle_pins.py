@@ -398,3 +398,71 @@ def test_dense_brute_force_rational(orc, fmt, k):
         for j in range(m):
             exact = sum(Fraction(float(wf[i, kk])) * Fraction(float(x[j, kk])) for kk in range(k))
             assert abs(Fraction(y[0, j, i]) - exact) <= Fraction(k * 2.0 ** -52) * Fraction(a[0, j, i])
+
+
+# ---------------------------------------------------------------- affine (group scale and bias)
+
+def _affine_case(bits, gs, k, codes_at, scale_bits, bias_bits):
+    """codes_at: {element index: code}; scale/bias binary16 bit patterns per group."""
+    per = 32 // bits
+    codes = np.zeros((1, k * bits // 32), dtype=np.uint32)
+    for i, q in codes_at.items():
+        codes[0, i // per] |= np.uint32(q << (bits * (i % per)))
+    sc = np.array([scale_bits], dtype=np.uint16).reshape(1, -1)
+    bi = np.array([bias_bits], dtype=np.uint16).reshape(1, -1)
+    return codes, sc, bi
+
+
+@pytest.mark.parametrize("bits,gs,k,codes_at,scales,biases,expect", [
+    # one code lights one element, at index i: word i // (32/bits), bits bits*(i % (32/bits)) (lowest first)
+    (4, 32, 32, {0: 5}, [0x3C00], [0x0000], {0: 5.0}),
+    (4, 32, 32, {1: 5}, [0x3C00], [0x0000], {1: 5.0}),
+    (4, 32, 32, {7: 15}, [0x3C00], [0x0000], {7: 15.0}),
+    (4, 32, 32, {8: 9}, [0x3C00], [0x0000], {8: 9.0}),
+    (4, 32, 32, {31: 1}, [0x3800], [0x0000], {31: 0.5}),
+    (8, 32, 32, {2: 200}, [0x3C00], [0x0000], {2: 200.0}),
+    (8, 32, 32, {5: 255}, [0x3400], [0x0000], {5: 63.75}),
+    # the bias adds to every element of its group, the scale multiplies the code
+    (4, 32, 32, {}, [0x3C00], [0xC000], {}),                  # all -2
+    (4, 32, 32, {3: 15}, [0x3800], [0xC000], {3: 5.5}),       # 0.5*15 - 2
+    # group g covers elements g*gs .. g*gs+gs-1
+    (4, 32, 64, {40: 3}, [0x3C00, 0x4000], [0x0000, 0x3C00], {40: 7.0}),   # group 1: 2*3 + 1
+    (8, 64, 128, {63: 1, 64: 1}, [0x3C00, 0x4400], [0x0000, 0x0000], {63: 1.0, 64: 4.0}),
+])
+def test_affine_decode_hand_derived(orc, bits, gs, k, codes_at, scales, biases, expect):
+    codes, sc, bi = _affine_case(bits, gs, k, codes_at, scales, biases)
+    got = orc.affine_dequantize(codes, sc, bi, bits, gs, 1, k)[0]
+    for i in range(k):
+        g = i // gs
+        base = float(orc.h2f(np.array([biases[g]], np.uint16))[0])
+        assert got[i] == np.float32(expect.get(i, base)), (i, got[i])
+
+
+@pytest.mark.parametrize("bits,gs", [(4, 32), (4, 64), (4, 128), (8, 32), (8, 64), (8, 128)])
+def test_affine_round_trip_bound(orc, bits, gs):
+    k, rows = 512, 6
+    v = inputs.weights(rows, k, 60)
+    v[1] *= 100.0
+    v[2] = np.float32(0.25)                       # constant rows: scale 0
+    c, s, b = orc.affine_quantize(v, bits, gs)
+    d = orc.affine_dequantize(c, s, b, bits, gs, rows, k)
+    qmax = 2 ** bits - 1
+    g = v.reshape(rows, k // gs, gs)
+    lo, hi = g.min(axis=2).astype(np.float64), g.max(axis=2).astype(np.float64)
+    sf, bf = orc.h2f(s).astype(np.float64), orc.h2f(b).astype(np.float64)
+    bound = 0.5 * sf + np.abs(lo - bf) + qmax * np.abs((hi - lo) / qmax - sf) + 1e-6 * (np.abs(lo) + np.abs(hi))
+    err = np.abs(d.astype(np.float64) - v.astype(np.float64)).reshape(rows, k // gs, gs).max(axis=2)
+    assert np.all(err <= bound)
+
+
+@pytest.mark.parametrize("bits,gs", [(4, 64), (8, 32)])
+def test_affine_brute_force_rational(orc, bits, gs):
+    n, k, m = 3, 128, 4
+    c, s, b = orc.affine_quantize(inputs.weights(n, k, 61), bits, gs)
+    wf = orc.affine_dequantize(c, s, b, bits, gs, n, k)
+    x = inputs.activations(m, k, 62)
+    y, a = orc.affine_matvec(c, s, b, bits, gs, n, k, 1, x, m, k, 0)
+    for i in range(n):
+        for j in range(m):
+            exact = sum(Fraction(float(wf[i, kk])) * Fraction(float(x[j, kk])) for kk in range(k))
+            assert abs(Fraction(y[0, j, i]) - exact) <= Fraction(k * 2.0 ** -52) * Fraction(a[0, j, i])
