@@ -47,6 +47,8 @@ WORKLOADS = {
     # dense weights under the same row contract
     "bf16_n8192_k4096_m1-8": ("bf16", 8192, 4096, 1, list(range(1, 9)), False, 11),
     "f32_n4096_k4096_m1-8": ("f32", 4096, 4096, 1, list(range(1, 9)), False, 12),
+    # affine group quantization (4-bit codes, f16 scale and bias per 64 values)
+    "a4_g64_n14336_k4096_m1-8": ("a4_g64", 14336, 4096, 1, list(range(1, 9)), False, 13),
     # fused epilogue y = W.x + bias (rem_matvec_axpby, one bias vector for all rows)
     "q8_0_n4096_k4096_m1-8_bias": ("q8_0", 4096, 4096, 1, list(range(1, 9)), False, 10),
 }
@@ -99,9 +101,17 @@ def profiled_traffic(workload: str):
     return float(rec["dram_bytes_per_launch"])
 
 
+def affine_group_size(fmt):
+    """Group size of an affine weight type name ("a4_g64" -> 64), else 0."""
+    return int(fmt.split("_g")[1]) if fmt.startswith("a") else 0
+
+
 def call_bytes(fmt, n, k, batch, m, row_bytes):
-    """Algorithmic bytes of one call: every weight once, x and y once."""
-    return batch * n * row_bytes + 4 * batch * m * k + 4 * batch * m * n
+    """Algorithmic bytes of one call: every weight once (affine: codes plus the
+    binary16 scale and bias of every group), x and y once."""
+    gs = affine_group_size(fmt)
+    wrow = row_bytes + (4 * (k // gs) if gs else 0)
+    return batch * n * wrow + 4 * batch * m * k + 4 * batch * m * n
 
 
 class Clocks:
@@ -173,10 +183,24 @@ def run_ours(args, rank, world, local_rank):
 
     # weights: N(0, 0.02) drawn on the device, quantized by the library
     wf = inputs.torch_normal((batch * n, k), 1000 + ci, inputs.W_STD, dev)
-    w0 = torch.empty(wbytes, dtype=torch.uint8, device=dev)
-    rem.check(rem.rem_quantize(wf, fmt, batch * n, k, w0))
-    del wf
+    gs = affine_group_size(fmt)
+    if gs:
+        # affine: random codes, f16 scales ~ 0.02*3/15 and biases ~ -0.02*3 per group (device-side, seeded)
+        del wf
+        g = torch.Generator(device=dev)
+        g.manual_seed(1000 + ci)
+        w0 = torch.randint(0, 256, (wbytes,), dtype=torch.uint8, device=dev, generator=g)
+        ng = batch * n * (k // gs)
+        scales = (torch.rand(ng, device=dev, generator=g) * 0.004 + 0.002).half()
+        biases = (torch.rand(ng, device=dev, generator=g) * -0.06).half()
+        ring = max(1, math.ceil(4 * l2 / (wbytes + 4 * ng)))
+    else:
+        w0 = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+        rem.check(rem.rem_quantize(wf, fmt, batch * n, k, w0))
+        del wf
     wring = [w0] + [w0.clone() for _ in range(ring - 1)]
+    sring = [scales] + [scales.clone() for _ in range(ring - 1)] if gs else None
+    bring = [biases] + [biases.clone() for _ in range(ring - 1)] if gs else None
     if grouped:   # token-major: x [m, batch*k], y [m, batch*n]
         x = inputs.torch_normal((mmax, batch * k), 2000 + ci, inputs.X_STD, dev)
         y = torch.empty((mmax, batch * n), dtype=torch.float32, device=dev)
@@ -191,6 +215,9 @@ def run_ours(args, rank, world, local_rank):
     bias = inputs.torch_normal((batch, n), 3000 + ci, inputs.X_STD, dev) if epi else None
 
     def call(slot, m, stream=None):
+        if gs:
+            return rem.rem_matvec_affine(wring[slot], sring[slot], bring[slot], fmt, n, k, batch, x, m, k, xbs, y,
+                                         n, ybs, 0, stream)
         if epi:
             return rem.rem_matvec_axpby(wring[slot], fmt, n, k, batch, x, m, k, xbs, y, n, ybs, epi[0], epi[1],
                                         bias, 0, n, stream)
@@ -355,16 +382,23 @@ def oracle_sample(fmt, n, k, batch, ms, grouped, ci, seconds: float):
     rows_total = batch * n
     mmax = max(ms)
     x = inputs.activations(mmax, k, 2000 + ci)
-    nbytes_per = lambda rows: sum(rows * oracle.row_bytes(fmt, k) + 4 * m * k + 4 * m * rows for m in ms)
+    gs = affine_group_size(fmt)
+    bits = int(fmt[1]) if gs else 0
+    rbytes = k * bits // 8 if gs else oracle.row_bytes(fmt, k)
+    nbytes_per = lambda rows: sum(call_bytes(fmt, rows, k, 1, m, rbytes) for m in ms)
 
     def prepare(rows):
-        w = oracle.quantize(inputs.weights(rows, k, 1000 + ci), fmt)
+        v = inputs.weights(rows, k, 1000 + ci)
+        w = oracle.affine_quantize(v, bits, gs) if gs else oracle.quantize(v, fmt)
         return w, np.arange(rows, dtype=np.uint64)
 
     def sweep(w, idx, rows):
         t0 = time.perf_counter()
         for m in ms:
-            oracle.matvec_rows(w, fmt, rows, k, x, m, k, 0, idx)
+            if gs:
+                oracle.affine_matvec_rows(*w, bits, gs, rows, k, x, m, k, 0, idx)
+            else:
+                oracle.matvec_rows(w, fmt, rows, k, x, m, k, 0, idx)
         return time.perf_counter() - t0
 
     # grow the row sample until one sweep takes a measurable time, then

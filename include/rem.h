@@ -53,7 +53,14 @@ typedef enum {
     /* dense weights under the same row contract (the row-independent gemv of
        nuvec-core 0.6.0 src/gpu.rs, gemv_rows over F32 / F16 / BF16 matrices) */
     REM_F32 = 5,   /* row-major [batch*n, k] IEEE binary32, little-endian     */
-    REM_BF16 = 6   /* row-major [batch*n, k] bfloat16 (upper half of binary32) */
+    REM_BF16 = 6,  /* row-major [batch*n, k] bfloat16 (upper half of binary32) */
+    /* affine group quantization (the Affine mode of nuvec-core 0.6.0
+       src/gpu.rs, with (group_size, bits) and pack_factor): codes
+       [batch*n, k*bits/32] uint32 words, lowest bits first; scales and biases
+       [batch*n, k/group] binary16 in their own arrays; w = scale*q + bias.
+       Only through rem_matvec_affine / rem_dequantize_affine.           */
+    REM_A4_G32 = 7, REM_A4_G64 = 8, REM_A4_G128 = 9,   /* 4-bit codes  */
+    REM_A8_G32 = 10, REM_A8_G64 = 11, REM_A8_G128 = 12 /* 8-bit codes  */
 } rem_wtype;
 
 /* Status codes. */
@@ -144,6 +151,33 @@ int rem_matvec_axpby(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t 
                      float* y, uint32_t y_row_stride, uint32_t y_batch_stride,
                      float alpha, float beta, const float* c, uint32_t c_row_stride,
                      uint32_t c_batch_stride, void* stream);
+
+/*
+ * rem_matvec_affine -- y[b, j, :] = W[b] . x[b, j, :] for affine group-quantized
+ * W (next step 2 of the few-row path: the Affine quantized matmul of nuvec-core
+ * 0.6.0 src/gpu.rs).  The page fixes the (group_size, bits) parameters and the
+ * packing factor (32/bits codes per 32-bit word for 4 and 8 bits); the
+ * element formula and layout are the plain reading of that mode:
+ *   codes    batch*n rows of k*bits/32 uint32 words; code i of a row at bits
+ *            [bits*(i % (32/bits)), +bits) of word i / (32/bits); 4-byte
+ *            aligned (16-byte aligned rows use TMA staging)
+ *   scales, biases   batch*n rows of k/group binary16 values, 2-byte aligned
+ *   w[r, i] = fl(fl(scale[r, i/group] * q) + bias[r, i/group])
+ * wtype is one of REM_A4_G32 .. REM_A8_G128; k must be a multiple of the group
+ * size.  Other arguments as rem_matvec_ex (split 0 = automatic).  Row
+ * exactness holds as for the other formats.
+ */
+int rem_matvec_affine(const void* codes, const uint16_t* scales, const uint16_t* biases, int wtype,
+                      uint32_t n, uint32_t k, uint32_t batch, const float* x, uint32_t m,
+                      uint32_t x_row_stride, uint32_t x_batch_stride, float* y,
+                      uint32_t y_row_stride, uint32_t y_batch_stride, uint32_t split, void* stream);
+
+/*
+ * rem_dequantize_affine -- exact F32 weights out[r, :] of `rows` affine rows
+ * (test hook, as rem_dequantize): w = fl(fl(scale*q) + bias).
+ */
+int rem_dequantize_affine(const void* codes, const uint16_t* scales, const uint16_t* biases, int wtype,
+                          uint32_t rows, uint32_t k, float* out, void* stream);
 
 /*
  * rem_matvec_many -- the same product for any number of input rows m >= 1,

@@ -17,7 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16", "WTYPES", "REM_OK", "REM_EINVAL", "REM_ELAUNCH", "REM_ECUDA",
+    "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16", "A4_G32", "A4_G64", "A4_G128", "A8_G32", "A8_G64",
+    "A8_G128", "WTYPES", "affine_wtype", "rem_matvec_affine", "rem_dequantize_affine", "REM_OK", "REM_EINVAL", "REM_ELAUNCH", "REM_ECUDA",
     "RemError", "build", "library_path", "load", "rem_matvec", "rem_matvec_ex", "rem_matvec_many",
     "rem_matvec_axpby", "rem_row_bytes",
     "rem_split_factor", "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version", "check",
@@ -25,10 +26,18 @@ __all__ = [
 ]
 
 F16, Q8_0, Q4_K, Q6_K, Q5_0, F32, BF16 = 0, 1, 2, 3, 4, 5, 6
-WTYPES = {"f16": F16, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q5_0": Q5_0, "f32": F32, "bf16": BF16}
+A4_G32, A4_G64, A4_G128, A8_G32, A8_G64, A8_G128 = 7, 8, 9, 10, 11, 12
+WTYPES = {"f16": F16, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q5_0": Q5_0, "f32": F32, "bf16": BF16,
+          "a4_g32": A4_G32, "a4_g64": A4_G64, "a4_g128": A4_G128, "a8_g32": A8_G32, "a8_g64": A8_G64,
+          "a8_g128": A8_G128}
+
+
+def affine_wtype(bits: int, group_size: int) -> int:
+    """The weight type of affine codes of `bits` bits in groups of `group_size`."""
+    return WTYPES[f"a{bits}_g{group_size}"]
 REM_OK, REM_EINVAL, REM_ELAUNCH, REM_ECUDA = 0, -1, -2, -3
-C_FUNCTIONS = ("rem_matvec", "rem_matvec_ex", "rem_matvec_many", "rem_matvec_axpby", "rem_row_bytes",
-               "rem_split_factor",
+C_FUNCTIONS = ("rem_matvec", "rem_matvec_ex", "rem_matvec_many", "rem_matvec_axpby", "rem_matvec_affine",
+               "rem_dequantize_affine", "rem_row_bytes", "rem_split_factor",
                "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -72,6 +81,10 @@ def load():
     lib.rem_matvec_axpby.argtypes = [vp, i32, u32, u32, u32, vp, u32, u32, u32, vp, u32, u32, f32, f32, vp, u32,
                                      u32, vp]
     lib.rem_matvec_axpby.restype = i32
+    lib.rem_matvec_affine.argtypes = [vp, vp, vp, i32, u32, u32, u32, vp, u32, u32, u32, vp, u32, u32, u32, vp]
+    lib.rem_matvec_affine.restype = i32
+    lib.rem_dequantize_affine.argtypes = [vp, vp, vp, i32, u32, u32, vp, vp]
+    lib.rem_dequantize_affine.restype = i32
     lib.rem_row_bytes.argtypes = [i32, u32]
     lib.rem_row_bytes.restype = u64
     lib.rem_split_factor.argtypes = [i32, u32, u32]
@@ -142,6 +155,19 @@ def rem_matvec_axpby(W, wtype, n: int, k: int, batch: int, x, m: int, x_row_stri
     return load().rem_matvec_axpby(_ptr(W), _wt(wtype), n, k, batch, _ptr(x), m, x_row_stride, x_batch_stride,
                                    _ptr(y), y_row_stride, y_batch_stride, alpha, beta, _ptr(c), c_row_stride,
                                    c_batch_stride, _stream(stream))
+
+
+def rem_matvec_affine(codes, scales, biases, wtype, n: int, k: int, batch: int, x, m: int, x_row_stride: int,
+                      x_batch_stride: int, y, y_row_stride: int, y_batch_stride: int, split: int = 0,
+                      stream=None) -> int:
+    return load().rem_matvec_affine(_ptr(codes), _ptr(scales), _ptr(biases), _wt(wtype), n, k, batch, _ptr(x), m,
+                                    x_row_stride, x_batch_stride, _ptr(y), y_row_stride, y_batch_stride, split,
+                                    _stream(stream))
+
+
+def rem_dequantize_affine(codes, scales, biases, wtype, rows: int, k: int, out, stream=None) -> int:
+    return load().rem_dequantize_affine(_ptr(codes), _ptr(scales), _ptr(biases), _wt(wtype), rows, k, _ptr(out),
+                                        _stream(stream))
 
 
 def rem_row_bytes(wtype, k: int) -> int:

@@ -283,7 +283,36 @@ __global__ void quant_kernel(const float* __restrict__ src, int wt, uint64_t row
     }
 }
 
+// Affine: one thread per group; w = fl(fl(scale * q) + bias), codes lowest-first in 32-bit words.
+__global__ void dequant_affine_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                                      const uint16_t* __restrict__ biases, int bits, int gs, uint64_t rows,
+                                      uint32_t k, float* __restrict__ out) {
+    const uint64_t ng = k / static_cast<uint32_t>(gs);
+    const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (tid >= rows * ng) return;
+    const uint64_t r = tid / ng, g = tid - r * ng;
+    const uint32_t per = 32u / static_cast<uint32_t>(bits), mask = (1u << bits) - 1u;
+    const uint32_t* cr = codes + r * (static_cast<uint64_t>(k) * bits / 32u);
+    const float sc = h2f(scales[tid]), bi = h2f(biases[tid]);
+    for (int e = 0; e < gs; ++e) {
+        const uint64_t i = g * gs + e;
+        const uint32_t q = (cr[i / per] >> (bits * (i % per))) & mask;
+        out[r * k + i] = __fadd_rn(__fmul_rn(sc, static_cast<float>(q)), bi);
+    }
+}
+
 }  // namespace aux
+
+int launch_dequantize_affine(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int wt,
+                             uint64_t rows, uint32_t k, float* out, void* stream) {
+    const uint64_t threads = rows * (k / static_cast<uint32_t>(affine_group(wt)));
+    if (threads == 0) return 0;
+    const uint32_t block = 128;
+    const uint64_t grid = (threads + block - 1) / block;
+    aux::dequant_affine_kernel<<<static_cast<unsigned>(grid), block, 0, static_cast<cudaStream_t>(stream)>>>(
+        codes, scales, biases, affine_bits(wt), affine_group(wt), rows, k, out);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
 
 int launch_dequantize(const uint8_t* w, int wt, uint64_t rows, uint32_t k, uint64_t row_bytes, float* out,
                       void* stream) {

@@ -40,7 +40,8 @@ int fail(int code, const char* fmt, ...) {
 bool valid_wt(int wt) { return wt >= 0 && wt < kNumWt; }
 
 const char* wt_name(int wt) {
-    static const char* names[] = {"F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16"};
+    static const char* names[] = {"F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16", "A4G32", "A4G64",
+                                  "A4G128", "A8G32", "A8G64", "A8G128"};
     return valid_wt(wt) ? names[wt] : "?";
 }
 
@@ -50,6 +51,7 @@ uint64_t row_bytes_of(int wt, uint32_t k) {
 }
 
 uint32_t k_multiple(int wt) {
+    if (is_affine(wt)) return static_cast<uint32_t>(affine_group(wt));
     switch (wt) {
     case kF16: case kF32: case kBF16: return 4;
     case kQ8_0: case kQ5_0: return 32;
@@ -58,6 +60,7 @@ uint32_t k_multiple(int wt) {
 }
 
 uint32_t w_align(int wt) {
+    if (is_affine(wt)) return 4;  // 32-bit code words
     switch (wt) {
     case kF16: case kBF16: return 8;
     case kF32: return 4;
@@ -307,10 +310,21 @@ struct Epilogue {
     uint32_t crs = 0, cbs = 0;
 };
 
+// Scale and bias arrays of an affine weight (binary16, one per group and row).
+struct AffineArgs {
+    const uint16_t* scales = nullptr;
+    const uint16_t* biases = nullptr;
+};
+
 int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& s, uint32_t split,
-                  uint32_t rows_per_cta, void* stream, const Epilogue& epi = Epilogue()) {
+                  uint32_t rows_per_cta, void* stream, const Epilogue& epi = Epilogue(),
+                  const AffineArgs* aff = nullptr) {
     int rc = validate_args(W, wt, x, y, s, split, rows_per_cta);
     if (rc != REM_OK) return rc;
+    if (is_affine(wt) && !aff)
+        return fail(REM_EINVAL, "rem_matvec: %s weights need their scales and biases: use rem_matvec_affine",
+                    wt_name(wt));
+    if (!is_affine(wt) && aff) return fail(REM_EINVAL, "rem_matvec_affine: %s is not an affine type", wt_name(wt));
     const uint64_t rb = row_bytes_of(wt, s.k);
     const uint64_t rows = static_cast<uint64_t>(s.batch) * s.n;
     DeviceState* ds = nullptr;
@@ -322,6 +336,14 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
         return rc;
     if ((rc = check_buffer(y, 4 * strided_extent(s.batch, s.ybs, s.m, s.yrs, s.n), "output", dev)) != REM_OK)
         return rc;
+    if (aff) {
+        const uint64_t sb = 2 * rows * (s.k / static_cast<uint32_t>(affine_group(wt)));
+        if (!aff->scales || !aff->biases || reinterpret_cast<uintptr_t>(aff->scales) % 2 != 0 ||
+            reinterpret_cast<uintptr_t>(aff->biases) % 2 != 0)
+            return fail(REM_EINVAL, "rem_matvec_affine: scales and biases must be non-null and 2-byte aligned");
+        if ((rc = check_buffer(aff->scales, sb, "scales", dev)) != REM_OK) return rc;
+        if ((rc = check_buffer(aff->biases, sb, "biases", dev)) != REM_OK) return rc;
+    }
 
     // split = CTAs per cluster that share one row group's K ranges
     uint32_t S = split ? split : auto_split(wt, rows, s.k);
@@ -522,6 +544,11 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     a.c = epi.c;
     a.crs = epi.crs;
     a.cbs = epi.cbs;
+    if (aff) {
+        a.scales = aff->scales;
+        a.biases = aff->biases;
+        a.ngroups = s.k / static_cast<uint32_t>(affine_group(wt));
+    }
 
     void* args[3] = {&wmap, &xmap, &a};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
@@ -556,6 +583,12 @@ const void* mv_kernel(int wt, int m, int nr0) {
     case kQ6_K: return lo ? mv_kernel_q6_k_a(m, nr0) : mv_kernel_q6_k_b(m, nr0);
     case kF32: return lo ? mv_kernel_f32_a(m, nr0) : mv_kernel_f32_b(m, nr0);
     case kBF16: return lo ? mv_kernel_bf16_a(m, nr0) : mv_kernel_bf16_b(m, nr0);
+    case kA4G32: return lo ? mv_kernel_a4g32_a(m, nr0) : mv_kernel_a4g32_b(m, nr0);
+    case kA4G64: return lo ? mv_kernel_a4g64_a(m, nr0) : mv_kernel_a4g64_b(m, nr0);
+    case kA4G128: return lo ? mv_kernel_a4g128_a(m, nr0) : mv_kernel_a4g128_b(m, nr0);
+    case kA8G32: return lo ? mv_kernel_a8g32_a(m, nr0) : mv_kernel_a8g32_b(m, nr0);
+    case kA8G64: return lo ? mv_kernel_a8g64_a(m, nr0) : mv_kernel_a8g64_b(m, nr0);
+    case kA8G128: return lo ? mv_kernel_a8g128_a(m, nr0) : mv_kernel_a8g128_b(m, nr0);
     default: return nullptr;
     }
 }
@@ -627,6 +660,47 @@ int rem_matvec_axpby(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t 
     return launch_matvec(W, wtype, x, y, s, 0, 0, stream, e);
 }
 
+int rem_matvec_affine(const void* codes, const uint16_t* scales, const uint16_t* biases, int wtype, uint32_t n,
+                      uint32_t k, uint32_t batch, const float* x, uint32_t m, uint32_t x_row_stride,
+                      uint32_t x_batch_stride, float* y, uint32_t y_row_stride, uint32_t y_batch_stride,
+                      uint32_t split, void* stream) {
+    g_err[0] = '\0';
+    if (!is_affine(wtype)) return fail(REM_EINVAL, "rem_matvec_affine: %d is not an affine weight type", wtype);
+    if (!scales || !biases)
+        return fail(REM_EINVAL, "rem_matvec_affine: scales and biases must be non-null and 2-byte aligned");
+    const Shape s{m, n, k, batch, x_row_stride, x_batch_stride, y_row_stride, y_batch_stride};
+    AffineArgs aff;
+    aff.scales = scales;
+    aff.biases = biases;
+    return launch_matvec(codes, wtype, x, y, s, split, 0, stream, Epilogue(), &aff);
+}
+
+int rem_dequantize_affine(const void* codes, const uint16_t* scales, const uint16_t* biases, int wtype,
+                          uint32_t rows, uint32_t k, float* out, void* stream) {
+    g_err[0] = '\0';
+    if (!is_affine(wtype)) return fail(REM_EINVAL, "rem_dequantize_affine: %d is not an affine weight type", wtype);
+    int rc = check_rows_buffer(codes, wtype, rows, k, "rem_dequantize_affine");
+    if (rc != REM_OK) return rc;
+    if (!scales || !biases || reinterpret_cast<uintptr_t>(scales) % 2 || reinterpret_cast<uintptr_t>(biases) % 2)
+        return fail(REM_EINVAL, "rem_dequantize_affine: scales and biases must be non-null and 2-byte aligned");
+    if (!out || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+        return fail(REM_EINVAL, "rem_dequantize_affine: output must be non-null and 4-byte aligned");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(REM_ECUDA, "rem_dequantize_affine: no current CUDA device");
+    }
+    const uint64_t sb = 2ull * rows * (k / static_cast<uint32_t>(affine_group(wtype)));
+    if ((rc = check_buffer(codes, row_bytes_of(wtype, k) * rows, "codes", dev)) != REM_OK) return rc;
+    if ((rc = check_buffer(scales, sb, "scales", dev)) != REM_OK) return rc;
+    if ((rc = check_buffer(biases, sb, "biases", dev)) != REM_OK) return rc;
+    if ((rc = check_buffer(out, 4ull * rows * k, "output", dev)) != REM_OK) return rc;
+    if (launch_dequantize_affine(static_cast<const uint32_t*>(codes), scales, biases, wtype, rows, k, out, stream) !=
+        0)
+        return fail(REM_ECUDA, "rem_dequantize_affine: launch failed");
+    return REM_OK;
+}
+
 int rem_matvec_many(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch, const float* x, uint32_t m,
                     uint32_t x_row_stride, uint32_t x_batch_stride, float* y, uint32_t y_row_stride,
                     uint32_t y_batch_stride, uint32_t split, void* stream) {
@@ -666,6 +740,7 @@ uint32_t rem_split_factor(int wtype, uint32_t rows, uint32_t k) {
 
 int rem_dequantize(const void* W, int wtype, uint32_t rows, uint32_t k, float* out, void* stream) {
     g_err[0] = '\0';
+    if (is_affine(wtype)) return fail(REM_EINVAL, "rem_dequantize: use rem_dequantize_affine for affine weights");
     int rc = check_rows_buffer(W, wtype, rows, k, "rem_dequantize");
     if (rc != REM_OK) return rc;
     if (!out || reinterpret_cast<uintptr_t>(out) % 4 != 0)
@@ -685,6 +760,7 @@ int rem_dequantize(const void* W, int wtype, uint32_t rows, uint32_t k, float* o
 
 int rem_quantize(const float* src, int wtype, uint32_t rows, uint32_t k, void* W, void* stream) {
     g_err[0] = '\0';
+    if (is_affine(wtype)) return fail(REM_EINVAL, "rem_quantize: affine weights are not produced here");
     int rc = check_rows_buffer(W, wtype, rows, k, "rem_quantize");
     if (rc != REM_OK) return rc;
     if (!src || reinterpret_cast<uintptr_t>(src) % 4 != 0)

@@ -7,7 +7,17 @@
 
 namespace rem {
 
-enum Wt : int { kF16 = 0, kQ8_0 = 1, kQ4_K = 2, kQ6_K = 3, kQ5_0 = 4, kF32 = 5, kBF16 = 6, kNumWt = 7 };
+enum Wt : int {
+    kF16 = 0, kQ8_0 = 1, kQ4_K = 2, kQ6_K = 3, kQ5_0 = 4, kF32 = 5, kBF16 = 6,
+    // affine group quantization: 4- or 8-bit codes, binary16 scale and bias per group of 32/64/128
+    kA4G32 = 7, kA4G64 = 8, kA4G128 = 9, kA8G32 = 10, kA8G64 = 11, kA8G128 = 12,
+    kNumWt = 13
+};
+__host__ __device__ constexpr bool is_affine(int wt) { return wt >= kA4G32 && wt <= kA8G128; }
+__host__ __device__ constexpr int affine_bits(int wt) { return wt <= kA4G128 ? 4 : 8; }
+__host__ __device__ constexpr int affine_group(int wt) {
+    return (wt == kA4G32 || wt == kA8G32) ? 32 : (wt == kA4G64 || wt == kA8G64) ? 64 : 128;
+}
 
 constexpr int kMaxRows = 8;        // ROW_EXACT_MATVEC_MAX_ROWS
 constexpr int kLanes = 32;         // weight rows per warp and NR0: one row per lane
@@ -16,28 +26,33 @@ constexpr int kMaxSplit = 8;       // K ranges per row = CTAs per cluster (porta
 constexpr int kMaxStages = 4;      // pipeline stages (mbarriers) per warp
 
 // Values and bytes of one block (the *_BLOCK_VALUES / *_BLOCK_BYTES constants).
+// (An affine "block" is one group's codes; its scale and bias live in their own arrays.)
 __host__ __device__ constexpr int block_values(int wt) {
-    return (wt == kF16 || wt == kF32 || wt == kBF16) ? 1 : (wt == kQ8_0 || wt == kQ5_0) ? 32 : 256;
+    return is_affine(wt) ? affine_group(wt)
+           : (wt == kF16 || wt == kF32 || wt == kBF16) ? 1 : (wt == kQ8_0 || wt == kQ5_0) ? 32 : 256;
 }
 __host__ __device__ constexpr int block_bytes(int wt) {
-    return (wt == kF16 || wt == kBF16) ? 2 : wt == kF32 ? 4 : wt == kQ8_0 ? 34 : wt == kQ5_0 ? 22
+    return is_affine(wt) ? affine_group(wt) * affine_bits(wt) / 8
+           : (wt == kF16 || wt == kBF16) ? 2 : wt == kF32 ? 4 : wt == kQ8_0 ? 34 : wt == kQ5_0 ? 22
            : wt == kQ4_K ? 144 : 210;
 }
 
 // Staging geometry.  A "chunk" is the slice of one weight row a lane decodes
 // between two pipeline waits: 72 F16 or BF16 values, 36 F32 values, 4 Q8_0
-// blocks, 8 Q5_0 blocks, or one Q4_K / Q6_K super-block.  A warp stages the same chunk of its 32*NR0
+// blocks, 8 Q5_0 blocks, one Q4_K / Q6_K super-block, or 128 bytes of affine
+// codes (256 4-bit / 128 8-bit values, staged as a 144-byte window).  A warp stages the same chunk of its 32*NR0
 // rows as one 2-D TMA box, one row every `box` bytes.  Box widths are odd
 // multiples of 16 bytes, so 32 lanes reading 16 bytes each at the same
 // offset of their own rows hit distinct bank quads (4 wavefronts, the
 // minimum).  Q8_0 and Q6_K stage the 16-byte aligned window (144 / 240
 // bytes) around their 136 / 210 chunk bytes.
 __host__ __device__ constexpr int chunk_values(int wt) {
-    return (wt == kF16 || wt == kBF16) ? 72 : wt == kF32 ? 36 : wt == kQ8_0 ? 128 : 256;
+    return is_affine(wt) ? 1024 / affine_bits(wt)
+           : (wt == kF16 || wt == kBF16) ? 72 : wt == kF32 ? 36 : wt == kQ8_0 ? 128 : 256;
 }
 __host__ __device__ constexpr int chunk_box(int wt) {
-    return (wt == kF16 || wt == kBF16 || wt == kF32 || wt == kQ8_0 || wt == kQ4_K) ? 144 : wt == kQ5_0 ? 176
-           : 240;
+    return (is_affine(wt) || wt == kF16 || wt == kBF16 || wt == kF32 || wt == kQ8_0 || wt == kQ4_K) ? 144
+           : wt == kQ5_0 ? 176 : 240;
 }
 
 // Kernel argument block (one launch).  Grid: a number of clusters of
@@ -63,6 +78,10 @@ struct MvArgs {
     float alpha, beta;
     const float* c;          // addend, element (b, j, i) at b*cbs + j*crs + i (read only when epi == 2)
     uint32_t crs, cbs;
+    // affine weights: binary16 scale and bias of group g of global row r at r*ngroups + g
+    const uint16_t* scales;
+    const uint16_t* biases;
+    uint32_t ngroups;
 };
 
 // Kernel lookup: rem_mv_kernel<wt, m, nr0>, m in 1..8, nr0 in {1, 2}.
@@ -78,6 +97,12 @@ REM_DECLARE_PARTS(mv_kernel_q4_k)
 REM_DECLARE_PARTS(mv_kernel_q6_k)
 REM_DECLARE_PARTS(mv_kernel_f32)
 REM_DECLARE_PARTS(mv_kernel_bf16)
+REM_DECLARE_PARTS(mv_kernel_a4g32)
+REM_DECLARE_PARTS(mv_kernel_a4g64)
+REM_DECLARE_PARTS(mv_kernel_a4g128)
+REM_DECLARE_PARTS(mv_kernel_a8g32)
+REM_DECLARE_PARTS(mv_kernel_a8g64)
+REM_DECLARE_PARTS(mv_kernel_a8g128)
 #undef REM_DECLARE_PARTS
 
 // Dynamic shared memory of one CTA; the kernel lays it out the same way:
@@ -100,6 +125,8 @@ inline uint32_t mv_smem_bytes(int wt, int nr0, int warps, int stages, int m, int
 // Auxiliary kernels (dequantize / quantize), rem_aux.cu.
 int launch_dequantize(const uint8_t* w, int wt, uint64_t rows, uint32_t k, uint64_t row_bytes,
                       float* out, void* stream);
+int launch_dequantize_affine(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int wt,
+                             uint64_t rows, uint32_t k, float* out, void* stream);
 int launch_quantize(const float* src, int wt, uint64_t rows, uint32_t k, uint64_t row_bytes,
                     uint8_t* w, void* stream);
 

@@ -176,7 +176,15 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // Staged bytes per row (the TMA box width) and the byte position inside the
 // staged row where chunk `cc` starts.
-template <int WT> struct Stage;
+// Affine codes (the primary template): chunk cc is the 128 bytes at 128*cc
+// (256 4-bit or 128 8-bit values), staged as a 144-byte window (an odd
+// number of 16-byte units keeps the 32 lanes' reads on distinct bank quads).
+template <int WT> struct Stage {
+    static_assert(is_affine(WT), "no staging geometry for this weight type");
+    static constexpr int kValues = 1024 / affine_bits(WT), kBox = 144;
+    __device__ static uint32_t gofs(uint32_t cc) { return cc * 128u; }
+    __device__ static int sofs(uint32_t) { return 0; }
+};
 template <> struct Stage<kF16> {
     static constexpr int kValues = 72, kBox = 144;
     __device__ static uint32_t gofs(uint32_t cc) { return cc * 144u; }  // global byte offset of the box
@@ -611,6 +619,97 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
     });
 }
 
+// Affine: values 4Q..4Q+3 of a staged row.  4-bit codes sit lowest-first, 8
+// per word: values 0..3 of a word at bits 0, 4, 8, 12 (exponents 2^23, 2^19,
+// 2^15, 2^11), values 4..7 at bits 16 and (after >> 12) 8, 12, 16.  8-bit
+// codes are the word's bytes.
+template <int BITS, int Q>
+__device__ __forceinline__ void affine_codes(const uint8_t* row, float2& w01, float2& w23) {
+    if constexpr (BITS == 8) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(row + 4 * Q);
+        const float2 bias = make_float2(-8388608.0f, -32768.0f);
+        w01 = bytes01_u(v, 0xFFu, 0xFF00u, bias);
+        w23 = bytes01_u(v >> 16, 0xFFu, 0xFF00u, bias);
+    } else {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(row + 4 * (Q / 2));
+        if constexpr ((Q & 1) == 0) {
+            w01 = add2(make_float2(fbits(lop_and_or(v, 0xFu, 0x4B000000u)), fbits(lop_and_or(v, 0xF0u, 0x49000000u))),
+                       make_float2(-8388608.0f, -524288.0f));
+            w23 = add2(make_float2(fbits(lop_and_or(v, 0xF00u, 0x47000000u)), fbits(lop_and_or(v, 0xF000u, 0x45000000u))),
+                       make_float2(-32768.0f, -2048.0f));
+        } else {
+            const uint32_t sh = v >> 12;
+            w01 = add2(make_float2(fbits(lop_and_or(v, 0xF0000u, 0x43000000u)), fbits(lop_and_or(sh, 0xF00u, 0x47000000u))),
+                       make_float2(-128.0f, -32768.0f));
+            w23 = add2(make_float2(fbits(lop_and_or(sh, 0xF000u, 0x45000000u)), fbits(lop_and_or(sh, 0xF0000u, 0x43000000u))),
+                       make_float2(-2048.0f, -128.0f));
+        }
+    }
+}
+
+// Input sums of the groups of one staged chunk (CV values, groups of GS), per
+// warp: lane l adds values 8l..8l+7 as ((x0+x1)+(x2+x3))+((x4+x5)+(x6+x7)),
+// then an xor butterfly over the GS/8 lanes of a group (distance 1, 2, ...).
+// The order is fixed and does not depend on M.  xs[g*M + j].
+template <int M, int CV, int GS>
+__device__ __forceinline__ void xsum_groups(const float* xc, float* xs, int lane) {
+    constexpr int LG = GS / 8;
+    const bool live = 8 * lane < CV;
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+        float s = 0.0f;
+        if (live) {
+            const float4 a = ldx4(xc + j * CV + 8 * lane);
+            const float4 b = ldx4(xc + j * CV + 8 * lane + 4);
+            s = __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w)),
+                          __fadd_rn(__fadd_rn(b.x, b.y), __fadd_rn(b.z, b.w)));
+        }
+#pragma unroll
+        for (int off = 1; off < LG; off <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, off));
+        if (live && (lane % LG) == 0) xs[(lane / LG) * M + j] = s;
+    }
+}
+
+// Affine chunk: for every group g, c = the chain of its value pairs, then
+// acc = fma2((scale, scale), c, acc) and acc.x = fma(bias, sum of the group's
+// inputs, acc.x).  Scales and biases come from global memory (rows past n
+// read none).
+template <int M, int NR0, int WT>
+__device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], const float* xc, float* xs,
+                                             int lane, const MvArgs& a, uint32_t b, uint32_t wrow0, uint32_t cc,
+                                             float2 (&acc)[NR0][M]) {
+    constexpr int BITS = affine_bits(WT), GS = affine_group(WT);
+    constexpr int CV = Stage<WT>::kValues, NG = CV / GS;
+    xsum_groups<M, CV, GS>(xc, xs, lane);
+    __syncwarp();
+    uint64_t base[NR0];
+    bool live[NR0];
+#pragma unroll
+    for (int i = 0; i < NR0; ++i) {
+        const uint32_t row = wrow0 + static_cast<uint32_t>(lane + 32 * i);
+        live[i] = row < a.n;
+        base[i] = (static_cast<uint64_t>(b) * a.n + row) * a.ngroups + static_cast<uint64_t>(cc) * NG;
+    }
+    static_for<0, NG>([&](auto gc) {
+        constexpr int g = decltype(gc)::value;
+        float sc[NR0], bi[NR0];
+#pragma unroll
+        for (int i = 0; i < NR0; ++i) {
+            sc[i] = live[i] ? h2f(__ldg(a.scales + base[i] + g)) : 0.0f;
+            bi[i] = live[i] ? h2f(__ldg(a.biases + base[i] + g)) : 0.0f;
+        }
+        float2 c[NR0][M];
+        chain<M, NR0, GS / 4, CV>(c, xc + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
+            affine_codes<BITS, g * (GS / 4) + decltype(qc)::value>(rows[i], w01, w23);
+        });
+        apply_scale<M, NR0>(acc, c, sc);
+#pragma unroll
+        for (int i = 0; i < NR0; ++i)
+#pragma unroll
+            for (int j = 0; j < M; ++j) acc[i][j].x = __fmaf_rn(bi[i], xs[g * M + j], acc[i][j].x);
+    });
+}
+
 // Sub-block input sums of one Q4_K chunk, per warp: lane (u = lane/4,
 // quarter = lane%4) adds 8 inputs, then two xor-shuffles combine the quarters
 // as (q0 + q1) + (q2 + q3).  The order is fixed and does not depend on M.
@@ -668,7 +767,10 @@ __device__ __forceinline__ void stage_w_plain(uint8_t* dst_rows, const uint8_t* 
                                               int nrows, uint32_t cc, uint32_t k, int lane) {
     constexpr int BOX = Stage<WT>::kBox;
     uint32_t first, len;  // byte range of the chunk inside the row
-    if constexpr (WT == kF16 || WT == kBF16) {
+    if constexpr (is_affine(WT)) {
+        first = cc * 128u;
+        len = static_cast<uint32_t>(min(static_cast<uint64_t>(128u), row_bytes - first));
+    } else if constexpr (WT == kF16 || WT == kBF16) {
         first = cc * 144u;
         len = 2u * min(72u, k - cc * 72u);
     } else if constexpr (WT == kF32) {
@@ -748,14 +850,17 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
 // Decode + multiply one staged chunk for the warp's rows.
 template <int WT, int M, int NR0>
 __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int warp, int lane, uint32_t cc,
-                                         float* xs, float2 (&acc)[NR0][M]) {
+                                         float* xs, float2 (&acc)[NR0][M], const MvArgs& a, uint32_t b,
+                                         uint32_t wrow0) {
     constexpr int BOX = Stage<WT>::kBox;
     constexpr int ROWS = kLanes * NR0;
     const uint8_t* rows[NR0];
 #pragma unroll
     for (int i = 0; i < NR0; ++i) rows[i] = st + (warp * ROWS + lane + 32 * i) * BOX;
     const float* xc = reinterpret_cast<const float*>(st + wstage);  // [M][CV]
-    if constexpr (WT == kF16) {
+    if constexpr (is_affine(WT)) {
+        chunk_affine<M, NR0, WT>(rows, xc, xs, lane, a, b, wrow0, cc, acc);
+    } else if constexpr (WT == kF16) {
         chunk_f16<M, NR0>(rows, xc, acc);
     } else if constexpr (WT == kBF16 || WT == kF32) {
         chunk_dense<M, NR0, WT>(rows, xc, acc);
@@ -1010,7 +1115,7 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             if (failed) continue;  // keep walking so every barrier below is still reached
             if (wactive)
                 mv_chunk<WT, M, NR0>(smem + st * stage_bytes, wstage, warp, lane, c0 + static_cast<uint32_t>(q), xs,
-                                     acc);
+                                     acc, a, b, wrow0);
             __syncwarp();
             if (lane == 0) mbar_arrive(eb + 8 * st);
         }

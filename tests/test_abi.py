@@ -45,7 +45,7 @@ def test_row_bytes(lib, wt, k, expect):
 
 
 def test_row_bytes_unknown_type(lib):
-    assert rem.rem_row_bytes(9, 4096) == 0
+    assert rem.rem_row_bytes(99, 4096) == 0
 
 
 @pytest.mark.parametrize("wt,rows,k,expect", [
@@ -65,7 +65,7 @@ def test_split_factor_from_shape(lib, wt, rows, k, expect):
 def test_split_factor_degenerate(lib):
     assert rem.rem_split_factor("q8_0", 0, 4096) == 0
     assert rem.rem_split_factor("q8_0", 64, 0) == 0
-    assert rem.rem_split_factor(7, 64, 256) == 0
+    assert rem.rem_split_factor(99, 64, 256) == 0
 
 
 W, X, Y = 0x100000, 0x200000, 0x300000     # aligned fake addresses, never dereferenced
@@ -89,7 +89,7 @@ CASES = [
     ("split", dict(split=17), "split (17)"),
     ("rows_per_cta", dict(rows_per_cta=48), "rows_per_cta (48)"),
     ("rows_per_cta256", dict(rows_per_cta=256), "rows_per_cta (256)"),
-    ("wtype", dict(wtype=7), "unknown weight type"),
+    ("wtype", dict(wtype=99), "unknown weight type"),
     ("nullW", dict(W=0), "non-null"),
     ("nullx", dict(x=0), "non-null"),
     ("nully", dict(y=0), "non-null"),
@@ -191,3 +191,21 @@ def test_axpby_addend_rules(lib, kw, msg):
     same strides."""
     assert _axpby(**kw) == rem.REM_EINVAL
     assert msg in rem.rem_last_error(), rem.rem_last_error()
+
+
+def test_affine_types_need_the_affine_entry(lib):
+    """An affine weight type through rem_matvec_ex (no scales) is refused, as
+    is a non-affine type, a null scale array or a k off the group size
+    through rem_matvec_affine; rem_dequantize and rem_quantize refuse affine
+    types."""
+    assert _ex(wtype=rem.A4_G64, k=256, x_row_stride=256) == rem.REM_EINVAL
+    assert "rem_matvec_affine" in rem.rem_last_error()
+    aff = lambda **kw: rem.rem_matvec_affine(kw.get("codes", W), kw.get("scales", 0x500000), kw.get("biases", 0x600000),
+                                             kw.get("wtype", rem.A4_G64), 64, kw.get("k", 256), 1, X, 2, 256, 0, Y, 64,
+                                             0, 0, stream=0)
+    assert aff(wtype=rem.Q8_0) == rem.REM_EINVAL and "not an affine" in rem.rem_last_error()
+    assert aff(scales=0) == rem.REM_EINVAL and "scales and biases" in rem.rem_last_error()
+    assert aff(k=96) == rem.REM_EINVAL and "multiple of 64" in rem.rem_last_error()
+    assert rem.rem_dequantize(W, rem.A8_G32, 4, 256, Y, stream=0) == rem.REM_EINVAL
+    assert rem.rem_quantize(X, rem.A8_G32, 4, 256, W, stream=0) == rem.REM_EINVAL
+    assert rem.rem_row_bytes(rem.A4_G32, 4096) == 2048 and rem.rem_row_bytes(rem.A8_G128, 4096) == 4096

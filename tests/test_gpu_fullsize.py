@@ -133,3 +133,36 @@ def test_full_size_many_rows_and_bias():
     ref = y_ref + bias[rows.astype(np.int64)].astype(np.float64)[:, None]
     tol = 1e-4 * a_ref + 1e-7 + 2.0 ** -22 * (np.abs(y_ref) + np.abs(bias[rows.astype(np.int64)])[:, None])
     assert np.all(np.abs(got - ref) <= tol)
+
+
+def test_full_size_affine_sampled():
+    """Affine 4-bit codes in groups of 64, 14336x4096, m = 1..8 through
+    rem_matvec_affine (the bench's affine workload shape), sampled rows."""
+    bits, gs, n, k = 4, 64, 14336, 4096
+    wt = rem.affine_wtype(bits, gs)
+    g = np.random.Generator(np.random.PCG64(1013))
+    codes = np.empty((n, k * bits // 32), np.uint32)
+    sc = np.empty((n, k // gs), np.uint16)
+    bi = np.empty((n, k // gs), np.uint16)
+    for r0 in range(0, n, 4096):
+        r1 = min(n, r0 + 4096)
+        v = (g.standard_normal(size=(r1 - r0, k), dtype=np.float32) * np.float32(inputs.W_STD)).astype(np.float32)
+        codes[r0:r1], sc[r0:r1], bi[r0:r1] = oracle.affine_quantize(v, bits, gs)
+    dev = H.dev()
+    cd = torch.from_numpy(codes.view(np.int32).reshape(-1)).to(dev)
+    sd = torch.from_numpy(sc.view(np.int16).reshape(-1)).to(dev)
+    bd = torch.from_numpy(bi.view(np.int16).reshape(-1)).to(dev)
+    x = inputs.activations(8, k, 2013)
+    xd = H.to_dev_f32(x)
+    rows = _sample_rows(1, n, 48, 5013)
+    first = None
+    for m in range(1, 9):
+        yd = H.canary(m * n)
+        rem.check(rem.rem_matvec_affine(cd, sd, bd, wt, n, k, 1, xd, m, k, 0, yd, n, 0, 0))
+        torch.cuda.synchronize()
+        got = yd.cpu().numpy().reshape(m, n)[:, rows.astype(np.int64)].T
+        y_ref, a_ref = oracle.affine_matvec_rows(codes, sc, bi, bits, gs, n, k, x, m, k, 0, rows)
+        assert oracle.within_tolerance(got, y_ref, a_ref).all(), m
+        if first is None:
+            first = got[:, 0].copy()
+        assert np.array_equal(got[:, 0].view(np.uint32), first.view(np.uint32)), m
