@@ -10,17 +10,20 @@
 // input rows.  K is cut into `split` contiguous ranges of chunks.  The
 // `split` CTAs of a thread-block cluster share the same rows and take one
 // range each; their partial sums are added in range order through
-// distributed shared memory by the cluster's rank-0 CTA.  Each CTA streams
-// its chunks through a ring of TMA stages: one box of weight rows and one box
-// of the matching inputs per stage, completed on one mbarrier.
+// distributed shared memory (each output by one rank of the cluster).  Each
+// CTA streams its chunks through a ring of TMA stages: one box of weight rows
+// and one box of the matching inputs per stage, completed on one mbarrier.
 //
 // Row exactness (module doc "Row exactness").  The arithmetic of output
 // (i, j) depends only on row i's bytes, input row j and `split`:
 //   * each block / sub-block u contributes through one packed chain
 //     c = fma2(w[2p..2p+1], x[2p..2p+1], c) over its value pairs in order,
 //   * then acc = fma2((a_u, a_u), c, acc) with the block scale a_u
-//     (Q4_K also acc.x = fma(-min_u, sum(x of u), acc.x); F16 acc = acc + c),
-//   * a range's partial is acc.x + acc.y, and ranges are summed in order.
+//     (Q4_K also acc.x = fma(-min_u, sum(x of u), acc.x), affine groups
+//     acc.x = fma(bias_u, sum(x of u), acc.x); F16 / BF16 / F32 chunks
+//     acc = acc + c),
+//   * a range's partial is acc.x + acc.y, and ranges are summed in order;
+//   * an optional epilogue y = fma(alpha, partial sum, beta * c) per output.
 // Nothing in that sequence depends on M, NR0, the CTA packing or the
 // staging path, so row j of an M-row launch equals the same row of an M=1
 // launch bit for bit.  fma.rn.f32x2 performs two independent, correctly
@@ -30,7 +33,7 @@
 // instruction: a code q placed in mantissa bits [p, p+w) under the exponent
 // 2^(23-p) reads as 2^(23-p) + q, and one add of -(2^(23-p) + offset)
 // yields q - offset exactly (offset 128 for int8 stored as uint8, 16 for
-// Q5_0, 32 for Q6_K).
+// Q5_0, 32 for Q6_K, 0 for Q4_K and affine codes).
 #pragma once
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -960,12 +963,13 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool fail
 // done with it.  The producer fills stages with TMA copies (rows 16-byte
 // aligned) or, as a fallback, with plain loads and stores by its 32 lanes,
 // each of which then arrives on `full`; the consumers run the same code
-// either way.  After a row block, CTAs of rank > 0 leave their partial sums
-// in shared memory (double-buffered by row-block parity), one cluster
-// barrier publishes them, and rank 0 adds them in range order through
-// distributed shared memory and stores y.  The producer takes part in that
-// barrier split-phase (arrive after issuing a row block, wait one row block
-// later), so it never stalls the stream.
+// either way.  After a row block every rank leaves its partial sums in
+// shared memory (double-buffered by row-block parity), one cluster barrier
+// publishes them, and each output is finished by one rank, which adds the
+// ranges' partials in range order through distributed shared memory and
+// stores y (see mv_finish).  The producer takes part in that barrier
+// split-phase (arrive after issuing a row block, wait one row block later),
+// so it never stalls the stream.
 template <int WT, int M, int NR0>
 __global__ void __launch_bounds__((kMaxWarps + 1) * 32)
 rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
