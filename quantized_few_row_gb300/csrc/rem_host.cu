@@ -86,6 +86,14 @@ bool log_plans() {
     return on;
 }
 
+// REM_LAYOUT=0|1|2 in the environment: the lane layout every launch must use
+// (read at each launch; -1 when unset or not one of those values).
+int forced_layout() {
+    const char* v = std::getenv("REM_LAYOUT");
+    if (!v || v[0] < '0' || v[0] >= '0' + kNumLayouts || v[1] != '\0') return -1;
+    return v[0] - '0';
+}
+
 // ---------------------------------------------------------------- driver entry points
 
 using PFN_encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -125,7 +133,7 @@ struct DeviceState {
     int sms = 0;
     int smem_optin = 0;
     int smem_per_sm = 0;
-    int max_threads[kNumWt][kMaxRows + 1][3] = {};  // per kernel <wt, m, nr0>
+    int max_threads[kNumWt][kMaxRows + 1][kNumLayouts] = {};  // per kernel <wt, m, layout>
 };
 
 std::mutex g_mu;
@@ -150,9 +158,9 @@ int device_state(DeviceState** out) {
         }
         for (int wt = 0; wt < kNumWt; ++wt) {
             for (int m = 1; m <= kMaxRows; ++m)
-                for (int nr0 = 1; nr0 <= 2; ++nr0) {
-                    const void* fn = mv_kernel(wt, m, nr0);
-                    if (!fn) continue;  // NR0 = 2 exists for some m only
+                for (int l = 0; l < kNumLayouts; ++l) {
+                    const void* fn = mv_kernel(wt, m, l);
+                    if (!fn) continue;  // some layouts exist for some m only
                     cudaFuncAttributes fa;
                     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess ||
                         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, st.smem_optin) !=
@@ -161,7 +169,7 @@ int device_state(DeviceState** out) {
                         return fail(REM_ECUDA, "rem_matvec: cannot prepare the %s kernels on device %d (%s)",
                                     wt_name(wt), dev, "no sm_103a image for this device?");
                     }
-                    st.max_threads[wt][m][nr0] = fa.maxThreadsPerBlock;
+                    st.max_threads[wt][m][l] = fa.maxThreadsPerBlock;
                 }
         }
         st.ready = true;
@@ -296,8 +304,21 @@ uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
     return s < cmax ? s : cmax;
 }
 
+// Planner weight of a lane layout.  Two rows per lane in one group share
+// every input load (1.8x).  Two lane groups (H = 2) share input loads too but
+// stage and decode each weight row twice, which pays off from four input rows
+// up, or at any m for weights without a per-block decode (F16, BF16, F32)
+// and for affine weights (whose per-group scale loads the second row of each
+// lane overlaps).
+double layout_weight(int wt, int m, int nr0, int h) {
+    if (nr0 == 2) return 1.8;
+    if (h == 1) return 1.0;
+    const bool cheap = wt == kF16 || wt == kBF16 || wt == kF32 || is_affine(wt);
+    return (m >= 4 || cheap) ? 1.2 : 0.9;
+}
+
 struct Plan {
-    int nr0, warps, stages, smem;
+    int nr0, h, warps, stages, smem;
     uint32_t cpb, grid;
     bool aligned, pdl;
 };
@@ -380,17 +401,17 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
 
-    // Rows per lane NR0, row-block width G (consumer warps per CTA) and ring
-    // depth D: the fitting triple with the best score.  The score models a
-    // kernel that is bound by how many consumer warps each SM keeps busy
-    // (latency of shared-memory loads and stage waits): the average consumer
-    // warps per SM (saturating at 8), with two rows per lane sharing every
-    // input load worth 1.8x, a single stage (no copy/compute overlap) 0.7x,
-    // the producer warp's share (G/(G+1))^2, 20% less per stage beyond two
-    // (deeper rings cost residency for no gain), all scaled by the share of
-    // resident CTA slots the last wave of row blocks keeps busy.  The weights
-    // were fitted to timings of every (NR0, G, D) on GB300 for the five
-    // formats at 4096..128256 rows.
+    // Lane layout (NR0 rows per lane and H lane groups), row-block width G
+    // (consumer warps per CTA) and ring depth D: the fitting combination with
+    // the best score.  The score models a kernel that is bound by how many
+    // consumer warps each SM keeps busy (latency of shared-memory loads and
+    // stage waits): the average consumer warps per SM (saturating at 8), times
+    // the lane layout's weight (layout_weight), a single stage (no copy /
+    // compute overlap) 0.7x, the producer warp's share (G/(G+1))^2, 20% less
+    // per stage beyond two (deeper rings cost residency for no gain), all
+    // scaled by the share of resident CTA slots the last wave of row blocks
+    // keeps busy.  The weights were fitted to timings of every (layout, G, D)
+    // on GB300 for the five formats at 4096..128256 rows.
     cudaLaunchConfig_t cfg{};
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];
@@ -406,11 +427,13 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     double best = -1.0;
     const void* fn = nullptr;
     int last_cap = 0;
-    for (int nr0 = 2; nr0 >= 1; --nr0) {
-        const void* f = mv_kernel(wt, static_cast<int>(s.m), nr0);
-        if (!f) continue;
+    const int pinned = forced_layout();
+    for (int l = kNumLayouts - 1; l >= 0; --l) {
+        const void* f = mv_kernel(wt, static_cast<int>(s.m), l);
+        if (!f || (pinned >= 0 && l != pinned)) continue;
+        const int nr0 = layout_nr0(l), h = layout_h(l);
         const uint32_t rpw = static_cast<uint32_t>(kLanes * nr0);
-        const int cap = ds->max_threads[wt][s.m][nr0];
+        const int cap = ds->max_threads[wt][s.m][l];
         for (int g = kMaxWarps; g >= 1; g /= 2) {
             if (rows_per_cta ? static_cast<uint32_t>(g) * rpw != rows_per_cta
                              : (g > 4 || static_cast<uint32_t>(g) * rpw > 256u))
@@ -424,7 +447,7 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
             const uint64_t per_cta = ((nchunk + S - 1) / S) * ((units + 2ull * ds->sms - 1) / (2ull * ds->sms));
             const int dmax = static_cast<int>(std::min<uint64_t>(kMaxStages, std::max<uint64_t>(2, per_cta)));
             for (int d = 1; d <= dmax; ++d) {
-                const int sm = static_cast<int>(mv_smem_bytes(wt, nr0, g, d, static_cast<int>(s.m), S));
+                const int sm = static_cast<int>(mv_smem_bytes(wt, nr0, h, g, d, static_cast<int>(s.m), S));
                 if (sm > ds->smem_optin) continue;
                 cfg.blockDim = dim3(static_cast<unsigned>((g + 1) * 32));
                 cfg.dynamicSmemBytes = static_cast<size_t>(sm);
@@ -435,12 +458,14 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
                 const double eff = static_cast<double>(units) / static_cast<double>(waves * ctas);
                 const double warps_sm = static_cast<double>(ctas) / ds->sms * g;
                 const double gf = static_cast<double>(g) / (g + 1);
-                double score = std::min(warps_sm, 8.0) * (nr0 == 2 ? 1.8 : 1.0) * (d == 1 ? 0.7 : 1.0) * gf * gf *
+                double score = std::min(warps_sm, 8.0) * layout_weight(wt, static_cast<int>(s.m), nr0, h) *
+                               (d == 1 ? 0.7 : 1.0) * gf * gf *
                                (1.0 - 0.2 * std::max(0, d - 2)) * eff;
                 if (score > best) {
                     best = score;
                     fn = f;
                     p.nr0 = nr0;
+                    p.h = h;
                     p.warps = g;
                     p.stages = d;
                     p.smem = sm;
@@ -449,6 +474,9 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
         }
     }
     if (best < 0) {
+        if (pinned >= 0 && !mv_kernel(wt, static_cast<int>(s.m), pinned))
+            return fail(REM_ELAUNCH, "rem_matvec: lane layout %d (REM_LAYOUT) has no %s kernel for m = %u", pinned,
+                        wt_name(wt), s.m);
         if (last_cap)
             return fail(REM_ELAUNCH, "rem_matvec: %u rows per block exceed the %s kernel's limit of %d threads",
                         rows_per_cta, wt_name(wt), last_cap);
@@ -514,9 +542,9 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
     }
     if (log_plans())
         fprintf(stderr,
-                "rem_matvec plan: %s m %u n %u k %u batch %u split %u nr0 %d warps %d stages %d smem %d grid %u "
+                "rem_matvec plan: %s m %u n %u k %u batch %u split %u nr0 %d h %d warps %d stages %d smem %d grid %u "
                 "row_blocks %llu tma %d pdl %d\n",
-                wt_name(wt), s.m, s.n, s.k, s.batch, S, p.nr0, p.warps, p.stages, p.smem, p.grid,
+                wt_name(wt), s.m, s.n, s.k, s.batch, S, p.nr0, p.h, p.warps, p.stages, p.smem, p.grid,
                 static_cast<unsigned long long>(nblocks), static_cast<int>(p.aligned), static_cast<int>(p.pdl));
 
     MvArgs a{};
@@ -573,22 +601,22 @@ int check_rows_buffer(const void* W, int wt, uint32_t rows, uint32_t k, const ch
 
 }  // namespace
 
-const void* mv_kernel(int wt, int m, int nr0) {
+const void* mv_kernel(int wt, int m, int layout) {
     const bool lo = m <= 4;
     switch (wt) {
-    case kF16: return lo ? mv_kernel_f16_a(m, nr0) : mv_kernel_f16_b(m, nr0);
-    case kQ8_0: return lo ? mv_kernel_q8_0_a(m, nr0) : mv_kernel_q8_0_b(m, nr0);
-    case kQ5_0: return lo ? mv_kernel_q5_0_a(m, nr0) : mv_kernel_q5_0_b(m, nr0);
-    case kQ4_K: return lo ? mv_kernel_q4_k_a(m, nr0) : mv_kernel_q4_k_b(m, nr0);
-    case kQ6_K: return lo ? mv_kernel_q6_k_a(m, nr0) : mv_kernel_q6_k_b(m, nr0);
-    case kF32: return lo ? mv_kernel_f32_a(m, nr0) : mv_kernel_f32_b(m, nr0);
-    case kBF16: return lo ? mv_kernel_bf16_a(m, nr0) : mv_kernel_bf16_b(m, nr0);
-    case kA4G32: return lo ? mv_kernel_a4g32_a(m, nr0) : mv_kernel_a4g32_b(m, nr0);
-    case kA4G64: return lo ? mv_kernel_a4g64_a(m, nr0) : mv_kernel_a4g64_b(m, nr0);
-    case kA4G128: return lo ? mv_kernel_a4g128_a(m, nr0) : mv_kernel_a4g128_b(m, nr0);
-    case kA8G32: return lo ? mv_kernel_a8g32_a(m, nr0) : mv_kernel_a8g32_b(m, nr0);
-    case kA8G64: return lo ? mv_kernel_a8g64_a(m, nr0) : mv_kernel_a8g64_b(m, nr0);
-    case kA8G128: return lo ? mv_kernel_a8g128_a(m, nr0) : mv_kernel_a8g128_b(m, nr0);
+    case kF16: return lo ? mv_kernel_f16_a(m, layout) : mv_kernel_f16_b(m, layout);
+    case kQ8_0: return lo ? mv_kernel_q8_0_a(m, layout) : mv_kernel_q8_0_b(m, layout);
+    case kQ5_0: return lo ? mv_kernel_q5_0_a(m, layout) : mv_kernel_q5_0_b(m, layout);
+    case kQ4_K: return lo ? mv_kernel_q4_k_a(m, layout) : mv_kernel_q4_k_b(m, layout);
+    case kQ6_K: return lo ? mv_kernel_q6_k_a(m, layout) : mv_kernel_q6_k_b(m, layout);
+    case kF32: return lo ? mv_kernel_f32_a(m, layout) : mv_kernel_f32_b(m, layout);
+    case kBF16: return lo ? mv_kernel_bf16_a(m, layout) : mv_kernel_bf16_b(m, layout);
+    case kA4G32: return lo ? mv_kernel_a4g32_a(m, layout) : mv_kernel_a4g32_b(m, layout);
+    case kA4G64: return lo ? mv_kernel_a4g64_a(m, layout) : mv_kernel_a4g64_b(m, layout);
+    case kA4G128: return lo ? mv_kernel_a4g128_a(m, layout) : mv_kernel_a4g128_b(m, layout);
+    case kA8G32: return lo ? mv_kernel_a8g32_a(m, layout) : mv_kernel_a8g32_b(m, layout);
+    case kA8G64: return lo ? mv_kernel_a8g64_a(m, layout) : mv_kernel_a8g64_b(m, layout);
+    case kA8G128: return lo ? mv_kernel_a8g128_a(m, layout) : mv_kernel_a8g128_b(m, layout);
     default: return nullptr;
     }
 }

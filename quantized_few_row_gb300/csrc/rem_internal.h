@@ -84,12 +84,22 @@ struct MvArgs {
     uint32_t ngroups;
 };
 
-// Kernel lookup: rem_mv_kernel<wt, m, nr0>, m in 1..8, nr0 in {1, 2}.
-// Each format is compiled in two units: M = 1..4 (_a) and M = 5..8 (_b).
-const void* mv_kernel(int wt, int m, int nr0);
+// Lane layouts of the mat-vec kernel.  A warp always owns 32*nr0 weight
+// rows; its lanes form h groups of 32/h lanes, each lane holding nr0*h of the
+// warp's rows (lane l: rows l%(32/h) + (32/h)*i) and ceil(m/h) of the m
+// input rows (group g: rows min(g*ceil(m/h), m - ceil(m/h)) onwards).  Every
+// input value a lane loads from shared memory then feeds nr0*h weight rows.
+constexpr int kNumLayouts = 3;
+constexpr int layout_nr0(int l) { return l == 1 ? 2 : 1; }
+constexpr int layout_h(int l) { return l == 2 ? 2 : 1; }
+
+// Kernel lookup: rem_mv_kernel<wt, m, nr0, h> of layout index `layout`
+// (0: nr0 1, h 1; 1: nr0 2, h 1; 2: nr0 1, h 2), m in 1..8; nullptr where
+// that kernel does not exist.
+const void* mv_kernel(int wt, int m, int layout);
 #define REM_DECLARE_PARTS(NAME) \
-    const void* NAME##_a(int m, int nr0); \
-    const void* NAME##_b(int m, int nr0);
+    const void* NAME##_a(int m, int layout); \
+    const void* NAME##_b(int m, int layout);
 REM_DECLARE_PARTS(mv_kernel_f16)
 REM_DECLARE_PARTS(mv_kernel_q8_0)
 REM_DECLARE_PARTS(mv_kernel_q5_0)
@@ -116,8 +126,9 @@ inline uint32_t mv_stage_bytes(int wt, int nr0, int warps, int m) {
     const uint32_t xb = (uint32_t)m * chunk_values(wt) * 4u;
     return (uint32_t)warps * kLanes * nr0 * chunk_box(wt) + ((xb + 127u) & ~127u);
 }
-inline uint32_t mv_smem_bytes(int wt, int nr0, int warps, int stages, int m, int split) {
-    const uint32_t parts = split > 1 ? 2u * (uint32_t)warps * nr0 * m * kLanes * 4u : 0u;
+inline uint32_t mv_smem_bytes(int wt, int nr0, int h, int warps, int stages, int m, int split) {
+    const uint32_t mh = (uint32_t)((m + h - 1) / h);
+    const uint32_t parts = split > 1 ? 2u * (uint32_t)warps * nr0 * h * mh * kLanes * 4u : 0u;
     return (uint32_t)stages * mv_stage_bytes(wt, nr0, warps, m) + parts + 16u * kMaxStages +
            (uint32_t)(warps + 1) * 8u * kMaxRows * 4u + 128u;
 }

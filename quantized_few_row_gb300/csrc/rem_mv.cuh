@@ -3,11 +3,13 @@
 // y[b, j, i] = sum_k W[b*n + i, k] * x[b, j, k],  j < M <= 8
 // (mlx-native 0.18.0 src/ops/row_exact_matvec.rs, module doc).
 //
-// Work mapping.  A warp owns 32*NR0 consecutive weight rows, one row per lane
-// (lane l holds rows l and l+32).  All lanes of a warp work on the same K
-// positions at the same time, so every input load is a shared-memory
-// broadcast and every weight row is read from HBM exactly once for all M
-// input rows.  K is cut into `split` contiguous ranges of chunks.  The
+// Work mapping.  A warp owns 32*NR0 consecutive weight rows.  Its lanes form
+// H groups (H = 1: lane l holds rows l and, with NR0 = 2, l+32 for all M
+// input rows; H = 2: lanes l and l+16 both hold rows l and l+16, for the
+// first and the second half of the input rows).  All lanes of a warp work on
+// the same K positions at the same time, so every input load is a
+// shared-memory broadcast (one address per lane group) feeding NR0*H rows,
+// and every weight row is read from HBM exactly once for all M input rows.  K is cut into `split` contiguous ranges of chunks.  The
 // `split` CTAs of a thread-block cluster share the same rows and take one
 // range each; their partial sums are added in range order through
 // distributed shared memory (each output by one rank of the cluster).  Each
@@ -24,7 +26,7 @@
 //     acc = acc + c),
 //   * a range's partial is acc.x + acc.y, and ranges are summed in order;
 //   * an optional epilogue y = fma(alpha, partial sum, beta * c) per output.
-// Nothing in that sequence depends on M, NR0, the CTA packing or the
+// Nothing in that sequence depends on M, NR0, H, the CTA packing or the
 // staging path, so row j of an M-row launch equals the same row of an M=1
 // launch bit for bit.  fma.rn.f32x2 performs two independent, correctly
 // rounded FMAs, identical to two scalar fmaf.
@@ -576,12 +578,13 @@ __device__ __forceinline__ void chunk_blocks32(const uint8_t* const (&rows)[NR0]
     });
 }
 
-// Q4_K super-block.  xs[u*M + j] = sum of the 32 inputs of sub-block u for
-// input row j (computed once per chunk for the warp, see xsum_q4_k).
+// Q4_K super-block.  xs[u*XSS + j] = sum of the 32 inputs of sub-block u for
+// the lane's input row j (computed once per chunk for the warp, see
+// xsum_q4_k; XSS is the launch's input row count).
 // Sub-block scales and mins: s < 4 from bytes s of scales[0..3] / [4..7];
 // s >= 4 joins the low (high) nibble of scales[s+4] with the top two bits of
 // scales[s-4] (scales[s]) -- one select per word.
-template <int M, int NR0>
+template <int M, int NR0, int XSS>
 __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], const float* xc, const float* xs,
                                            float2 (&acc)[NR0][M]) {
     float d[NR0], dmin[NR0];
@@ -617,7 +620,7 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
 #pragma unroll
             for (int i = 0; i < NR0; ++i)
 #pragma unroll
-                for (int j = 0; j < M; ++j) acc[i][j].x = __fmaf_rn(-mnv[i], xs[u * M + j], acc[i][j].x);
+                for (int j = 0; j < M; ++j) acc[i][j].x = __fmaf_rn(-mnv[i], xs[u * XSS + j], acc[i][j].x);
         });
     });
 }
@@ -676,20 +679,21 @@ __device__ __forceinline__ void xsum_groups(const float* xc, float* xs, int lane
 // Affine chunk: for every group g, c = the chain of its value pairs, then
 // acc = fma2((scale, scale), c, acc) and acc.x = fma(bias, sum of the group's
 // inputs, acc.x).  Scales and biases come from global memory (rows past n
-// read none).
-template <int M, int NR0, int WT>
-__device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], const float* xc, float* xs,
-                                             int lane, const MvArgs& a, uint32_t b, uint32_t wrow0, uint32_t cc,
-                                             float2 (&acc)[NR0][M]) {
+// read none).  The lane holds NR0 rows (warp row rl + LW*i) and M input rows
+// starting at row mb of the launch's MA; xl is its first input row.
+template <int MA, int M, int NR0, int LW, int WT>
+__device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], const float* xc, const float* xl,
+                                             float* xs, int mb, int rl, int lane, const MvArgs& a, uint32_t b,
+                                             uint32_t wrow0, uint32_t cc, float2 (&acc)[NR0][M]) {
     constexpr int BITS = affine_bits(WT), GS = affine_group(WT);
     constexpr int CV = Stage<WT>::kValues, NG = CV / GS;
-    xsum_groups<M, CV, GS>(xc, xs, lane);
+    xsum_groups<MA, CV, GS>(xc, xs, lane);
     __syncwarp();
     uint64_t base[NR0];
     bool live[NR0];
 #pragma unroll
     for (int i = 0; i < NR0; ++i) {
-        const uint32_t row = wrow0 + static_cast<uint32_t>(lane + 32 * i);
+        const uint32_t row = wrow0 + static_cast<uint32_t>(rl + LW * i);
         live[i] = row < a.n;
         base[i] = (static_cast<uint64_t>(b) * a.n + row) * a.ngroups + static_cast<uint64_t>(cc) * NG;
     }
@@ -702,14 +706,14 @@ __device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], 
             bi[i] = live[i] ? h2f(__ldg(a.biases + base[i] + g)) : 0.0f;
         }
         float2 c[NR0][M];
-        chain<M, NR0, GS / 4, CV>(c, xc + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
+        chain<M, NR0, GS / 4, CV>(c, xl + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
             affine_codes<BITS, g * (GS / 4) + decltype(qc)::value>(rows[i], w01, w23);
         });
         apply_scale<M, NR0>(acc, c, sc);
 #pragma unroll
         for (int i = 0; i < NR0; ++i)
 #pragma unroll
-            for (int j = 0; j < M; ++j) acc[i][j].x = __fmaf_rn(bi[i], xs[g * M + j], acc[i][j].x);
+            for (int j = 0; j < M; ++j) acc[i][j].x = __fmaf_rn(bi[i], xs[g * MA + mb + j], acc[i][j].x);
     });
 }
 
@@ -850,91 +854,122 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
 
 // ---------------------------------------------------------------- per-chunk and per-row-block steps
 
-// Decode + multiply one staged chunk for the warp's rows.
-template <int WT, int M, int NR0>
+// A lane's share of its warp's work under lane layout (NR0, H): the lanes
+// form H groups of LW = 32/H; lane l holds the R = NR0*H warp rows
+// rl + LW*i (rl = l % LW) and the MH = ceil(M/H) input rows mb .. mb+MH-1,
+// mb = min(g*MH, M - MH) for its group g.  With odd M the last group starts
+// early and repeats input rows of the group before it; those slots are
+// computed (identically) but stored by their owner only.
+template <int M, int NR0, int H>
+struct LaneMap {
+    static constexpr int R = NR0 * H;
+    static constexpr int MH = (M + H - 1) / H;
+    static constexpr int LW = kLanes / H;
+    __device__ __forceinline__ static int rl(int lane) { return lane % LW; }
+    __device__ __forceinline__ static int grp(int lane) { return lane / LW; }
+    __device__ __forceinline__ static int mb(int lane) { return min(grp(lane) * MH, M - MH); }
+    // slot j of the lane is its group's own input row (not a repeat)
+    __device__ __forceinline__ static bool owns(int lane, int j) { return mb(lane) + j >= grp(lane) * MH; }
+};
+
+// Decode + multiply one staged chunk for the lane's rows.
+template <int WT, int M, int NR0, int H>
 __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int warp, int lane, uint32_t cc,
-                                         float* xs, float2 (&acc)[NR0][M], const MvArgs& a, uint32_t b,
-                                         uint32_t wrow0) {
+                                         float* xs, float2 (&acc)[NR0 * H][(M + H - 1) / H], const MvArgs& a,
+                                         uint32_t b, uint32_t wrow0) {
+    using L = LaneMap<M, NR0, H>;
+    constexpr int R = L::R, MH = L::MH, LW = L::LW;
     constexpr int BOX = Stage<WT>::kBox;
+    constexpr int CV = Stage<WT>::kValues;
     constexpr int ROWS = kLanes * NR0;
-    const uint8_t* rows[NR0];
+    const int rl = L::rl(lane), mb = L::mb(lane);
+    const uint8_t* rows[R];
 #pragma unroll
-    for (int i = 0; i < NR0; ++i) rows[i] = st + (warp * ROWS + lane + 32 * i) * BOX;
+    for (int i = 0; i < R; ++i) rows[i] = st + (warp * ROWS + rl + LW * i) * BOX;
     const float* xc = reinterpret_cast<const float*>(st + wstage);  // [M][CV]
+    const float* xl = xc + mb * CV;                                  // the lane's first input row
     if constexpr (is_affine(WT)) {
-        chunk_affine<M, NR0, WT>(rows, xc, xs, lane, a, b, wrow0, cc, acc);
+        chunk_affine<M, MH, R, LW, WT>(rows, xc, xl, xs, mb, rl, lane, a, b, wrow0, cc, acc);
     } else if constexpr (WT == kF16) {
-        chunk_f16<M, NR0>(rows, xc, acc);
+        chunk_f16<MH, R>(rows, xl, acc);
     } else if constexpr (WT == kBF16 || WT == kF32) {
-        chunk_dense<M, NR0, WT>(rows, xc, acc);
+        chunk_dense<MH, R, WT>(rows, xl, acc);
     } else if constexpr (WT == kQ8_0) {
-        if (Stage<WT>::sofs(cc) == 0) chunk_blocks32<M, NR0, BlkQ8, 4, 34, 0>(rows, xc, acc);
-        else chunk_blocks32<M, NR0, BlkQ8, 4, 34, 8>(rows, xc, acc);
+        if (Stage<WT>::sofs(cc) == 0) chunk_blocks32<MH, R, BlkQ8, 4, 34, 0>(rows, xl, acc);
+        else chunk_blocks32<MH, R, BlkQ8, 4, 34, 8>(rows, xl, acc);
     } else if constexpr (WT == kQ5_0) {
-        chunk_blocks32<M, NR0, BlkQ5, 8, 22, 0>(rows, xc, acc);
+        chunk_blocks32<MH, R, BlkQ5, 8, 22, 0>(rows, xl, acc);
     } else if constexpr (WT == kQ4_K) {
         xsum_q4_k<M>(xc, xs, lane);
         __syncwarp();
-        chunk_q4_k<M, NR0>(rows, xc, xs, acc);
+        chunk_q4_k<MH, R, M>(rows, xl, xs + mb, acc);
     } else {
-        chunk_q6_k<M, NR0>(rows, xc, Stage<WT>::sofs(cc), acc);
+        static_assert(WT != kQ6_K || H == 1, "Q6_K keeps one lane group");
+        chunk_q6_k<MH, R>(rows, xl, Stage<WT>::sofs(cc), acc);
     }
 }
 
 // End of a row block for one consumer warp: the range partial
 // (acc.x + acc.y), then either the store (split 1) or the in-order sum of the
 // cluster's ranges.  With split S every rank publishes its partials in shared
-// memory, one cluster barrier makes them visible, and output (i, j) of the
-// warp's rows is finished by rank (i*M + j) mod S: it loads the S partials of
-// that output (its own and the peers', through distributed shared memory),
-// all loads issued before the first add, and adds them in rank order.  Every
-// thread of every CTA of the cluster reaches the cluster barrier once per row
-// block.
-template <int M, int NR0>
-__device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool failed, const MvArgs& a, uint32_t b,
-                                          uint32_t wrow0, bool wactive, int lane, int warp,
-                                          uint32_t s, uint32_t S, uint32_t t, float* parts, uint32_t part_floats) {
-    float part[NR0][M];
+// memory, one cluster barrier makes them visible, and slot (i, j) of each
+// lane is finished by rank (i*MH + j) mod S: it loads the S partials of that
+// output (its own and the peers', through distributed shared memory), all
+// loads issued before the first add, and adds them in rank order.  Slots
+// that repeat another group's input row are neither finished nor stored.
+// Every thread of every CTA of the cluster reaches the cluster barrier once
+// per row block.
+template <int M, int NR0, int H>
+__device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0 * H][(M + H - 1) / H], bool failed,
+                                          const MvArgs& a, uint32_t b, uint32_t wrow0, bool wactive, int lane,
+                                          int warp, uint32_t s, uint32_t S, uint32_t t, float* parts,
+                                          uint32_t part_floats) {
+    using L = LaneMap<M, NR0, H>;
+    constexpr int R = L::R, MH = L::MH, LW = L::LW;
+    const int rl = L::rl(lane), mb = L::mb(lane);
+    float part[R][MH];
 #pragma unroll
-    for (int i = 0; i < NR0; ++i)
+    for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int j = 0; j < M; ++j)
+        for (int j = 0; j < MH; ++j)
             part[i][j] = failed ? __int_as_float(0x7FC00000) : __fadd_rn(acc[i][j].x, acc[i][j].y);
     // the store, with the optional epilogue alpha * acc + beta * c (each output
     // element on its own, after the fixed reduction: row exactness is kept)
     auto store = [&](int i, int j, float v) {
-        const uint32_t row = wrow0 + static_cast<uint32_t>(lane + 32 * i);
+        const uint32_t row = wrow0 + static_cast<uint32_t>(rl + LW * i);
+        const uint64_t m = static_cast<uint64_t>(mb + j);
         if (row >= a.n) return;
         if (a.epi == 1) {
             v = __fmul_rn(a.alpha, v);
         } else if (a.epi == 2) {
-            const float cv = a.c[static_cast<uint64_t>(b) * a.cbs + static_cast<uint64_t>(j) * a.crs + row];
+            const float cv = a.c[static_cast<uint64_t>(b) * a.cbs + m * a.crs + row];
             v = __fmaf_rn(a.alpha, v, __fmul_rn(a.beta, cv));
         }
-        a.y[static_cast<uint64_t>(b) * a.ybs + static_cast<uint64_t>(j) * a.yrs + row] = v;
+        a.y[static_cast<uint64_t>(b) * a.ybs + m * a.yrs + row] = v;
     };
     if (S == 1) {
         if (wactive) {
 #pragma unroll
-            for (int i = 0; i < NR0; ++i)
+            for (int i = 0; i < R; ++i)
 #pragma unroll
-                for (int j = 0; j < M; ++j) store(i, j, part[i][j]);
+                for (int j = 0; j < MH; ++j)
+                    if (L::owns(lane, j)) store(i, j, part[i][j]);
         }
         return;
     }
     float* buf = parts + (t & 1u) * part_floats;
 #pragma unroll
-    for (int i = 0; i < NR0; ++i)
+    for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int j = 0; j < M; ++j) buf[((warp * NR0 + i) * M + j) * 32 + lane] = part[i][j];
+        for (int j = 0; j < MH; ++j) buf[((warp * R + i) * MH + j) * 32 + lane] = part[i][j];
     cluster_sync();  // phase t: the ranges' partials of this row block are published
     if (wactive) {
 #pragma unroll
-        for (int i = 0; i < NR0; ++i)
+        for (int i = 0; i < R; ++i)
 #pragma unroll
-            for (int j = 0; j < M; ++j) {
-                if (static_cast<uint32_t>(i * M + j) % S != s) continue;
-                const float* slot = buf + ((warp * NR0 + i) * M + j) * 32 + lane;
+            for (int j = 0; j < MH; ++j) {
+                if (static_cast<uint32_t>(i * MH + j) % S != s || !L::owns(lane, j)) continue;
+                const float* slot = buf + ((warp * R + i) * MH + j) * 32 + lane;
                 float p[kMaxSplit];
 #pragma unroll
                 for (int r = 0; r < kMaxSplit; ++r)
@@ -970,7 +1005,7 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0][M], bool fail
 // stores y (see mv_finish).  The producer takes part in that barrier
 // split-phase (arrive after issuing a row block, wait one row block later),
 // so it never stalls the stream.
-template <int WT, int M, int NR0>
+template <int WT, int M, int NR0, int H>
 __global__ void __launch_bounds__((kMaxWarps + 1) * 32)
 rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
     constexpr int BOX = Stage<WT>::kBox;
@@ -992,8 +1027,9 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     const uint32_t ncl = gridDim.x / S;
     const uint32_t wstage = static_cast<uint32_t>(G * ROWS * BOX);
     const uint32_t stage_bytes = wstage + XPAD;
-    const uint32_t part_floats = static_cast<uint32_t>(G * NR0 * M * 32);
-    float* parts = reinterpret_cast<float*>(smem + D * stage_bytes);  // [2][G][NR0][M][32] when S > 1
+    constexpr int R = LaneMap<M, NR0, H>::R, MH = LaneMap<M, NR0, H>::MH;
+    const uint32_t part_floats = static_cast<uint32_t>(G * R * MH * 32);
+    float* parts = reinterpret_cast<float*>(smem + D * stage_bytes);  // [2][G][R][MH][32] when S > 1
     uint64_t* full = reinterpret_cast<uint64_t*>(parts + (S > 1 ? 2 * part_floats : 0));
     uint64_t* empty = full + kMaxStages;
     float* xs = reinterpret_cast<float*>(empty + kMaxStages) + warp * (8 * kMaxRows);
@@ -1106,11 +1142,11 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         block_origin(rb, b, row0);
         const uint32_t wrow0 = row0 + static_cast<uint32_t>(warp * ROWS);
         const bool wactive = wrow0 < a.n;
-        float2 acc[NR0][M];
+        float2 acc[R][MH];
 #pragma unroll
-        for (int r = 0; r < NR0; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int j = 0; j < M; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
+            for (int j = 0; j < MH; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
         for (int q = 0; q < nck; ++q, ++i) {
             const int st = static_cast<int>(i % D);
             if (!failed &&
@@ -1118,12 +1154,12 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 failed = true;
             if (failed) continue;  // keep walking so every barrier below is still reached
             if (wactive)
-                mv_chunk<WT, M, NR0>(smem + st * stage_bytes, wstage, warp, lane, c0 + static_cast<uint32_t>(q), xs,
-                                     acc, a, b, wrow0);
+                mv_chunk<WT, M, NR0, H>(smem + st * stage_bytes, wstage, warp, lane, c0 + static_cast<uint32_t>(q),
+                                        xs, acc, a, b, wrow0);
             __syncwarp();
             if (lane == 0) mbar_arrive(eb + 8 * st);
         }
-        mv_finish<M, NR0>(acc, failed, a, b, wrow0, wactive, lane, warp, s, S, t, parts, part_floats);
+        mv_finish<M, NR0, H>(acc, failed, a, b, wrow0, wactive, lane, warp, s, S, t, parts, part_floats);
     }
     if (S > 1) cluster_sync();
 }
@@ -1131,31 +1167,34 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 }  // namespace dev
 }  // namespace rem
 
-// Kernel pointer of one instantiation; two rows per lane (NR0 = 2) exist only
-// from M = 4 up and not for Q6_K (whose 53 staged words per row would not
-// fit twice in registers).
+// Kernel pointer of one instantiation.  Two rows per lane in one group
+// (NR0 = 2) exist from M = 4 up, two lane groups (H = 2) from M = 2 up;
+// neither for Q6_K, whose 53 staged words per row would not fit twice in
+// registers.
 namespace rem {
-template <int WT, int M, int NR0>
+template <int WT, int M, int NR0, int H>
 inline const void* mv_kernel_ptr() {
-    if constexpr (NR0 == 2 && (M < 4 || WT == kQ6_K)) {
+    if constexpr ((NR0 == 2 && (M < 4 || WT == kQ6_K)) || (H == 2 && (M < 2 || WT == kQ6_K)) ||
+                  (NR0 == 2 && H == 2)) {
         return nullptr;
     } else {
-        return reinterpret_cast<const void*>(&dev::rem_mv_kernel<WT, M, NR0>);
+        return reinterpret_cast<const void*>(&dev::rem_mv_kernel<WT, M, NR0, H>);
     }
 }
 }  // namespace rem
 
 // Each translation unit instantiates a range of M values of one weight
-// format and exposes them through a lookup function.
+// format and exposes them through a lookup function (by layout index:
+// (NR0, H) = (1, 1), (2, 1), (1, 2)).
+#define REM_LAYOUTS(WT, MM) \
+    {mv_kernel_ptr<WT, MM, 1, 1>(), mv_kernel_ptr<WT, MM, 2, 1>(), mv_kernel_ptr<WT, MM, 1, 2>()}
 #define REM_INSTANTIATE(WT, NAME, M0, NM)                                                           \
     namespace rem {                                                                                 \
-    const void* NAME(int m, int nr0) {                                                              \
-        static const void* const table[4][2] = {                                                    \
-            {mv_kernel_ptr<WT, M0, 1>(), mv_kernel_ptr<WT, M0, 2>()},                               \
-            {mv_kernel_ptr<WT, (NM > 1 ? M0 + 1 : M0), 1>(), mv_kernel_ptr<WT, (NM > 1 ? M0 + 1 : M0), 2>()}, \
-            {mv_kernel_ptr<WT, (NM > 2 ? M0 + 2 : M0), 1>(), mv_kernel_ptr<WT, (NM > 2 ? M0 + 2 : M0), 2>()}, \
-            {mv_kernel_ptr<WT, (NM > 3 ? M0 + 3 : M0), 1>(), mv_kernel_ptr<WT, (NM > 3 ? M0 + 3 : M0), 2>()}}; \
-        if (m < M0 || m >= M0 + NM || nr0 < 1 || nr0 > 2) return nullptr;                          \
-        return table[m - M0][nr0 - 1];                                                              \
+    const void* NAME(int m, int layout) {                                                           \
+        static const void* const table[4][kNumLayouts] = {                                          \
+            REM_LAYOUTS(WT, M0), REM_LAYOUTS(WT, (NM > 1 ? M0 + 1 : M0)),                           \
+            REM_LAYOUTS(WT, (NM > 2 ? M0 + 2 : M0)), REM_LAYOUTS(WT, (NM > 3 ? M0 + 3 : M0))};      \
+        if (m < M0 || m >= M0 + NM || layout < 0 || layout >= kNumLayouts) return nullptr;          \
+        return table[m - M0][layout];                                                               \
     }                                                                                               \
     }

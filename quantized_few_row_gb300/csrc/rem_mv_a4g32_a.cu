@@ -1,4 +1,4 @@
-// Instantiates rem_mv_kernel<kA4G32, M, NR0> for M = 1..4.
+// Instantiates rem_mv_kernel<kA4G32, M, NR0, H> for M = 1..4.
 #include "rem_mv.cuh"
 
 REM_INSTANTIATE(rem::kA4G32, mv_kernel_a4g32_a, 1, 4)

@@ -1,4 +1,4 @@
-// Instantiates rem_mv_kernel<kA8G128, M, NR0> for M = 1..4.
+// Instantiates rem_mv_kernel<kA8G128, M, NR0, H> for M = 1..4.
 #include "rem_mv.cuh"
 
 REM_INSTANTIATE(rem::kA8G128, mv_kernel_a8g128_a, 1, 4)

@@ -1,4 +1,4 @@
-// Instantiates rem_mv_kernel<kA8G64, M, NR0> for M = 5..8.
+// Instantiates rem_mv_kernel<kA8G64, M, NR0, H> for M = 5..8.
 #include "rem_mv.cuh"
 
 REM_INSTANTIATE(rem::kA8G64, mv_kernel_a8g64_b, 5, 4)

@@ -1,4 +1,4 @@
-// Instantiates rem_mv_kernel<kQ4_K, M, NR0> for M = 1..4.
+// Instantiates rem_mv_kernel<kQ4_K, M, NR0, H> for M = 1..4.
 #include "rem_mv.cuh"
 
 REM_INSTANTIATE(rem::kQ4_K, mv_kernel_q4_k_a, 1, 4)
