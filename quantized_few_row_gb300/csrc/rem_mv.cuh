@@ -678,9 +678,11 @@ __device__ __forceinline__ void xsum_groups(const float* xc, float* xs, int lane
 
 // Affine chunk: for every group g, c = the chain of its value pairs, then
 // acc = fma2((scale, scale), c, acc) and acc.x = fma(bias, sum of the group's
-// inputs, acc.x).  Scales and biases come from global memory (rows past n
-// read none).  The lane holds NR0 rows (warp row rl + LW*i) and M input rows
-// starting at row mb of the launch's MA; xl is its first input row.
+// inputs, acc.x).  Scales and biases come from global memory; rows past n
+// and groups past k (a last chunk that ends inside the row) read none, and
+// their zero scale and bias add exact zeros.  The lane holds NR0 rows (warp
+// row rl + LW*i) and M input rows starting at row mb of the launch's MA; xl
+// is its first input row.
 template <int MA, int M, int NR0, int LW, int WT>
 __device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], const float* xc, const float* xl,
                                              float* xs, int mb, int rl, int lane, const MvArgs& a, uint32_t b,
@@ -702,8 +704,9 @@ __device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], 
         float sc[NR0], bi[NR0];
 #pragma unroll
         for (int i = 0; i < NR0; ++i) {
-            sc[i] = live[i] ? h2f(__ldg(a.scales + base[i] + g)) : 0.0f;
-            bi[i] = live[i] ? h2f(__ldg(a.biases + base[i] + g)) : 0.0f;
+            const bool on = live[i] && cc * NG + g < a.ngroups;
+            sc[i] = on ? h2f(__ldg(a.scales + base[i] + g)) : 0.0f;
+            bi[i] = on ? h2f(__ldg(a.biases + base[i] + g)) : 0.0f;
         }
         float2 c[NR0][M];
         chain<M, NR0, GS / 4, CV>(c, xl + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
@@ -1170,7 +1173,7 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 // Kernel pointer of one instantiation.  Two rows per lane in one group
 // (NR0 = 2) exist from M = 4 up, two lane groups (H = 2) from M = 2 up;
 // neither for Q6_K, whose 53 staged words per row would not fit twice in
-// registers.
+// registers (and whose decode, not the input loads, bounds it).
 namespace rem {
 template <int WT, int M, int NR0, int H>
 inline const void* mv_kernel_ptr() {

@@ -110,3 +110,29 @@ def test_affine_grouped_token_major():
     y = _run(codes, sc, bi, wt, n, k, G, x, m, G * k, k, G * n, n, m * G * n)
     y_ref, a_ref = oracle.affine_matvec(codes, sc, bi, bits, gs, n, k, G, x, m, G * k, k)
     H.assert_close_to_oracle(H.gather_y(y, G, m, n, G * n, n), y_ref, a_ref, "affine grouped")
+
+
+@pytest.mark.parametrize("bits,gs,k", [(4, 64, 320), (4, 32, 288), (4, 128, 640), (8, 32, 96), (8, 32, 224),
+                                       (8, 64, 192)])
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_affine_partial_last_chunk(bits, gs, k, m):
+    """k a multiple of the group size but not of the staged chunk (256 4-bit or
+    128 8-bit values): the groups past k read no scale or bias and add
+    nothing.  The scale and bias arrays are followed by NaN halves on the
+    device, so a read past the last row's groups would show as NaN."""
+    wt = rem.affine_wtype(bits, gs)
+    n = 37
+    codes, sc, bi = oracle.affine_quantize(inputs.weights(n, k, 540), bits, gs)
+    x = inputs.activations(m, k, 640)
+    guard = np.full(64, 0x7E00, dtype=np.uint16)
+    ch, cp = _dev(codes)
+    sh, sp = _dev(np.concatenate([sc.reshape(-1), guard]))
+    bh, bp = _dev(np.concatenate([bi.reshape(-1), guard]))
+    xd = H.to_dev_f32(x)
+    yd = H.canary(m * n)
+    rem.check(rem.rem_matvec_affine(cp, sp, bp, wt, n, k, 1, xd, m, k, 0, yd, n, 0, 0))
+    torch.cuda.synchronize()
+    y = yd.cpu().numpy().reshape(1, m, n)
+    y_ref, a_ref = oracle.affine_matvec(codes, sc, bi, bits, gs, n, k, 1, x, m, k, 0)
+    assert np.all(np.isfinite(y))
+    H.assert_close_to_oracle(y, y_ref, a_ref, f"a{bits} g{gs} k={k} m={m}")

@@ -45,15 +45,11 @@ def pinned(layout):
             os.environ["REM_LAYOUT"] = old
 
 
-def layouts(fmt, m):
-    """Layouts with a kernel for (fmt, m): 1 needs m >= 4, 2 needs m >= 2, neither exists for Q6_K."""
-    out = [0]
-    if fmt != "q6_K":
-        if m >= 4:
-            out.append(1)
-        if m >= 2:
-            out.append(2)
-    return out
+def layouts(m, fmt="q8_0"):
+    """Layouts with a kernel for (m, fmt): 1 needs m >= 4, 2 needs m >= 2; Q6_K has layout 0 only."""
+    if fmt == "q6_K":
+        return [0]
+    return [0] + ([1] if m >= 4 else []) + ([2] if m >= 2 else [])
 
 
 # (format, n, k, batch, m, split, token-major, weight byte offset)
@@ -68,7 +64,9 @@ CASES = [
     ("f16", 130, 520, 1, 6, 0, False, 0),      # ragged k
     ("bf16", 64, 264, 2, 4, 3, True, 0),
     ("f32", 50, 260, 1, 8, 0, False, 0),
-    ("q6_K", 64, 512, 1, 8, 0, False, 0),      # one layout only
+    ("q6_K", 64, 512, 1, 8, 0, False, 0),
+    ("q6_K", 70, 2048, 2, 5, 0, True, 0),      # super-blocks at every 2-byte offset of the staged window
+    ("q6_K", 33, 768, 1, 3, 3, False, 2),      # plain staging
 ]
 
 
@@ -85,7 +83,7 @@ def test_layouts_bitwise_equal_and_match_oracle(fmt, n, k, batch, m, split, tm, 
         xrs, xbs, yrs, ybs = k, m * k, n, m * n
     y_ref, a_ref = oracle.matvec(w, fmt, n, k, batch, x, m, xrs, xbs)
     got = {}
-    for lay in layouts(fmt, m):
+    for lay in layouts(m, fmt):
         with pinned(lay):
             y = H.run_matvec(w, fmt, n, k, batch, x, m, xrs, xbs, yrs, ybs, batch * m * n, split=split,
                              w_offset=off)
@@ -119,7 +117,7 @@ def test_layouts_epilogue(fmt):
     wh, wp = H.to_dev_bytes(w)
     xd, cd = H.to_dev_f32(x), H.to_dev_f32(c)
     outs = {}
-    for lay in layouts(fmt, m):
+    for lay in layouts(m, fmt):
         yd = H.canary(m * n)
         with pinned(lay):
             rem.check(rem.rem_matvec_axpby(wp, fmt, n, k, 1, xd, m, k, 0, yd, n, 0, -1.75, 0.3, cd, n, 0))
@@ -146,7 +144,7 @@ def test_layouts_affine(bits, gs):
     bh, bp = H.to_dev_bytes(np.ascontiguousarray(bi).view(np.uint8))
     xd = H.to_dev_f32(x)
     outs = {}
-    for lay in layouts("q8_0", m):
+    for lay in layouts(m):
         yd = H.canary(batch * m * n)
         with pinned(lay):
             rem.check(rem.rem_matvec_affine(cp, sp, bp, wt, n, k, batch, xd, m, k, m * k, yd, n, m * n, 0))
