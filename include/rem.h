@@ -35,8 +35,8 @@
  * schedule to stderr.  REM_LAYOUT=0, 1 or 2 (read at every launch) pins the
  * lane layout of the mat-vec kernels: one weight row per lane, two rows per
  * lane, or two lane groups of two rows each sharing the input rows; a call
- * whose m has no kernel of that layout (1: m < 4, 2: m < 2; neither for
- * Q6_K) returns REM_ELAUNCH.  The layout never changes the results' bits; the
+ * whose m has no kernel of that layout (2: m < 2; Q6_K has layout 0 only)
+ * returns REM_ELAUNCH.  The layout never changes the results' bits; the
  * pin exists to test exactly that.
  */
 #ifndef REM_H

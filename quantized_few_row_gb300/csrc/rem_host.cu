@@ -305,13 +305,14 @@ uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
 }
 
 // Planner weight of a lane layout.  Two rows per lane in one group share
-// every input load (1.8x).  Two lane groups (H = 2) share input loads too but
-// stage and decode each weight row twice, which pays off from four input rows
-// up, or at any m for weights without a per-block decode (F16, BF16, F32)
-// and for affine weights (whose per-group scale loads the second row of each
-// lane overlaps).
+// every input load (1.8x; 1.3x at m = 1, where the input loads weigh less
+// against the decode, except for affine weights, whose per-group scale loads
+// the second row of each lane overlaps).  Two lane groups (H = 2) share input
+// loads too but stage and decode each weight row twice, which pays off from
+// four input rows up, or at any m for weights without a per-block decode
+// (F16, BF16, F32) and for affine weights.
 double layout_weight(int wt, int m, int nr0, int h) {
-    if (nr0 == 2) return 1.8;
+    if (nr0 == 2) return (m >= 2 || is_affine(wt)) ? 1.8 : 1.3;
     if (h == 1) return 1.0;
     const bool cheap = wt == kF16 || wt == kBF16 || wt == kF32 || is_affine(wt);
     return (m >= 4 || cheap) ? 1.2 : 0.9;

@@ -292,6 +292,15 @@ __device__ __forceinline__ uint32_t u32_at(const uint32_t (&W)[N]) {
     }
 }
 
+// Word I (0..3) of a 16-byte line.
+template <int I>
+__device__ __forceinline__ uint32_t word_of(const uint4& v) {
+    if constexpr (I == 0) return v.x;
+    else if constexpr (I == 1) return v.y;
+    else if constexpr (I == 2) return v.z;
+    else return v.w;
+}
+
 // Spread the 4 low bits of h to bit 4 of each byte (bit k -> bit 8k+4).
 __device__ __forceinline__ uint32_t spread4(uint32_t h) { return (h * 0x02040810u) & 0x10101010u; }
 
@@ -611,10 +620,14 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
                 mnv[i] = __fmul_rn(dmin[i], ubyte_f<u & 3>(mnw[i][u >> 2], 0x3Fu));
             }
             float2 c[NR0][M];
-            // the qs word of group Q is read when the chain needs it
+            // qs words 4t..4t+3 of the pair are read as one 16-byte line when
+            // the chain first needs them (4-byte reads at the 144-byte row
+            // stride would hit 8 banks from 32 lanes)
+            uint4 qv[NR0];
             chain<M, NR0, 8, 256>(c, xc + 32 * u, [&](auto qc, int i, float2& w01, float2& w23) {
-                const uint32_t v = *reinterpret_cast<const uint32_t*>(rows[i] + 16 + 32 * cq + 4 * decltype(qc)::value);
-                q4k_group<H>(v, w01, w23);
+                constexpr int Q = decltype(qc)::value;
+                if constexpr ((Q & 3) == 0) qv[i] = lds16(rows[i] + 16 + 32 * cq + 4 * Q);
+                q4k_group<H>(word_of<Q & 3>(qv[i]), w01, w23);
             });
             apply_scale<M, NR0>(acc, c, sc);
 #pragma unroll
@@ -625,19 +638,18 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
     });
 }
 
-// Affine: values 4Q..4Q+3 of a staged row.  4-bit codes sit lowest-first, 8
-// per word: values 0..3 of a word at bits 0, 4, 8, 12 (exponents 2^23, 2^19,
+// Affine: values 4Q..4Q+3 of a staged row from their code word v (word Q
+// for 8-bit codes, word Q/2 for 4-bit).  4-bit codes sit lowest-first, 8 per
+// word: values 0..3 of a word at bits 0, 4, 8, 12 (exponents 2^23, 2^19,
 // 2^15, 2^11), values 4..7 at bits 16 and (after >> 12) 8, 12, 16.  8-bit
 // codes are the word's bytes.
 template <int BITS, int Q>
-__device__ __forceinline__ void affine_codes(const uint8_t* row, float2& w01, float2& w23) {
+__device__ __forceinline__ void affine_codes(uint32_t v, float2& w01, float2& w23) {
     if constexpr (BITS == 8) {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(row + 4 * Q);
         const float2 bias = make_float2(-8388608.0f, -32768.0f);
         w01 = bytes01_u(v, 0xFFu, 0xFF00u, bias);
         w23 = bytes01_u(v >> 16, 0xFFu, 0xFF00u, bias);
     } else {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(row + 4 * (Q / 2));
         if constexpr ((Q & 1) == 0) {
             w01 = add2(make_float2(fbits(lop_and_or(v, 0xFu, 0x4B000000u)), fbits(lop_and_or(v, 0xF0u, 0x49000000u))),
                        make_float2(-8388608.0f, -524288.0f));
@@ -709,8 +721,14 @@ __device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], 
             bi[i] = on ? h2f(__ldg(a.biases + base[i] + g)) : 0.0f;
         }
         float2 c[NR0][M];
+        // code words are read as 16-byte lines when the chain first needs
+        // them (a group's codes are a whole number of lines)
+        uint4 cv[NR0];
         chain<M, NR0, GS / 4, CV>(c, xl + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
-            affine_codes<BITS, g * (GS / 4) + decltype(qc)::value>(rows[i], w01, w23);
+            constexpr int Q = g * (GS / 4) + decltype(qc)::value;
+            constexpr int WI = BITS == 8 ? Q : Q / 2;  // code word of values 4Q..4Q+3
+            if constexpr ((WI & 3) == 0 && (BITS == 8 || (Q & 1) == 0)) cv[i] = lds16(rows[i] + 4 * WI);
+            affine_codes<BITS, Q>(word_of<WI & 3>(cv[i]), w01, w23);
         });
         apply_scale<M, NR0>(acc, c, sc);
 #pragma unroll
@@ -1171,14 +1189,13 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 }  // namespace rem
 
 // Kernel pointer of one instantiation.  Two rows per lane in one group
-// (NR0 = 2) exist from M = 4 up, two lane groups (H = 2) from M = 2 up;
+// (NR0 = 2) exist for every M, two lane groups (H = 2) from M = 2 up;
 // neither for Q6_K, whose 53 staged words per row would not fit twice in
 // registers (and whose decode, not the input loads, bounds it).
 namespace rem {
 template <int WT, int M, int NR0, int H>
 inline const void* mv_kernel_ptr() {
-    if constexpr ((NR0 == 2 && (M < 4 || WT == kQ6_K)) || (H == 2 && (M < 2 || WT == kQ6_K)) ||
-                  (NR0 == 2 && H == 2)) {
+    if constexpr ((NR0 == 2 && WT == kQ6_K) || (H == 2 && (M < 2 || WT == kQ6_K)) || (NR0 == 2 && H == 2)) {
         return nullptr;
     } else {
         return reinterpret_cast<const void*>(&dev::rem_mv_kernel<WT, M, NR0, H>);

@@ -46,15 +46,16 @@ def pinned(layout):
 
 
 def layouts(m, fmt="q8_0"):
-    """Layouts with a kernel for (m, fmt): 1 needs m >= 4, 2 needs m >= 2; Q6_K has layout 0 only."""
+    """Layouts with a kernel for (m, fmt): 2 needs m >= 2; Q6_K has layout 0 only."""
     if fmt == "q6_K":
         return [0]
-    return [0] + ([1] if m >= 4 else []) + ([2] if m >= 2 else [])
+    return [0, 1] + ([2] if m >= 2 else [])
 
 
 # (format, n, k, batch, m, split, token-major, weight byte offset)
 CASES = [
     ("q8_0", 100, 1024, 1, 5, 0, False, 0),    # ragged n, odd m, automatic split
+    ("q4_K", 150, 1024, 1, 1, 0, False, 0),    # m = 1: one or two rows per lane
     ("q8_0", 100, 1024, 1, 8, 1, False, 0),    # split 1: direct stores
     ("q8_0", 90, 512, 1, 6, 0, False, 2),      # plain staging (rows not 16-byte aligned)
     ("q4_K", 70, 1024, 2, 7, 0, False, 0),     # batch-major, odd m
@@ -160,11 +161,11 @@ def test_pinned_layout_without_kernel_is_a_launch_error():
     wh, wp = H.to_dev_bytes(w)
     xd = H.to_dev_f32(x)
     yd = H.canary(2 * n)
-    with pinned(1):   # two rows per lane exists from m = 4 only
-        rc = rem.rem_matvec_ex(wp, "q8_0", n, k, 1, xd, 2, k, 0, yd, n, 0, 0, 0)
+    with pinned(2):   # two lane groups exist from m = 2 only
+        rc = rem.rem_matvec_ex(wp, "q8_0", n, k, 1, xd, 1, k, 0, yd, n, 0, 0, 0)
     assert rc == rem.REM_ELAUNCH
     assert "REM_LAYOUT" in rem.rem_last_error()
     torch.cuda.synchronize()
     assert np.all(yd.cpu().numpy() == H.CANARY)
-    with pinned(2):
-        rem.check(rem.rem_matvec_ex(wp, "q8_0", n, k, 1, xd, 2, k, 0, yd, n, 0, 0, 0))
+    with pinned(1):   # two rows per lane exist at every m
+        rem.check(rem.rem_matvec_ex(wp, "q8_0", n, k, 1, xd, 1, k, 0, yd, n, 0, 0, 0))
