@@ -163,6 +163,21 @@ class Clocks:
 
 # ---------------------------------------------------------------- our arm
 
+def max_over_ranks(seconds: float, world: int, device) -> float:
+    """The slowest rank's time (all ranks call it; world 1 returns its own)."""
+    if world <= 1:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step: int, steps: int, seconds: float, world: int) -> float:
+    """Whole-job GB/s: every replica processes the same step bytes; time is the slowest rank's."""
+    return world * bytes_per_step * steps / seconds / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -267,16 +282,13 @@ def run_ours(args, rank, world, local_rank):
         ev1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
-    elapsed = ev0.elapsed_time(ev1) / 1e3
+    elapsed = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
     if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
         torch.distributed.barrier()
 
     extra = 4 * batch * n if epi else 0     # the bias vector, read once per call
     step_bytes = sum(call_bytes(fmt, n, k, batch, m, rb) + extra for m in ms)
-    value = world * step_bytes * args.steps / elapsed / 1e9
+    value = job_throughput(step_bytes, args.steps, elapsed, world)
 
     # per-m device time (cold ring, graph of one call per ring slot)
     per_m = {}
@@ -330,8 +342,8 @@ def run_ours(args, rank, world, local_rank):
         yh.copy_(yp, non_blocking=True)
     t1.record(cur)
     torch.cuda.synchronize()
-    e2e_elapsed = t0.elapsed_time(t1) / 1e3
-    e2e_value = world * step_bytes * e2e_steps / e2e_elapsed / 1e9
+    e2e_elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, world, dev)
+    e2e_value = job_throughput(step_bytes, e2e_steps, e2e_elapsed, world)
     # the packed path computes what the device-resident layout does, bit for bit (same W, same split)
     for i, m in enumerate(ms):
         rem.check(call(0, m))
