@@ -32,11 +32,12 @@
  * call's name) is available from rem_last_error() on the calling thread.
  *
  * Environment.  REM_LOG_PLAN (any value, read once) prints each launch's
- * schedule to stderr.  REM_LAYOUT=0, 1 or 2 (read at every launch) pins the
- * lane layout of the mat-vec kernels: one weight row per lane, two rows per
- * lane, or two lane groups of two rows each sharing the input rows; a call
- * whose m has no kernel of that layout (2: m < 2; Q6_K has layout 0 only)
- * returns REM_ELAUNCH.  The layout never changes the results' bits; the
+ * schedule to stderr.  REM_LAYOUT=0, 1, 2 or 3 (read at every launch) pins
+ * the lane layout of the mat-vec kernels: one weight row per lane, two rows
+ * per lane, two lane groups of two rows each sharing the input rows, or two
+ * lane groups of four rows each; a call whose m has no kernel of that layout
+ * (2: m < 2; 3: m other than 6 or 8, or weights other than F16 / BF16;
+ * Q6_K has layout 0 only) returns REM_ELAUNCH.  The layout never changes the results' bits; the
  * pin exists to test exactly that.
  */
 #ifndef REM_H

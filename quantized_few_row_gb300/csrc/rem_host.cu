@@ -304,7 +304,9 @@ uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
     return s < cmax ? s : cmax;
 }
 
-// Planner weight of a lane layout.  Two rows per lane in one group share
+// Planner weight of a lane layout.  Four rows per lane (two of them in each
+// of two lane groups) share every input load four ways (2.0; they exist only
+// where they measured faster).  Two rows per lane in one group share
 // every input load (1.8x; 1.3x at m = 1, where the input loads weigh less
 // against the decode, except for affine weights, whose per-group scale loads
 // the second row of each lane overlaps).  Two lane groups (H = 2) share input
@@ -312,6 +314,7 @@ uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
 // four input rows up, or at any m for weights without a per-block decode
 // (F16, BF16, F32) and for affine weights.
 double layout_weight(int wt, int m, int nr0, int h) {
+    if (nr0 == 2 && h == 2) return 2.0;  // F16 / BF16 at m = 6, 8 (the only kernels of this layout)
     if (nr0 == 2) return (m >= 2 || is_affine(wt)) ? 1.8 : 1.3;
     if (h == 1) return 1.0;
     const bool cheap = wt == kF16 || wt == kBF16 || wt == kF32 || is_affine(wt);

@@ -89,13 +89,13 @@ struct MvArgs {
 // warp's rows (lane l: rows l%(32/h) + (32/h)*i) and ceil(m/h) of the m
 // input rows (group g: rows min(g*ceil(m/h), m - ceil(m/h)) onwards).  Every
 // input value a lane loads from shared memory then feeds nr0*h weight rows.
-constexpr int kNumLayouts = 3;
-constexpr int layout_nr0(int l) { return l == 1 ? 2 : 1; }
-constexpr int layout_h(int l) { return l == 2 ? 2 : 1; }
+constexpr int kNumLayouts = 4;
+constexpr int layout_nr0(int l) { return (l == 1 || l == 3) ? 2 : 1; }
+constexpr int layout_h(int l) { return l >= 2 ? 2 : 1; }
 
 // Kernel lookup: rem_mv_kernel<wt, m, nr0, h> of layout index `layout`
-// (0: nr0 1, h 1; 1: nr0 2, h 1; 2: nr0 1, h 2), m in 1..8; nullptr where
-// that kernel does not exist.
+// (0: nr0 1, h 1; 1: nr0 2, h 1; 2: nr0 1, h 2; 3: nr0 2, h 2), m in 1..8;
+// nullptr where that kernel does not exist.
 const void* mv_kernel(int wt, int m, int layout);
 #define REM_DECLARE_PARTS(NAME) \
     const void* NAME##_a(int m, int layout); \

@@ -5,8 +5,9 @@
 //
 // Work mapping.  A warp owns 32*NR0 consecutive weight rows.  Its lanes form
 // H groups (H = 1: lane l holds rows l and, with NR0 = 2, l+32 for all M
-// input rows; H = 2: lanes l and l+16 both hold rows l and l+16, for the
-// first and the second half of the input rows).  All lanes of a warp work on
+// input rows; H = 2: lanes l and l+16 both hold rows l and l+16 (and, with
+// NR0 = 2, l+32 and l+48), for the first and the second half of the input
+// rows).  All lanes of a warp work on
 // the same K positions at the same time, so every input load is a
 // shared-memory broadcast (one address per lane group) feeding NR0*H rows,
 // and every weight row is read from HBM exactly once for all M input rows.  K is cut into `split` contiguous ranges of chunks.  The
@@ -1191,11 +1192,16 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 // Kernel pointer of one instantiation.  Two rows per lane in one group
 // (NR0 = 2) exist for every M, two lane groups (H = 2) from M = 2 up;
 // neither for Q6_K, whose 53 staged words per row would not fit twice in
-// registers (and whose decode, not the input loads, bounds it).
+// registers (and whose decode, not the input loads, bounds it).  Both
+// together (four rows per lane) exist for F16 and BF16 at M = 6 and 8, the
+// only formats and sizes where they measured faster: every other format
+// pays more for decoding each row twice than it saves on input loads, and an
+// odd M wastes the repeated input row.
 namespace rem {
 template <int WT, int M, int NR0, int H>
 inline const void* mv_kernel_ptr() {
-    if constexpr ((NR0 == 2 && WT == kQ6_K) || (H == 2 && (M < 2 || WT == kQ6_K)) || (NR0 == 2 && H == 2)) {
+    if constexpr ((NR0 == 2 && WT == kQ6_K) || (H == 2 && (M < 2 || WT == kQ6_K)) ||
+                  (NR0 == 2 && H == 2 && ((M != 6 && M != 8) || (WT != kF16 && WT != kBF16)))) {
         return nullptr;
     } else {
         return reinterpret_cast<const void*>(&dev::rem_mv_kernel<WT, M, NR0, H>);
@@ -1205,9 +1211,10 @@ inline const void* mv_kernel_ptr() {
 
 // Each translation unit instantiates a range of M values of one weight
 // format and exposes them through a lookup function (by layout index:
-// (NR0, H) = (1, 1), (2, 1), (1, 2)).
-#define REM_LAYOUTS(WT, MM) \
-    {mv_kernel_ptr<WT, MM, 1, 1>(), mv_kernel_ptr<WT, MM, 2, 1>(), mv_kernel_ptr<WT, MM, 1, 2>()}
+// (NR0, H) = (1, 1), (2, 1), (1, 2), (2, 2)).
+#define REM_LAYOUTS(WT, MM)                                                                      \
+    {mv_kernel_ptr<WT, MM, 1, 1>(), mv_kernel_ptr<WT, MM, 2, 1>(), mv_kernel_ptr<WT, MM, 1, 2>(), \
+     mv_kernel_ptr<WT, MM, 2, 2>()}
 #define REM_INSTANTIATE(WT, NAME, M0, NM)                                                           \
     namespace rem {                                                                                 \
     const void* NAME(int m, int layout) {                                                           \

@@ -46,10 +46,11 @@ def pinned(layout):
 
 
 def layouts(m, fmt="q8_0"):
-    """Layouts with a kernel for (m, fmt): 2 needs m >= 2; Q6_K has layout 0 only."""
+    """Layouts with a kernel for (m, fmt): 2 needs m >= 2, 3 needs m in (6, 8) and F16 / BF16; Q6_K has layout 0
+    only."""
     if fmt == "q6_K":
         return [0]
-    return [0, 1] + ([2] if m >= 2 else [])
+    return [0, 1] + ([2] if m >= 2 else []) + ([3] if m in (6, 8) and fmt in ("f16", "bf16") else [])
 
 
 # (format, n, k, batch, m, split, token-major, weight byte offset)
@@ -63,7 +64,10 @@ CASES = [
     ("q5_0", 96, 1024, 3, 3, 2, True, 0),      # token-major grouped
     ("q5_0", 40, 2048, 1, 8, 8, False, 0),     # split 8 (a full cluster)
     ("f16", 130, 520, 1, 6, 0, False, 0),      # ragged k
+    ("f16", 200, 1040, 2, 8, 0, True, 8),      # four rows per lane, token-major, plain staging
+    ("f16", 70, 1040, 1, 7, 0, False, 0),
     ("bf16", 64, 264, 2, 4, 3, True, 0),
+    ("bf16", 100, 1024, 1, 8, 4, False, 0),
     ("f32", 50, 260, 1, 8, 0, False, 0),
     ("q6_K", 64, 512, 1, 8, 0, False, 0),
     ("q6_K", 70, 2048, 2, 5, 0, True, 0),      # super-blocks at every 2-byte offset of the staged window
