@@ -134,6 +134,12 @@ class Clocks:
                  "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # nvidia-smi takes a moment to start: wait (at most 5 s) for its first
+        # sample so that the timed region that follows is sampled
+        t_end = time.time() + 5.0
+        while time.time() < t_end and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
 
     def stop(self, busy_mhz_floor: float = 0.0):
         if self.proc is None:
@@ -470,7 +476,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
