@@ -315,6 +315,23 @@ def run_ours(args, rank, world, local_rank):
         stream.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / (reps * ring)
         per_m[m] = us
+    # warm, for comparison only: the same weight copy on every call (L2-resident below ~126 MB)
+    per_m_warm = {}
+    for m in ms:
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for _ in range(16):
+                    rem.check(call(0, m))
+            for _ in range(2):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(10):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        per_m_warm[m] = e0.elapsed_time(e1) * 1e3 / (10 * 16)
     clk = clocks.stop(busy_mhz_floor=0.0)
 
     # end to end through the public binding: each step's inputs (one x segment per call, packed) go
@@ -388,6 +405,7 @@ def run_ours(args, rank, world, local_rank):
                    "timed": "CUDA graphs of one step each, events on the launching stream",
                    "parallelism": f"replicas x{world}"},
         "per_m_us": {str(m): round(per_m[m], 3) for m in ms},
+        "per_m_warm_us": {str(m): round(per_m_warm[m], 3) for m in ms},
         "per_m": per_m_out,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(args.workload),
@@ -453,6 +471,19 @@ def oracle_sample(fmt, n, k, batch, ms, grouped, ci, seconds: float):
                                      f"{total:.2f} s")
 
 
+def oracle_sample_one_core(workload: str, seconds: float):
+    """oracle_sample on one host thread (a child process with OMP_NUM_THREADS=1)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    code = ("import json, bench; fmt, n, k, batch, ms, g, ci = bench.WORKLOADS[%r]; "
+            "print(json.dumps(bench.oracle_sample(fmt, n, k, batch, ms, g, ci, %r)))" % (workload, seconds))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=int(20 * seconds) + 300)
+    if r.returncode != 0:
+        return None
+    v, cores, desc = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+
 def run_reference(args):
     fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload]
     per_step = max(0.2, 60.0 / max(1, args.steps + args.warmup))
@@ -509,6 +540,7 @@ def main():
             v, cores, desc = oracle_sample(fmt, n, k, batch, ms, grouped, ci, args.cpu_seconds)
             res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                    "sample": desc}
+            res["cpu_baseline_1core"] = oracle_sample_one_core(args.workload, min(4.0, args.cpu_seconds))
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch
