@@ -13,9 +13,10 @@
  *
  * Row exactness (module doc "Row exactness"): output row j is bitwise
  * identical whether it is computed alone (m = 1) or as one row of any
- * m <= 8, on every run, as long as the split factor is the same.  The split
- * factor is derived from (wtype, batch*n, k) alone (rem_split_factor);
- * rows_per_cta only packs rows and never changes bits.
+ * m <= 8, on every run, as long as the split factor and the engine are the
+ * same.  Both are derived from (wtype, batch*n, k) alone (rem_split_factor,
+ * rem_engine_of); rows_per_cta and the lane layout only pack rows and never
+ * change bits.
  *
  * Memory and ownership.  Every pointer passed to a compute call is a CUDA
  * device pointer (or managed memory) owned by the caller; the library never
@@ -30,15 +31,21 @@
  * Errors.  Every call validates its arguments before it launches anything;
  * on an error nothing is written and a message prefixed "rem_matvec:" (or the
  * call's name) is available from rem_last_error() on the calling thread.
+ * A kernel never waits without bound: a wait that runs out (the schedule's
+ * wait_ns, 10 s by default) makes the launch write NaN for the outputs it
+ * could not finish and records the event in a per-device status word that
+ * rem_device_status() reads.  The library reads no environment variables.
  *
- * Environment.  REM_LOG_PLAN (any value, read once) prints each launch's
- * schedule to stderr.  REM_LAYOUT=0, 1, 2 or 3 (read at every launch) pins
- * the lane layout of the mat-vec kernels: one weight row per lane, two rows
- * per lane, two lane groups of two rows each sharing the input rows, or two
- * lane groups of four rows each; a call whose m has no kernel of that layout
- * (2: m < 2; 3: m other than 6 or 8, or weights other than F16 / BF16;
- * Q6_K has layout 0 only) returns REM_ELAUNCH.  The layout never changes the results' bits; the
- * pin exists to test exactly that.
+ * Engines.  Two kernels compute the product, and the engine is part of the
+ * arithmetic, like the split factor: rows are bitwise comparable between
+ * calls with the same engine and split.  By default the engine follows from
+ * (wtype, batch*n, k) alone (rem_engine_of).
+ *   REM_ENGINE_SIMT  lanes over rows on the FP32 pipe: every weight type
+ *   REM_ENGINE_TC    the tensor cores (tcgen05) for Q8_0, Q5_0 and Q6_K: per
+ *                    block, the exact codes times each input split into two
+ *                    bfloat16 parts, summed in binary32, then scaled by the
+ *                    block scale in binary32; up to 16 input rows per pass
+ *                    over the weights
  */
 #ifndef REM_H
 #define REM_H
@@ -80,6 +87,40 @@ typedef enum {
                           kernel of the weight type can launch on this device */
     REM_ECUDA = -3     /* a CUDA call failed (device, attribute or launch)     */
 } rem_status;
+
+/* Engines (see "Engines" above). */
+#define REM_ENGINE_AUTO (-1)
+#define REM_ENGINE_SIMT 0
+#define REM_ENGINE_TC 1
+
+/* Test hook of rem_schedule.test_flags: the kernel issues no copy for its
+   first pipeline stage (TMA staging only), so that stage's waits run out
+   after wait_ns and the launch reports through rem_device_status. */
+#define REM_TEST_SKIP_FIRST_STAGE 1u
+
+/*
+ * Schedule of rem_matvec_sched.  Zero / -1 fields take the default.
+ *   split         K ranges per weight row (0 = rem_split_factor); changes bits
+ *   rows_per_cta  0, 32, 64 or 128 (SIMT engine; numerically inert; the
+ *                 tensor-core engine always takes 128 rows per thread block)
+ *   layout        -1, or the SIMT engine's lane layout 0..3: one weight row per
+ *                 lane, two rows per lane, two lane groups of two rows each
+ *                 sharing the input rows, two lane groups of four rows each
+ *                 (2 needs m >= 2; 3 exists for F16 / BF16 at m = 6 and 8 only;
+ *                 Q6_K has layout 0 only; a layout without a kernel for the
+ *                 call is REM_ELAUNCH).  Numerically inert.
+ *   engine        REM_ENGINE_AUTO, REM_ENGINE_SIMT or REM_ENGINE_TC; changes bits
+ *   wait_ns       bound of every in-kernel wait in nanoseconds (0 = 10 s)
+ *   test_flags    0, or REM_TEST_SKIP_FIRST_STAGE (tests only)
+ */
+typedef struct {
+    uint32_t split;
+    uint32_t rows_per_cta;
+    int32_t layout;
+    int32_t engine;
+    uint64_t wait_ns;
+    uint32_t test_flags;
+} rem_schedule;
 
 #define REM_MAX_ROWS 8     /* ROW_EXACT_MATVEC_MAX_ROWS */
 #define REM_MAX_SPLIT 16   /* largest split factor the argument rules accept */
@@ -193,9 +234,10 @@ int rem_dequantize_affine(const void* codes, const uint16_t* scales, const uint1
  * the first of the next steps past the few-row limit (ROW_EXACT_MATVEC_MAX_ROWS
  * in row_exact_matvec.rs caps one dispatch at 8 rows; the matrix-vector regime
  * extends further, cf. qmv_batch_limit in nuvec-core 0.6.0 src/gpu.rs).  The
- * m input rows run in groups of up to REM_MAX_ROWS, one launch per group,
- * each reading W once (ceil(m/8) passes over W).  Rows are independent, so
- * row j is bitwise the row an m = 1 call with the same split produces.
+ * m input rows run in groups, one launch per group, each reading W once:
+ * groups of up to 16 rows on the tensor-core engine (ceil(m/16) passes over
+ * W), of up to REM_MAX_ROWS on the SIMT engine (ceil(m/8) passes).  Rows are independent, so row j is bitwise the
+ * row an m = 1 call with the same split and engine produces.
  *
  *   Arguments as rem_matvec_ex (strides in elements, split 0 = automatic from
  *   (wtype, batch*n, k)) without rows_per_cta.  The output rules apply to all
@@ -207,6 +249,46 @@ int rem_matvec_many(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t b
                     const float* x, uint32_t m, uint32_t x_row_stride, uint32_t x_batch_stride,
                     float* y, uint32_t y_row_stride, uint32_t y_batch_stride,
                     uint32_t split, void* stream);
+
+/*
+ * rem_matvec_sched -- the product for any m >= 1 with an explicit schedule
+ * (NULL = all defaults).  Arguments as rem_matvec_many; the input rows run in
+ * launches of up to 8 rows (SIMT engine) or 16 rows (tensor-core engine),
+ * each reading W once, all checked before the first launch.
+ * Returns REM_EINVAL for a schedule field out of range, for the tensor-core
+ * engine on a format it does not take, and for the argument errors of
+ * rem_matvec_ex.
+ */
+int rem_matvec_sched(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t batch,
+                     const float* x, uint32_t m, uint32_t x_row_stride, uint32_t x_batch_stride,
+                     float* y, uint32_t y_row_stride, uint32_t y_batch_stride,
+                     const rem_schedule* sched, void* stream);
+
+/*
+ * rem_set_thread_schedule -- schedule defaults for every later call of the
+ * calling thread (NULL: back to the library's defaults).  The fields mean
+ * what they mean in rem_schedule; an explicit split or rows_per_cta argument
+ * and the set fields of rem_matvec_sched's schedule take precedence.  Meant
+ * for tests and tuning (pinning a lane layout or an engine); it changes no
+ * other thread.  REM_EINVAL for a field out of range.  Host only.
+ */
+int rem_set_thread_schedule(const rem_schedule* sched);
+
+/*
+ * rem_engine_of -- the engine the default schedule uses for `rows`
+ * (= batch*n) weight rows of k elements: REM_ENGINE_TC for Q8_0, Q5_0 and
+ * Q6_K, REM_ENGINE_SIMT otherwise; -1 for an unknown wtype or rows == 0 or
+ * k == 0.  Host only; makes no CUDA call.
+ */
+int rem_engine_of(int wtype, uint32_t rows, uint32_t k);
+
+/*
+ * rem_device_status -- REM_OK, or REM_ECUDA (with a message) if a kernel of
+ * this library on the current device gave up on a bounded wait since the
+ * status was last cleared; `clear` != 0 clears it.  Synchronous (it reads a
+ * word of device memory); not for the hot path.
+ */
+int rem_device_status(int clear);
 
 /*
  * rem_row_bytes -- bytes of one weight row of k elements
@@ -255,7 +337,12 @@ int rem_quantize(const float* src, int wtype, uint32_t rows, uint32_t k, void* W
 /* Thread-local message of the last failing call on this thread ("" if none). */
 const char* rem_last_error(void);
 
-/* ABI version of this header (incremented on incompatible changes). */
+/* Thread-local one-line description of the last launch on this thread
+   (engine, split, layout, stages, grid, ...; "" before the first). */
+const char* rem_last_plan(void);
+
+/* ABI version of this header (incremented on incompatible changes; 2: the
+   schedule struct replaces the environment pin of the lane layout). */
 int rem_version(void);
 
 #ifdef __cplusplus

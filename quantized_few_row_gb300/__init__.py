@@ -22,7 +22,8 @@ __all__ = [
     "RemError", "build", "library_path", "load", "rem_matvec", "rem_matvec_ex", "rem_matvec_many",
     "rem_matvec_axpby", "rem_row_bytes",
     "rem_split_factor", "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version", "check",
-    "C_FUNCTIONS",
+    "C_FUNCTIONS", "Schedule", "rem_matvec_sched", "rem_engine_of", "rem_device_status", "rem_last_plan",
+    "ENGINE_AUTO", "ENGINE_SIMT", "ENGINE_TC", "TEST_SKIP_FIRST_STAGE", "rem_set_thread_schedule",
 ]
 
 F16, Q8_0, Q4_K, Q6_K, Q5_0, F32, BF16 = 0, 1, 2, 3, 4, 5, 6
@@ -36,9 +37,21 @@ def affine_wtype(bits: int, group_size: int) -> int:
     """The weight type of affine codes of `bits` bits in groups of `group_size`."""
     return WTYPES[f"a{bits}_g{group_size}"]
 REM_OK, REM_EINVAL, REM_ELAUNCH, REM_ECUDA = 0, -1, -2, -3
+ENGINE_AUTO, ENGINE_SIMT, ENGINE_TC = -1, 0, 1
+TEST_SKIP_FIRST_STAGE = 1
 C_FUNCTIONS = ("rem_matvec", "rem_matvec_ex", "rem_matvec_many", "rem_matvec_axpby", "rem_matvec_affine",
                "rem_dequantize_affine", "rem_row_bytes", "rem_split_factor",
-               "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version")
+               "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version", "rem_matvec_sched",
+               "rem_engine_of", "rem_device_status", "rem_last_plan", "rem_set_thread_schedule")
+
+
+class Schedule(ctypes.Structure):
+    """rem_schedule: split, rows_per_cta, layout, engine, wait_ns, test_flags (zero / -1 = default)."""
+    _fields_ = [("split", ctypes.c_uint32), ("rows_per_cta", ctypes.c_uint32), ("layout", ctypes.c_int32),
+                ("engine", ctypes.c_int32), ("wait_ns", ctypes.c_uint64), ("test_flags", ctypes.c_uint32)]
+
+    def __init__(self, split=0, rows_per_cta=0, layout=-1, engine=-1, wait_ns=0, test_flags=0):
+        super().__init__(split, rows_per_cta, layout, engine, wait_ns, test_flags)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "librem.so")
@@ -97,6 +110,17 @@ def load():
     lib.rem_last_error.restype = ctypes.c_char_p
     lib.rem_version.argtypes = []
     lib.rem_version.restype = i32
+    lib.rem_matvec_sched.argtypes = [vp, i32, u32, u32, u32, vp, u32, u32, u32, vp, u32, u32,
+                                     ctypes.POINTER(Schedule), vp]
+    lib.rem_matvec_sched.restype = i32
+    lib.rem_engine_of.argtypes = [i32, u32, u32]
+    lib.rem_engine_of.restype = i32
+    lib.rem_device_status.argtypes = [i32]
+    lib.rem_device_status.restype = i32
+    lib.rem_set_thread_schedule.argtypes = [ctypes.POINTER(Schedule)]
+    lib.rem_set_thread_schedule.restype = i32
+    lib.rem_last_plan.argtypes = []
+    lib.rem_last_plan.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
@@ -168,6 +192,29 @@ def rem_matvec_affine(codes, scales, biases, wtype, n: int, k: int, batch: int, 
 def rem_dequantize_affine(codes, scales, biases, wtype, rows: int, k: int, out, stream=None) -> int:
     return load().rem_dequantize_affine(_ptr(codes), _ptr(scales), _ptr(biases), _wt(wtype), rows, k, _ptr(out),
                                         _stream(stream))
+
+
+def rem_matvec_sched(W, wtype, n: int, k: int, batch: int, x, m: int, x_row_stride: int, x_batch_stride: int,
+                     y, y_row_stride: int, y_batch_stride: int, sched: Schedule | None = None, stream=None) -> int:
+    return load().rem_matvec_sched(_ptr(W), _wt(wtype), n, k, batch, _ptr(x), m, x_row_stride, x_batch_stride,
+                                   _ptr(y), y_row_stride, y_batch_stride,
+                                   ctypes.byref(sched) if sched is not None else None, _stream(stream))
+
+
+def rem_engine_of(wtype, rows: int, k: int) -> int:
+    return int(load().rem_engine_of(_wt(wtype), rows, k))
+
+
+def rem_device_status(clear: bool = False) -> int:
+    return int(load().rem_device_status(1 if clear else 0))
+
+
+def rem_set_thread_schedule(sched: Schedule | None) -> int:
+    return int(load().rem_set_thread_schedule(ctypes.byref(sched) if sched is not None else None))
+
+
+def rem_last_plan() -> str:
+    return load().rem_last_plan().decode()
 
 
 def rem_row_bytes(wtype, k: int) -> int:

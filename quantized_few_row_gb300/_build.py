@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "librem.so")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["rem_host.cu", "rem_aux.cu"] + [f"rem_mv_{f}_{p}.cu" for f in ("f16", "q8_0", "q5_0", "q4_k", "q6_k", "f32", "bf16", "a4g32", "a4g64",
+SOURCES = ["rem_host.cu", "rem_aux.cu", "rem_tc_q8_0.cu", "rem_tc_q5_0.cu", "rem_tc_q6_k.cu"] + [f"rem_mv_{f}_{p}.cu" for f in ("f16", "q8_0", "q5_0", "q4_k", "q6_k", "f32", "bf16", "a4g32", "a4g64",
                                                       "a4g128", "a8g32", "a8g64", "a8g128")
                                             for p in ("a", "b")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -73,6 +73,7 @@ struct MvArgs {
     uint32_t aligned;        // 1: TMA staging (16-byte aligned rows, encodable input map)
     uint32_t x_bm;           // input map dimension order: 1 = [k, batch, m] (token-major), 0 = [k, m, batch]
     uint32_t pdl;            // 1: launched as a programmatic dependent of the stream's previous kernel
+    uint32_t m;              // input rows of the launch (the tensor-core kernel pads them to its MP)
     // epilogue: 0 = y = acc; 1 = y = alpha*acc; 2 = y = fma(alpha, acc, beta*c)
     uint32_t epi;
     float alpha, beta;
@@ -82,7 +83,18 @@ struct MvArgs {
     const uint16_t* scales;
     const uint16_t* biases;
     uint32_t ngroups;
+    // failure reporting: a wait that runs out after wait_ns nanoseconds ORs
+    // kStatusWaitTimeout into *status and the launch writes NaN for the
+    // outputs it could not finish
+    uint32_t* status;
+    uint64_t wait_ns;
+    uint32_t test_flags;     // kTest* bits (test hooks; 0 in normal use)
 };
+
+// Bits of the device status word.
+constexpr uint32_t kStatusWaitTimeout = 1u;  // a bounded wait ran out
+// Test hooks (MvArgs::test_flags).
+constexpr uint32_t kTestSkipFirstStage = 1u;  // no copy for the first pipeline stage (TMA staging)
 
 // Lane layouts of the mat-vec kernel.  A warp always owns 32*nr0 weight
 // rows; its lanes form h groups of 32/h lanes, each lane holding nr0*h of the
@@ -118,8 +130,7 @@ REM_DECLARE_PARTS(mv_kernel_a8g128)
 // Dynamic shared memory of one CTA; the kernel lays it out the same way:
 // stages x [weight box (warps*32*NR0 rows x box) | input box (m x chunk
 // floats, padded to 128 B)], then the full and empty mbarriers of the
-// stages, then per-warp Q4_K sub-block input sums, plus slack to align the
-// base to 128 bytes.  With split > 1 two buffers of cross-range partial sums
+// stages, plus slack to align the base to 128 bytes.  With split > 1 two buffers of cross-range partial sums
 // (one per row-block parity) sit between the stages and the mbarriers.
 // `warps` counts consumer warps; the producer warp adds one more.
 inline uint32_t mv_stage_bytes(int wt, int nr0, int warps, int m) {
@@ -129,9 +140,73 @@ inline uint32_t mv_stage_bytes(int wt, int nr0, int warps, int m) {
 inline uint32_t mv_smem_bytes(int wt, int nr0, int h, int warps, int stages, int m, int split) {
     const uint32_t mh = (uint32_t)((m + h - 1) / h);
     const uint32_t parts = split > 1 ? 2u * (uint32_t)warps * nr0 * h * mh * kLanes * 4u : 0u;
-    return (uint32_t)stages * mv_stage_bytes(wt, nr0, warps, m) + parts + 16u * kMaxStages +
-           (uint32_t)(warps + 1) * 8u * kMaxRows * 4u + 128u;
+    return (uint32_t)stages * mv_stage_bytes(wt, nr0, warps, m) + parts + 16u * kMaxStages + 128u;
 }
+
+// ---------------------------------------------------------------- tensor-core engine
+
+// The tensor-core kernel rem_tc_kernel<wt, mp> (rem_tc.cuh) serves the
+// block-scaled formats Q8_0, Q5_0 and Q6_K for up to mp input rows per
+// launch, mp in {8, 16}.  A CTA owns 128 weight rows.
+constexpr int kTcRows = 128;
+__host__ __device__ constexpr bool tc_format(int wt) { return wt == kQ8_0 || wt == kQ5_0 || wt == kQ6_K; }
+__host__ __device__ constexpr int tc_max_mp(int) { return 16; }
+// K-steps (16 values) per scale block: Q6_K sub-blocks of 16, Q8_0 / Q5_0 blocks of 32.
+__host__ __device__ constexpr int tc_kpb(int wt) { return wt == kQ6_K ? 1 : 2; }
+// K-steps of a 64-value unit each consumer warp decodes: one (16 consumer
+// warps, four per lane quarter of the tile).  Every tile width takes the same
+// warp assignment, so the arithmetic of an output does not depend on it.
+__host__ __device__ constexpr int tc_kpw(int) { return 1; }
+__host__ __device__ constexpr int tc_consumer_warps(int mp) { return 4 * (4 / tc_kpw(mp)); }
+__host__ __device__ constexpr int tc_threads(int mp) { return (tc_consumer_warps(mp) + 2) * 32; }
+// K-steps one accumulator region covers (the MMAs of a scale block's
+// K-steps accumulate when one warp reads them all) and regions per unit.
+__host__ __device__ constexpr int tc_region_ksteps(int wt, int mp) {
+    return tc_kpw(mp) < tc_kpb(wt) ? tc_kpw(mp) : tc_kpb(wt);
+}
+__host__ __device__ constexpr int tc_regions(int wt, int mp) { return 4 / tc_region_ksteps(wt, mp); }
+// Units of 64 values per staged chunk: Q8_0 2 (a chunk is 4 blocks), Q5_0 and Q6_K 4.
+__host__ __device__ constexpr int tc_units_per_chunk(int wt) { return wt == kQ8_0 ? 2 : 4; }
+// Tensor-memory columns of one A/D slot: 32 columns of A (a unit as bf16
+// pairs) and one 2*mp-column accumulator per region of the unit.
+__host__ __device__ constexpr int tc_slot_cols(int wt, int mp) { return 32 + tc_regions(wt, mp) * 2 * mp; }
+// A/D slots in tensor memory: the deepest ring (4, 2 or 1 slots) that divides
+// the units of a chunk and fits the SM's 512 columns (a tensor-core CTA runs
+// alone on its SM).
+__host__ __device__ constexpr int tc_slots(int wt, int mp) {
+    return (tc_units_per_chunk(wt) % 4 == 0 && 4 * tc_slot_cols(wt, mp) <= 512) ? 4
+           : (2 * tc_slot_cols(wt, mp) <= 512) ? 2 : 1;
+}
+// Tensor-memory columns a CTA allocates: its slots, rounded up to a power of two.
+__host__ __device__ constexpr int tc_tmem_cols(int wt, int mp) {
+    return (tc_slots(wt, mp) * tc_slot_cols(wt, mp)) <= 32    ? 32
+           : (tc_slots(wt, mp) * tc_slot_cols(wt, mp)) <= 64  ? 64
+           : (tc_slots(wt, mp) * tc_slot_cols(wt, mp)) <= 128 ? 128
+           : (tc_slots(wt, mp) * tc_slot_cols(wt, mp)) <= 256 ? 256
+                                                               : 512;
+}
+// Dynamic shared memory of one tensor-core CTA: stages x [weight box (128 rows
+// x box) | input box (mp x chunk floats, padded to 128 B)], two B tiles of a
+// chunk (bf16, 2*mp rows x chunk values), two buffers of partials (the warp
+// groups past the first of each lane quarter, x 4 quarters x mp x 32 floats;
+// the cross-range partials reuse them), the scales of the regions in flight
+// (consumer warps x slots x regions per warp x 32 floats), the mbarriers and
+// the tensor-memory address, plus slack to align the base to 128 bytes.
+inline uint32_t tc_smem_bytes(int wt, int mp, int stages, int split) {
+    const uint32_t xpad = ((uint32_t)mp * chunk_values(wt) * 4u + 127u) & ~127u;
+    const uint32_t stage = (uint32_t)kTcRows * chunk_box(wt) + xpad;
+    const uint32_t btiles = 2u * (uint32_t)(chunk_values(wt) / 16) * 64u * (uint32_t)mp;
+    const uint32_t groups = (uint32_t)tc_consumer_warps(mp) / 4u;
+    const uint32_t pbuf = 2u * (groups - 1u) * 4u * (uint32_t)mp * 32u * 4u;
+    const uint32_t rpw = (uint32_t)(tc_kpw(mp) / tc_region_ksteps(wt, mp));
+    const uint32_t scales = (uint32_t)tc_consumer_warps(mp) * (uint32_t)tc_slots(wt, mp) * rpw * 32u * 4u;
+    (void)split;
+    return (uint32_t)stages * stage + btiles + pbuf + scales + 8u * (4 * kMaxStages + 1) + 16u + 128u;
+}
+const void* tc_kernel(int wt, int mp);
+const void* tc_kernel_q8_0(int mp);
+const void* tc_kernel_q5_0(int mp);
+const void* tc_kernel_q6_k(int mp);
 
 // Auxiliary kernels (dequantize / quantize), rem_aux.cu.
 int launch_dequantize(const uint8_t* w, int wt, uint64_t rows, uint32_t k, uint64_t row_bytes,

@@ -111,10 +111,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // Weight bytes a CTA prefetches into L2 ahead of its dependency wait.
 constexpr uint32_t kPrefetchBytes = 64u << 10;
 
-// Bounded wait: a phase that does not complete within the limit reports
-// failure instead of spinning forever.
-constexpr uint32_t kWaitLimit = 1u << 20;
-
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -128,19 +124,44 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: true once the phase of `parity` has completed, false when it
+// has not completed `limit_ns` nanoseconds (of the global timer) after the
+// first unsuccessful try.  The poll count is capped as well, so the wait
+// ends even if the timer were not to advance.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return false;
+}
+
+// A wait ran out: record it in the launch's status word (read back by
+// rem_device_status) before the caller writes NaN where its results go.
+__device__ __forceinline__ void report_timeout(uint32_t* status, uint32_t what) {
+    if (status) atomicOr(status, what);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
@@ -474,6 +495,28 @@ __device__ __forceinline__ void chain(float2 (&c)[NR0][M], const float* xu, Gen&
     });
 }
 
+// The same walk over groups of 4 values, accumulating straight into acc
+// (acc = fma2(w01, x[4Q..4Q+1], acc), acc = fma2(w23, x[4Q+2..4Q+3], acc)):
+// for weights whose values gen() already dequantizes element by element.
+template <int M, int NR0, int NG, int XS, typename Gen>
+__device__ __forceinline__ void chain_acc(float2 (&acc)[NR0][M], const float* xu, Gen&& gen) {
+    static_for<0, NG>([&](auto qc) {
+        constexpr int Q = decltype(qc)::value;
+        float2 w01[NR0], w23[NR0];
+#pragma unroll
+        for (int i = 0; i < NR0; ++i) gen(qc, i, w01[i], w23[i]);
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+            const float4 xv = ldx4(xu + j * XS + 4 * Q);
+#pragma unroll
+            for (int i = 0; i < NR0; ++i) {
+                acc[i][j] = fma2(w01[i], make_float2(xv.x, xv.y), acc[i][j]);
+                acc[i][j] = fma2(w23[i], make_float2(xv.z, xv.w), acc[i][j]);
+            }
+        }
+    });
+}
+
 // F16 chunk of 72 values (a zero-filled tail past k adds exact zeros).
 template <int M, int NR0>
 __device__ __forceinline__ void chunk_f16(const uint8_t* const (&rows)[NR0], const float* xc,
@@ -588,14 +631,18 @@ __device__ __forceinline__ void chunk_blocks32(const uint8_t* const (&rows)[NR0]
     });
 }
 
-// Q4_K super-block.  xs[u*XSS + j] = sum of the 32 inputs of sub-block u for
-// the lane's input row j (computed once per chunk for the warp, see
-// xsum_q4_k; XSS is the launch's input row count).
+// Q4_K super-block.  Every weight is dequantized on its own, as the format
+// defines it: w = fl(fl(d*sc)*q) - fl(dmin*mn).  d*sc (a binary16 times a
+// 6-bit integer) and d*sc*q (times a 4-bit code) are exact in binary32, so
+// the definition is one rounding of a*q - b, which is fma(a, q, -b) bit for
+// bit.  Then acc += w*x.  (Folding the min into a sum of the inputs, a*sum(q*x)
+// - b*sum(x), would round the two large terms separately and lose the
+// accuracy of a weight that is their small difference.)
 // Sub-block scales and mins: s < 4 from bytes s of scales[0..3] / [4..7];
 // s >= 4 joins the low (high) nibble of scales[s+4] with the top two bits of
 // scales[s-4] (scales[s]) -- one select per word.
-template <int M, int NR0, int XSS>
-__device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], const float* xc, const float* xs,
+template <int M, int NR0>
+__device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], const float* xc,
                                            float2 (&acc)[NR0][M]) {
     float d[NR0], dmin[NR0];
     uint32_t scw[NR0][2], mnw[NR0][2];
@@ -614,27 +661,25 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* const (&rows)[NR0], co
         static_for<0, 2>([&](auto hc) {
             constexpr int H = decltype(hc)::value;
             constexpr int u = 2 * cq + H;
-            float sc[NR0], mnv[NR0];
+            float2 a2[NR0], nb2[NR0];
 #pragma unroll
             for (int i = 0; i < NR0; ++i) {
-                sc[i] = __fmul_rn(d[i], ubyte_f<u & 3>(scw[i][u >> 2], 0x3Fu));
-                mnv[i] = __fmul_rn(dmin[i], ubyte_f<u & 3>(mnw[i][u >> 2], 0x3Fu));
+                const float sc = __fmul_rn(d[i], ubyte_f<u & 3>(scw[i][u >> 2], 0x3Fu));
+                const float mn = __fmul_rn(dmin[i], ubyte_f<u & 3>(mnw[i][u >> 2], 0x3Fu));
+                a2[i] = make_float2(sc, sc);
+                nb2[i] = make_float2(-mn, -mn);
             }
-            float2 c[NR0][M];
             // qs words 4t..4t+3 of the pair are read as one 16-byte line when
             // the chain first needs them (4-byte reads at the 144-byte row
             // stride would hit 8 banks from 32 lanes)
             uint4 qv[NR0];
-            chain<M, NR0, 8, 256>(c, xc + 32 * u, [&](auto qc, int i, float2& w01, float2& w23) {
+            chain_acc<M, NR0, 8, 256>(acc, xc + 32 * u, [&](auto qc, int i, float2& w01, float2& w23) {
                 constexpr int Q = decltype(qc)::value;
                 if constexpr ((Q & 3) == 0) qv[i] = lds16(rows[i] + 16 + 32 * cq + 4 * Q);
                 q4k_group<H>(word_of<Q & 3>(qv[i]), w01, w23);
+                w01 = fma2(a2[i], w01, nb2[i]);
+                w23 = fma2(a2[i], w23, nb2[i]);
             });
-            apply_scale<M, NR0>(acc, c, sc);
-#pragma unroll
-            for (int i = 0; i < NR0; ++i)
-#pragma unroll
-                for (int j = 0; j < M; ++j) acc[i][j].x = __fmaf_rn(-mnv[i], xs[u * XSS + j], acc[i][j].x);
         });
     });
 }
@@ -666,44 +711,19 @@ __device__ __forceinline__ void affine_codes(uint32_t v, float2& w01, float2& w2
     }
 }
 
-// Input sums of the groups of one staged chunk (CV values, groups of GS), per
-// warp: lane l adds values 8l..8l+7 as ((x0+x1)+(x2+x3))+((x4+x5)+(x6+x7)),
-// then an xor butterfly over the GS/8 lanes of a group (distance 1, 2, ...).
-// The order is fixed and does not depend on M.  xs[g*M + j].
-template <int M, int CV, int GS>
-__device__ __forceinline__ void xsum_groups(const float* xc, float* xs, int lane) {
-    constexpr int LG = GS / 8;
-    const bool live = 8 * lane < CV;
-#pragma unroll
-    for (int j = 0; j < M; ++j) {
-        float s = 0.0f;
-        if (live) {
-            const float4 a = ldx4(xc + j * CV + 8 * lane);
-            const float4 b = ldx4(xc + j * CV + 8 * lane + 4);
-            s = __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w)),
-                          __fadd_rn(__fadd_rn(b.x, b.y), __fadd_rn(b.z, b.w)));
-        }
-#pragma unroll
-        for (int off = 1; off < LG; off <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, off));
-        if (live && (lane % LG) == 0) xs[(lane / LG) * M + j] = s;
-    }
-}
-
-// Affine chunk: for every group g, c = the chain of its value pairs, then
-// acc = fma2((scale, scale), c, acc) and acc.x = fma(bias, sum of the group's
-// inputs, acc.x).  Scales and biases come from global memory; rows past n
-// and groups past k (a last chunk that ends inside the row) read none, and
-// their zero scale and bias add exact zeros.  The lane holds NR0 rows (warp
-// row rl + LW*i) and M input rows starting at row mb of the launch's MA; xl
-// is its first input row.
-template <int MA, int M, int NR0, int LW, int WT>
-__device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], const float* xc, const float* xl,
-                                             float* xs, int mb, int rl, int lane, const MvArgs& a, uint32_t b,
-                                             uint32_t wrow0, uint32_t cc, float2 (&acc)[NR0][M]) {
+// Affine chunk: every weight is dequantized on its own, w = fl(fl(scale*q) +
+// bias); scale*q (a binary16 times a code of at most 8 bits) is exact in
+// binary32, so that is fma(scale, q, bias) bit for bit.  Then acc += w*x.
+// Scales and biases come from global memory; rows past n and groups past k
+// (a last chunk that ends inside the row) read none, and their zero scale
+// and bias give weights of exactly zero.  The lane holds NR0 rows (warp row
+// rl + LW*i); xl is its first input row.
+template <int M, int NR0, int LW, int WT>
+__device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], const float* xl, int rl,
+                                             const MvArgs& a, uint32_t b, uint32_t wrow0, uint32_t cc,
+                                             float2 (&acc)[NR0][M]) {
     constexpr int BITS = affine_bits(WT), GS = affine_group(WT);
     constexpr int CV = Stage<WT>::kValues, NG = CV / GS;
-    xsum_groups<MA, CV, GS>(xc, xs, lane);
-    __syncwarp();
     uint64_t base[NR0];
     bool live[NR0];
 #pragma unroll
@@ -714,48 +734,27 @@ __device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], 
     }
     static_for<0, NG>([&](auto gc) {
         constexpr int g = decltype(gc)::value;
-        float sc[NR0], bi[NR0];
+        float2 sc2[NR0], bi2[NR0];
 #pragma unroll
         for (int i = 0; i < NR0; ++i) {
             const bool on = live[i] && cc * NG + g < a.ngroups;
-            sc[i] = on ? h2f(__ldg(a.scales + base[i] + g)) : 0.0f;
-            bi[i] = on ? h2f(__ldg(a.biases + base[i] + g)) : 0.0f;
+            const float sc = on ? h2f(__ldg(a.scales + base[i] + g)) : 0.0f;
+            const float bi = on ? h2f(__ldg(a.biases + base[i] + g)) : 0.0f;
+            sc2[i] = make_float2(sc, sc);
+            bi2[i] = make_float2(bi, bi);
         }
-        float2 c[NR0][M];
         // code words are read as 16-byte lines when the chain first needs
         // them (a group's codes are a whole number of lines)
         uint4 cv[NR0];
-        chain<M, NR0, GS / 4, CV>(c, xl + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
+        chain_acc<M, NR0, GS / 4, CV>(acc, xl + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
             constexpr int Q = g * (GS / 4) + decltype(qc)::value;
             constexpr int WI = BITS == 8 ? Q : Q / 2;  // code word of values 4Q..4Q+3
             if constexpr ((WI & 3) == 0 && (BITS == 8 || (Q & 1) == 0)) cv[i] = lds16(rows[i] + 4 * WI);
             affine_codes<BITS, Q>(word_of<WI & 3>(cv[i]), w01, w23);
+            w01 = fma2(sc2[i], w01, bi2[i]);
+            w23 = fma2(sc2[i], w23, bi2[i]);
         });
-        apply_scale<M, NR0>(acc, c, sc);
-#pragma unroll
-        for (int i = 0; i < NR0; ++i)
-#pragma unroll
-            for (int j = 0; j < M; ++j) acc[i][j].x = __fmaf_rn(bi[i], xs[g * MA + mb + j], acc[i][j].x);
     });
-}
-
-// Sub-block input sums of one Q4_K chunk, per warp: lane (u = lane/4,
-// quarter = lane%4) adds 8 inputs, then two xor-shuffles combine the quarters
-// as (q0 + q1) + (q2 + q3).  The order is fixed and does not depend on M.
-// xc is the staged [M][256] input slice.
-template <int M>
-__device__ __forceinline__ void xsum_q4_k(const float* xc, float* xs, int lane) {
-    const int u = lane >> 2, qt = lane & 3;
-#pragma unroll
-    for (int j = 0; j < M; ++j) {
-        const float4 a = ldx4(xc + j * 256 + 32 * u + 8 * qt);
-        const float4 b = ldx4(xc + j * 256 + 32 * u + 8 * qt + 4);
-        float s = __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w)),
-                            __fadd_rn(__fadd_rn(b.x, b.y), __fadd_rn(b.z, b.w)));
-        s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
-        s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
-        if (qt == 0) xs[u * M + j] = s;
-    }
 }
 
 // Q6_K super-block staged at byte o of each row: 16 sub-blocks of 16
@@ -897,8 +896,8 @@ struct LaneMap {
 // Decode + multiply one staged chunk for the lane's rows.
 template <int WT, int M, int NR0, int H>
 __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int warp, int lane, uint32_t cc,
-                                         float* xs, float2 (&acc)[NR0 * H][(M + H - 1) / H], const MvArgs& a,
-                                         uint32_t b, uint32_t wrow0) {
+                                         float2 (&acc)[NR0 * H][(M + H - 1) / H], const MvArgs& a, uint32_t b,
+                                         uint32_t wrow0) {
     using L = LaneMap<M, NR0, H>;
     constexpr int R = L::R, MH = L::MH, LW = L::LW;
     constexpr int BOX = Stage<WT>::kBox;
@@ -911,7 +910,7 @@ __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int
     const float* xc = reinterpret_cast<const float*>(st + wstage);  // [M][CV]
     const float* xl = xc + mb * CV;                                  // the lane's first input row
     if constexpr (is_affine(WT)) {
-        chunk_affine<M, MH, R, LW, WT>(rows, xc, xl, xs, mb, rl, lane, a, b, wrow0, cc, acc);
+        chunk_affine<MH, R, LW, WT>(rows, xl, rl, a, b, wrow0, cc, acc);
     } else if constexpr (WT == kF16) {
         chunk_f16<MH, R>(rows, xl, acc);
     } else if constexpr (WT == kBF16 || WT == kF32) {
@@ -922,39 +921,32 @@ __device__ __forceinline__ void mv_chunk(const uint8_t* st, uint32_t wstage, int
     } else if constexpr (WT == kQ5_0) {
         chunk_blocks32<MH, R, BlkQ5, 8, 22, 0>(rows, xl, acc);
     } else if constexpr (WT == kQ4_K) {
-        xsum_q4_k<M>(xc, xs, lane);
-        __syncwarp();
-        chunk_q4_k<MH, R, M>(rows, xl, xs + mb, acc);
+        chunk_q4_k<MH, R>(rows, xl, acc);
     } else {
         static_assert(WT != kQ6_K || H == 1, "Q6_K keeps one lane group");
         chunk_q6_k<MH, R>(rows, xl, Stage<WT>::sofs(cc), acc);
     }
 }
 
-// End of a row block for one consumer warp: the range partial
-// (acc.x + acc.y), then either the store (split 1) or the in-order sum of the
-// cluster's ranges.  With split S every rank publishes its partials in shared
-// memory, one cluster barrier makes them visible, and slot (i, j) of each
-// lane is finished by rank (i*MH + j) mod S: it loads the S partials of that
-// output (its own and the peers', through distributed shared memory), all
-// loads issued before the first add, and adds them in rank order.  Slots
-// that repeat another group's input row are neither finished nor stored.
-// Every thread of every CTA of the cluster reaches the cluster barrier once
-// per row block.
-template <int M, int NR0, int H>
-__device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0 * H][(M + H - 1) / H], bool failed,
-                                          const MvArgs& a, uint32_t b, uint32_t wrow0, bool wactive, int lane,
-                                          int warp, uint32_t s, uint32_t S, uint32_t t, float* parts,
-                                          uint32_t part_floats) {
-    using L = LaneMap<M, NR0, H>;
-    constexpr int R = L::R, MH = L::MH, LW = L::LW;
-    const int rl = L::rl(lane), mb = L::mb(lane);
-    float part[R][MH];
-#pragma unroll
-    for (int i = 0; i < R; ++i)
-#pragma unroll
-        for (int j = 0; j < MH; ++j)
-            part[i][j] = failed ? __int_as_float(0x7FC00000) : __fadd_rn(acc[i][j].x, acc[i][j].y);
+// End of a row block for one consumer warp, given the lane's range partials
+// part[i][j] of output row wrow0 + rl + LW*i and input row mb + j: either the
+// store (split 1) or the in-order sum of the cluster's ranges.  With split S
+// every rank publishes its partials in shared memory, one cluster barrier
+// makes them visible, and slot (i, j) of each lane is finished by rank
+// (i*MH + j) mod S: it loads the S partials of that output (its own and the
+// peers', through distributed shared memory), all loads issued before the
+// first add, and adds them in rank order.  Slots for which owns(j) is false
+// (an input row another lane group stores, or one past the launch's m) are
+// neither finished nor stored; a warp that is no holder (its partials were
+// already added into another warp's) only takes part in the barrier.  Every
+// thread of every CTA of the cluster reaches the cluster barrier once per row
+// block.
+// parts holds two buffers (row-block parities) buf_stride floats apart.
+template <int R, int MH, int LW, typename Owns>
+__device__ __forceinline__ void finish_row_block(const float (&part)[R][MH], const MvArgs& a, uint32_t b,
+                                                 uint32_t wrow0, bool wactive, int rl, int mb, int lane, int warp,
+                                                 uint32_t s, uint32_t S, uint32_t t, float* parts,
+                                                 uint32_t buf_stride, Owns&& owns, bool holder = true) {
     // the store, with the optional epilogue alpha * acc + beta * c (each output
     // element on its own, after the fixed reduction: row exactness is kept)
     auto store = [&](int i, int j, float v) {
@@ -970,27 +962,29 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0 * H][(M + H - 
         a.y[static_cast<uint64_t>(b) * a.ybs + m * a.yrs + row] = v;
     };
     if (S == 1) {
-        if (wactive) {
+        if (wactive && holder) {
 #pragma unroll
             for (int i = 0; i < R; ++i)
 #pragma unroll
                 for (int j = 0; j < MH; ++j)
-                    if (L::owns(lane, j)) store(i, j, part[i][j]);
+                    if (owns(j)) store(i, j, part[i][j]);
         }
         return;
     }
-    float* buf = parts + (t & 1u) * part_floats;
+    float* buf = parts + (t & 1u) * buf_stride;
+    if (holder) {
 #pragma unroll
-    for (int i = 0; i < R; ++i)
+        for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int j = 0; j < MH; ++j) buf[((warp * R + i) * MH + j) * 32 + lane] = part[i][j];
+            for (int j = 0; j < MH; ++j) buf[((warp * R + i) * MH + j) * 32 + lane] = part[i][j];
+    }
     cluster_sync();  // phase t: the ranges' partials of this row block are published
-    if (wactive) {
+    if (wactive && holder) {
 #pragma unroll
         for (int i = 0; i < R; ++i)
 #pragma unroll
             for (int j = 0; j < MH; ++j) {
-                if (static_cast<uint32_t>(i * MH + j) % S != s || !L::owns(lane, j)) continue;
+                if (static_cast<uint32_t>(i * MH + j) % S != s || !owns(j)) continue;
                 const float* slot = buf + ((warp * R + i) * MH + j) * 32 + lane;
                 float p[kMaxSplit];
 #pragma unroll
@@ -1003,6 +997,25 @@ __device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0 * H][(M + H - 
                 store(i, j, v);
             }
     }
+}
+
+// The lanes-over-rows kernel's finish: a range's partial is acc.x + acc.y
+// (NaN for every output when a wait ran out), then finish_row_block.
+template <int M, int NR0, int H>
+__device__ __forceinline__ void mv_finish(const float2 (&acc)[NR0 * H][(M + H - 1) / H], bool failed,
+                                          const MvArgs& a, uint32_t b, uint32_t wrow0, bool wactive, int lane,
+                                          int warp, uint32_t s, uint32_t S, uint32_t t, float* parts,
+                                          uint32_t part_floats) {
+    using L = LaneMap<M, NR0, H>;
+    constexpr int R = L::R, MH = L::MH, LW = L::LW;
+    float part[R][MH];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int j = 0; j < MH; ++j)
+            part[i][j] = failed ? __int_as_float(0x7FC00000) : __fadd_rn(acc[i][j].x, acc[i][j].y);
+    finish_row_block<R, MH, LW>(part, a, b, wrow0, wactive, L::rl(lane), L::mb(lane), lane, warp, s, S, t, parts,
+                                part_floats, [&](int j) { return L::owns(lane, j); });
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -1054,7 +1067,6 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     float* parts = reinterpret_cast<float*>(smem + D * stage_bytes);  // [2][G][R][MH][32] when S > 1
     uint64_t* full = reinterpret_cast<uint64_t*>(parts + (S > 1 ? 2 * part_floats : 0));
     uint64_t* empty = full + kMaxStages;
-    float* xs = reinterpret_cast<float*>(empty + kMaxStages) + warp * (8 * kMaxRows);
     const uint32_t c0 = static_cast<uint32_t>((static_cast<uint64_t>(s) * a.nchunk) / S);
     const uint32_t c1 = static_cast<uint32_t>((static_cast<uint64_t>(s + 1) * a.nchunk) / S);
     const int nck = static_cast<int>(c1 - c0);
@@ -1098,6 +1110,8 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         uint32_t i = 0;  // running chunk counter over all row blocks
         bool stop = false;
         uint32_t t = 0;
+        // test hook: issue no copy for the first stage, so that its waits run out
+        const bool skip_first = (a.test_flags & kTestSkipFirstStage) != 0u;
         for (uint32_t rb = cid; rb < nblocks; rb += ncl, ++t) {
             uint32_t b, row0;
             block_origin(rb, b, row0);
@@ -1107,10 +1121,12 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     for (int q = 0; q < nck; ++q, ++i) {
                         const int st = static_cast<int>(i % D);
                         if (i >= static_cast<uint32_t>(D) &&
-                            !mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1))) {
+                            !mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1), a.wait_ns)) {
+                            report_timeout(a.status, kStatusWaitTimeout);
                             stop = true;
                             break;
                         }
+                        if (skip_first && i == 0) continue;
                         const uint32_t cc = c0 + static_cast<uint32_t>(q);
                         uint8_t* sp = smem + st * stage_bytes;
                         mbar_expect_tx(fb + 8 * st, wstage + XBYTES);
@@ -1128,7 +1144,9 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 for (int q = 0; q < nck; ++q, ++i) {
                     const int st = static_cast<int>(i % D);
                     if (i >= static_cast<uint32_t>(D) &&
-                        !__all_sync(0xFFFFFFFFu, mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1)))) {
+                        !__all_sync(0xFFFFFFFFu,
+                                    mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1), a.wait_ns))) {
+                        if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
                         stop = true;
                         break;
                     }
@@ -1150,7 +1168,8 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         if (a.aligned && lane == 0) {
             const uint32_t issued = i;
             for (uint32_t r = issued > static_cast<uint32_t>(D) ? issued - D : 0u; r < issued; ++r)
-                (void)mbar_wait(fb + 8 * (r % D), static_cast<uint32_t>((r / D) & 1));
+                if (!(skip_first && r == 0))
+                    (void)mbar_wait(fb + 8 * (r % D), static_cast<uint32_t>((r / D) & 1), a.wait_ns);
         }
         __syncwarp();
         if (S > 1) cluster_sync();
@@ -1172,12 +1191,14 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         for (int q = 0; q < nck; ++q, ++i) {
             const int st = static_cast<int>(i % D);
             if (!failed &&
-                !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, static_cast<uint32_t>((i / D) & 1))))
+                !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, static_cast<uint32_t>((i / D) & 1), a.wait_ns))) {
                 failed = true;
+                if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
+            }
             if (failed) continue;  // keep walking so every barrier below is still reached
             if (wactive)
                 mv_chunk<WT, M, NR0, H>(smem + st * stage_bytes, wstage, warp, lane, c0 + static_cast<uint32_t>(q),
-                                        xs, acc, a, b, wrow0);
+                                        acc, a, b, wrow0);
             __syncwarp();
             if (lane == 0) mbar_arrive(eb + 8 * st);
         }

@@ -1,0 +1,806 @@
+// rem_tc.cuh -- the row-exact few-row mat-vec on the tensor cores (tcgen05),
+// for the block-scaled weights Q8_0, Q5_0 and Q6_K.
+//
+// y[b, j, i] = sum_k W[b*n + i, k] * x[b, j, k]
+// (mlx-native 0.18.0 src/ops/row_exact_matvec.rs, module doc).  For these
+// formats every weight is w = a_u * (q - offset) with one scale a_u per block
+// u (Q8_0 and Q5_0: d of a 32-value block; Q6_K: d * sc of a 16-value
+// sub-block), so
+//     y = sum_u a_u * sum_{k in u} (q_k - offset) * x_k.
+// The integer codes q - offset are exact in bfloat16, and each input value is
+// split into bfloat16 parts x = x_hi + x_lo + r with x_hi the upper half of
+// its binary32 bits and x_lo = bf16_rn(x - x_hi), so |r| <= 2^-16 |x|.  One
+// tcgen05.mma (M = 128 weight rows, K = 16 values, N = 2*MP columns: the MP
+// x_hi rows of the inputs, then the MP x_lo rows) gives, per block, the exact
+// products (q - offset)*x_hi and (q - offset)*x_lo summed in binary32 in
+// tensor memory; the consumer warps then form c = D_hi + D_lo and
+// acc = fma(a_u, c, acc) per output, in block order.  The error against the
+// exact sum is below 2^-15 * sum |w*x| plus the binary32 rounding of the
+// sums, well inside the required 1e-4 * sum |w*x|.
+//
+// Row exactness.  Output (i, j) depends only on weight row i (lane i of the
+// tile), the bits of input row j (column j and MP + j of every B tile), and
+// the fixed order of blocks and K ranges; the tensor core computes each
+// output column on its own, so neither m (the launch pads its inputs to MP
+// rows with zeros) nor anything else of the launch changes it.
+//
+// Work mapping.  A CTA owns a tile of 128 consecutive weight rows (lane l of
+// consumer warp w holds row 32w + l = TMEM lane 32w + l) and one K range
+// (`split` CTAs of a cluster share a tile, as in the lanes-over-rows kernel).
+// Warps: 4 consumers, 1 TMA producer, 1 MMA issuer (which also owns the
+// tensor memory).  Per staged chunk of K the consumers convert the chunk's
+// inputs to the B tiles (shared memory, canonical K-major layout without
+// swizzle), then per unit of 64 values they decode their rows' codes into 32
+// columns of bf16 pairs and store them to the unit's A slot in tensor memory;
+// the MMA warp issues the unit's 4 MMAs into the slot's D columns and commits
+// to the slot's mbarrier; the consumers read D back and scale it.  NS slots
+// of A and D rotate, so decoding the next units overlaps the MMAs.
+#pragma once
+#include "rem_mv.cuh"
+
+namespace rem {
+namespace dev {
+
+// ---------------------------------------------------------------- tcgen05
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Instruction descriptor of kind::f16: D f32, A and B bf16, both K-major,
+// M = 128, N = n.
+__host__ __device__ constexpr uint32_t tc_idesc(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (8u << 24);
+}
+
+// Shared-memory descriptor of a K-major tile without swizzle: core matrices of
+// 8 rows x 16 bytes, the two core matrices of a K step 128 bytes apart (LBO),
+// consecutive groups of 8 rows 256 bytes apart (SBO).
+__device__ __forceinline__ uint64_t tc_bdesc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128u >> 4) << 16) |
+           (static_cast<uint64_t>(256u >> 4) << 32) | (1ull << 46);
+}
+
+// D[128 x N] (+)= A[128 x 16] (tensor memory) * B[16 x N] (shared memory).
+__device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// The mbarrier receives one arrival when every MMA this thread issued so far
+// has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// N consecutive 32-bit columns of the warp's 32 lanes (N = 16, 32, 64).
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 16) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+            "%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr)
+            : "memory");
+    } else {
+        static_assert(N % 32 == 0, "16, 32 or 64 columns");
+#pragma unroll
+        for (int h = 0; h < N / 32; ++h) {
+            uint32_t* q = r + 32 * h;
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+                "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]),
+                  "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]),
+                  "=r"(q[15]), "=r"(q[16]), "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]),
+                  "=r"(q[22]), "=r"(q[23]), "=r"(q[24]), "=r"(q[25]), "=r"(q[26]), "=r"(q[27]), "=r"(q[28]),
+                  "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
+                : "r"(taddr + 32u * h)
+                : "memory");
+        }
+    }
+}
+
+// ---------------------------------------------------------------- bfloat16 pairs
+
+// a - b on two bfloat16 lanes (exact here: the results are small integers).
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// bfloat16 pair (lo in bits 0..15, hi in bits 16..31), each rounded to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// Bytes 0 and 2 (pair 0) and bytes 1 and 3 (pair 1) of v, masked to `mask`
+// (at most 7 bits), as bfloat16 pairs 128 + code, then minus `off2` (the
+// pair 128 + offset): exact code - offset.
+__device__ __forceinline__ void codes_bf16(uint32_t v, uint32_t mask, uint32_t off2, uint32_t& p0, uint32_t& p1) {
+    p0 = bf16x2_sub(lop_and_or(v, mask, 0x43004300u), off2);
+    p1 = bf16x2_sub(lop_and_or(v >> 8, mask, 0x43004300u), off2);
+}
+
+// N little-endian words starting at byte POS (even) of a 16-byte aligned
+// staged row, read as whole 16-byte lines.
+template <int POS, int N>
+__device__ __forceinline__ void row_words(const uint8_t* row, uint32_t (&w)[N]) {
+    constexpr int L0 = POS / 16;
+    constexpr int LAST = (POS % 4 == 0) ? POS + 4 * N - 1 : POS + 4 * N + 1;  // last byte read
+    constexpr int NL = LAST / 16 - L0 + 1;
+    uint32_t P[4 * NL];
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+        const uint4 v = lds16(row + 16 * (L0 + l));
+        P[4 * l] = v.x; P[4 * l + 1] = v.y; P[4 * l + 2] = v.z; P[4 * l + 3] = v.w;
+    }
+    constexpr int B0 = POS - 16 * L0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        if constexpr (B0 % 4 == 0) w[i] = P[B0 / 4 + i];
+        else w[i] = __byte_perm(P[B0 / 4 + i], P[B0 / 4 + i + 1], 0x5432);
+    }
+}
+
+// ---------------------------------------------------------------- formats
+
+// Per format: kUPC units of 64 values (4 K-steps of 16) per staged chunk, the
+// permutation of the 16 values of a K-step in A's columns (kPerm: 0 = natural
+// order, 1 = values 4g, 4g+2, 4g+1, 4g+3 for each group g of 4: the pairs a
+// byte-parallel decode produces), and decode<KPW>(row, o, u, s0, a, scale):
+// K-steps s0 .. s0+KPW-1 of unit u of a chunk staged at byte o of the row ->
+// 8*KPW columns of bf16 pairs (K-step s0 + s in columns 8s..8s+7) and the
+// scales of its accumulator regions (one per K-step, or one per scale block
+// when a warp decodes all of a block's K-steps).  Every decode reads its
+// words with 16-byte loads at compile-time positions, so the few (o, block)
+// combinations of a format are separate bodies; the rest is runtime
+// arithmetic.
+template <int WT> struct TcFmt;
+
+// Q8_0: a chunk is 4 blocks (d f16 | 32 int8), 128 values at byte o = 0 or 8
+// of the staged window; unit u is blocks 2u, 2u+1, K-step s0 of it the codes
+// 16(s0%2) .. 16(s0%2)+15 of block 2u + s0/2.
+template <> struct TcFmt<kQ8_0> {
+    static constexpr int kUPC = 2, kPerm = 0;
+    // NW code words of block B (at byte P of the row) from word W0 of its codes
+    template <int P, int W0, int NW>
+    __device__ __forceinline__ static void codes(const uint8_t* row, uint32_t* a, float& scale) {
+        uint32_t dw[1], q[NW + 1];
+        row_words<P, 1>(row, dw);
+        row_words<P + 4 * W0, NW + 1>(row, q);           // the words straddle: codes follow d (2 bytes)
+        scale = h2f(dw[0]);
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const uint32_t v = __byte_perm(q[i], q[i + 1], 0x5432);
+            const float2 w01 = bytes01_s(v), w23 = bytes01_s(v >> 16);
+            a[2 * i] = bf16x2_rn(w01.x, w01.y);
+            a[2 * i + 1] = bf16x2_rn(w23.x, w23.y);
+        }
+    }
+    template <int KPW>
+    __device__ __forceinline__ static void decode(const uint8_t* row, int o, int u, int s0, uint32_t (&a)[8 * KPW],
+                                                  float (&scale)[1]) {
+        // KPW 1: (o, block, half) -> 16 bodies; KPW 2: (o, block) -> 8
+        const int sel = KPW == 1 ? (o ? 8 : 0) + 2 * (2 * u + (s0 >> 1)) + (s0 & 1) : (o ? 4 : 0) + 2 * u + (s0 >> 1);
+#define REM_Q8_CASE(I, P, W0) case I: codes<P, W0, 4 * KPW>(row, a, scale[0]); break;
+        if constexpr (KPW == 1) {
+            switch (sel) {
+            REM_Q8_CASE(0, 0, 0) REM_Q8_CASE(1, 0, 4) REM_Q8_CASE(2, 34, 0) REM_Q8_CASE(3, 34, 4)
+            REM_Q8_CASE(4, 68, 0) REM_Q8_CASE(5, 68, 4) REM_Q8_CASE(6, 102, 0) REM_Q8_CASE(7, 102, 4)
+            REM_Q8_CASE(8, 8, 0) REM_Q8_CASE(9, 8, 4) REM_Q8_CASE(10, 42, 0) REM_Q8_CASE(11, 42, 4)
+            REM_Q8_CASE(12, 76, 0) REM_Q8_CASE(13, 76, 4) REM_Q8_CASE(14, 110, 0) default: codes<110, 4, 4>(row, a, scale[0]); break;
+            }
+        } else {
+            switch (sel) {
+            REM_Q8_CASE(0, 0, 0) REM_Q8_CASE(1, 34, 0) REM_Q8_CASE(2, 68, 0) REM_Q8_CASE(3, 102, 0)
+            REM_Q8_CASE(4, 8, 0) REM_Q8_CASE(5, 42, 0) REM_Q8_CASE(6, 76, 0) default: codes<110, 0, 8>(row, a, scale[0]); break;
+            }
+        }
+#undef REM_Q8_CASE
+    }
+};
+
+// Q5_0: a chunk is 8 blocks (d f16 | qh u32 | 16 nibble bytes), 256 values
+// at byte 0 of the staged row; unit u is blocks 2u, 2u+1, K-step s0 of it the
+// low (s0 even: values 0..15) or high (s0 odd: values 16..31) nibbles of
+// block 2u + s0/2; bit 4 of value e is bit e of qh.
+template <> struct TcFmt<kQ5_0> {
+    static constexpr int kUPC = 4, kPerm = 1;
+    template <int P, int KH0, int NK>
+    __device__ __forceinline__ static void block(const uint8_t* row, uint32_t* a, float& scale) {
+        uint32_t q[6];
+        row_words<P, 6>(row, q);    // d | qh | qs (22 bytes, plus 2)
+        scale = h2f(q[0]);
+        const uint32_t qh = __byte_perm(q[0], q[1], 0x5432);
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+            constexpr int dummy = 0;
+            (void)dummy;
+            const int kh = KH0 + kk;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t qs = __byte_perm(q[1 + i], q[2 + i], 0x5432);  // bytes 4i..4i+3 of qs
+                const uint32_t nib = kh ? (qs >> 4) : qs;
+                const uint32_t v = lop_and_or(nib, 0x0F0F0F0Fu, spread4((qh >> (16 * kh + 4 * i)) & 0xFu));
+                codes_bf16(v, 0x001F001Fu, 0x43104310u, a[8 * kk + 2 * i], a[8 * kk + 2 * i + 1]);
+            }
+        }
+    }
+    template <int KPW>
+    __device__ __forceinline__ static void decode(const uint8_t* row, int, int u, int s0, uint32_t (&a)[8 * KPW],
+                                                  float (&scale)[1]) {
+        const int blk = 2 * u + (s0 >> 1);
+#define REM_Q5_CASE(B) \
+        case B: if constexpr (KPW == 1) { if (s0 & 1) block<22 * B, 1, 1>(row, a, scale[0]); else block<22 * B, 0, 1>(row, a, scale[0]); } \
+                else block<22 * B, 0, 2>(row, a, scale[0]); break;
+        switch (blk) {
+            REM_Q5_CASE(0) REM_Q5_CASE(1) REM_Q5_CASE(2) REM_Q5_CASE(3) REM_Q5_CASE(4) REM_Q5_CASE(5) REM_Q5_CASE(6)
+            default: if constexpr (KPW == 1) { if (s0 & 1) block<154, 1, 1>(row, a, scale[0]); else block<154, 0, 1>(row, a, scale[0]); }
+                     else block<154, 0, 2>(row, a, scale[0]);
+                     break;
+        }
+#undef REM_Q5_CASE
+    }
+};
+
+// Q6_K: a chunk is one super-block (ql u8[128] | qh u8[64] | sc int8[16] | d
+// f16) at byte o (even, < 16) of the staged window; its K-steps are the 16
+// sub-blocks in order, each one scale block.  Sub-block s = 8h + 2t + g holds
+// values 128h + 32t + 16g + l' (l' < 16): low bits from ql[64h + 32(t&1) +
+// 16g + l'] (the low nibble for t < 2, the high one for t >= 2), high bits
+// 2t, 2t+1 of qh[32h + 16g + l'], scale d * sc[s].  Unit u holds sub-blocks
+// 4u..4u+3 (h = u/2, t = 2(u%2) + s0/2 for its K-step s0): a warp's K-steps
+// s0 .. s0+KPW-1 read ql bytes 64h + 16 s0 on and qh bytes 32h + 16(s0%2) on,
+// both at 16-byte aligned row offsets.
+template <> struct TcFmt<kQ6_K> {
+    static constexpr int kUPC = 4, kPerm = 1;
+    template <int O, int KPW>
+    __device__ __forceinline__ static void body(const uint8_t* row, int u, int s0, uint32_t (&a)[8 * KPW],
+                                                float (&scale)[KPW]) {
+        const int h = u >> 1, odd = u & 1, t2 = s0 >> 1;      // t = 2*odd + t2
+        uint32_t ql[4 * KPW], qh[4 * KPW], sc4[4], dw[1];
+        row_words<O, 4 * KPW>(row + 64 * h + 16 * s0, ql);
+        row_words<O + 128, 4 * KPW>(row + 32 * h + 16 * (s0 & 1), qh);
+        row_words<O + 192, 4>(row, sc4);
+        row_words<O + 208, 1>(row, dw);
+        const float d = h2f(dw[0]);
+        const uint32_t scw = (u == 0 ? sc4[0] : u == 1 ? sc4[1] : u == 2 ? sc4[2] : sc4[3]) >> (8 * s0);
+#pragma unroll
+        for (int k = 0; k < KPW; ++k) scale[k] = __fmul_rn(d, k == 0 ? sbyte_f<0>(scw) : sbyte_f<1>(scw));
+        // high bits 2t, 2t+1 of each qh byte -> bits 4, 5: t < 2 shifts left by 4 - 2t, t >= 2 right by 2t - 4
+        if (odd) {
+            const int r = 2 * t2;
+#pragma unroll
+            for (int i = 0; i < 4 * KPW; ++i)
+                codes_bf16(lop_sel(ql[i] >> 4, qh[i] >> r, 0x0F0F0F0Fu), 0x003F003Fu, 0x43204320u, a[2 * i], a[2 * i + 1]);
+        } else {
+            const int l = 4 - 2 * t2;
+#pragma unroll
+            for (int i = 0; i < 4 * KPW; ++i)
+                codes_bf16(lop_sel(ql[i], qh[i] << l, 0x0F0F0F0Fu), 0x003F003Fu, 0x43204320u, a[2 * i], a[2 * i + 1]);
+        }
+    }
+    template <int KPW>
+    __device__ __forceinline__ static void decode(const uint8_t* row, int o, int u, int s0, uint32_t (&a)[8 * KPW],
+                                                  float (&scale)[KPW]) {
+        switch (o) {
+        case 0: body<0, KPW>(row, u, s0, a, scale); break;
+        case 2: body<2, KPW>(row, u, s0, a, scale); break;
+        case 4: body<4, KPW>(row, u, s0, a, scale); break;
+        case 6: body<6, KPW>(row, u, s0, a, scale); break;
+        case 8: body<8, KPW>(row, u, s0, a, scale); break;
+        case 10: body<10, KPW>(row, u, s0, a, scale); break;
+        case 12: body<12, KPW>(row, u, s0, a, scale); break;
+        default: body<14, KPW>(row, u, s0, a, scale); break;
+        }
+    }
+};
+
+// ---------------------------------------------------------------- the kernel
+
+// Geometry shared by the kernel and the host (rem_internal.h mirrors it).
+template <int WT, int MP>
+struct TcGeom {
+    using F = TcFmt<WT>;
+    static constexpr int CV = Stage<WT>::kValues;           // values per chunk
+    static constexpr int BOX = Stage<WT>::kBox;             // staged bytes per row
+    static constexpr int NCOL = 2 * MP;                     // MMA N: x_hi rows, then x_lo rows
+    static constexpr int KSTEPS = CV / 16;                  // K-steps per chunk
+    static constexpr int BKSTEP = 32 * NCOL;                // B bytes per K-step (NCOL rows x 32 bytes)
+    static constexpr int BCHUNK = KSTEPS * BKSTEP;          // B bytes per chunk
+    static constexpr int KPW = tc_kpw(MP);                  // K-steps of a unit per consumer warp
+    static constexpr int CW = tc_consumer_warps(MP);        // consumer warps
+    static constexpr int GROUPS = CW / 4;                   // warps per lane quarter
+    static constexpr int RK = tc_region_ksteps(WT, MP);     // K-steps per accumulator region
+    static constexpr int RPW = KPW / RK;                    // regions per warp
+    static constexpr int NS = tc_slots(WT, MP);             // A/D slots
+    static constexpr int ACOLS = 32;                        // A columns per slot (4 K-steps)
+    static constexpr int DCOLS = tc_regions(WT, MP) * NCOL; // D columns per slot
+    static constexpr int TCOLS = tc_tmem_cols(WT, MP);      // tensor memory allocated
+    static constexpr int THREADS = tc_threads(MP);
+    static_assert(F::kUPC == tc_units_per_chunk(WT), "units per chunk");
+    static_assert(F::kUPC % NS == 0, "units per chunk must be a multiple of the slots");
+    static_assert(NS * (ACOLS + DCOLS) <= TCOLS, "slots exceed the tensor memory");
+};
+
+// Consumer-side conversion of one chunk's inputs ([m][CV] binary32 at xs) into
+// the B tiles at bt: K-step s, logical value v (A column order) of input row
+// j -> x_hi at tile row j, x_lo at tile row MP + j.  Work item = one 16-byte
+// row of a core matrix (8 logical values of one input row): items of input
+// row j are 32*j .. 32*j + 2*KSTEPS - 1, spread over the consumer warps.
+// Rows m..MP-1 stay zero.
+template <int WT, int MP>
+__device__ __forceinline__ void tc_convert_x(const float* xs, uint8_t* bt, uint32_t m, int tid) {
+    using G = TcGeom<WT, MP>;
+    constexpr int PER = 2 * G::KSTEPS;                      // items per input row (32 or 16)
+    constexpr int NT = G::CW * kLanes;
+    // thread t takes items it = t', t' + NT, ... of the interleaved order t' = (t % CW) * 32 + t / CW
+    const int tt = (tid % G::CW) * kLanes + tid / G::CW;
+    for (int it = tt; it < static_cast<int>(m) * 32; it += NT) {
+        const int j = it >> 5, r = it & 31;
+        if (r >= PER) continue;
+        const int s = r >> 1, kh = r & 1;
+        const float* src = xs + j * G::CV + 16 * s + 8 * kh;
+        const float4 u = ldx4(src), v = ldx4(src + 4);
+        float e[8];
+        if constexpr (TcFmt<WT>::kPerm == 1) {
+            e[0] = u.x; e[1] = u.z; e[2] = u.y; e[3] = u.w; e[4] = v.x; e[5] = v.z; e[6] = v.y; e[7] = v.w;
+        } else {
+            e[0] = u.x; e[1] = u.y; e[2] = u.z; e[3] = u.w; e[4] = v.x; e[5] = v.y; e[6] = v.z; e[7] = v.w;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t b0 = __float_as_uint(e[2 * p]), b1 = __float_as_uint(e[2 * p + 1]);
+            hi[p] = __byte_perm(b0, b1, 0x7632);     // upper halves: x_hi of both values
+            // x_lo = bf16_rn(x - x_hi); zero where x is not finite (x_hi keeps inf / NaN)
+            const float r0 = (b0 & 0x7F800000u) == 0x7F800000u ? 0.0f : __fsub_rn(e[2 * p], __uint_as_float(b0 & 0xFFFF0000u));
+            const float r1 = (b1 & 0x7F800000u) == 0x7F800000u ? 0.0f : __fsub_rn(e[2 * p + 1], __uint_as_float(b1 & 0xFFFF0000u));
+            lo[p] = bf16x2_rn(r0, r1);
+        }
+        uint8_t* dst = bt + s * G::BKSTEP + (j >> 3) * 256 + kh * 128 + (j & 7) * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(dst + (MP / 8) * 256) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// Plain input staging for runtime m (the TMA path needs 16-byte aligned
+// weight rows): the [m][CV] slice of chunk cc, zero past k.
+template <int CV>
+__device__ __forceinline__ void stage_x_plain_m(float* dst, const float* xb, uint32_t xrs, uint32_t m, uint32_t cc,
+                                                uint32_t k, int lane) {
+    constexpr int Q = CV / 4;
+    for (int idx = lane; idx < static_cast<int>(m) * Q; idx += 32) {
+        const int j = idx / Q, q = idx - (idx / Q) * Q;
+        const uint32_t col = cc * CV + 4u * q;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < k) v = ldg4(xb + static_cast<uint64_t>(j) * xrs + col);
+        *reinterpret_cast<float4*>(dst + j * CV + 4 * q) = v;
+    }
+}
+
+// 8*KPW columns of the warp's 32 lanes.
+template <int KPW>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[8 * KPW]) {
+    if constexpr (KPW == 1) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                     : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15, %16};" ::"r"(taddr),
+            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+            "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+            : "memory");
+    }
+}
+
+// Scaling of a warp's RPW accumulator regions whose D columns were loaded
+// into d: per region c = D_hi + D_lo for input rows 0..NJ-1 (NJ >= m; the
+// rest of acc stays zero and is never stored) and acc = fma(scale, c, acc),
+// in region order.
+template <int MP, int NCOL, int RPW, int NJ>
+__device__ __forceinline__ void tc_scale_regions(const uint32_t (&d)[RPW][NCOL], const float* sc, float (&acc)[MP]) {
+#pragma unroll
+    for (int b = 0; b < RPW; ++b)
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+            acc[j] = __fmaf_rn(sc[b * 32], __fadd_rn(__uint_as_float(d[b][j]), __uint_as_float(d[b][MP + j])), acc[j]);
+}
+template <int MP, int NCOL, int RPW>
+__device__ __forceinline__ void tc_scale(const uint32_t (&d)[RPW][NCOL], const float* sc, uint32_t m, float (&acc)[MP]) {
+    if (m <= 1) tc_scale_regions<MP, NCOL, RPW, 1>(d, sc, acc);
+    else if (m <= 2) tc_scale_regions<MP, NCOL, RPW, 2>(d, sc, acc);
+    else if (m <= 4) tc_scale_regions<MP, NCOL, RPW, 4>(d, sc, acc);
+    else if (MP == 8 || m <= 8) tc_scale_regions<MP, NCOL, RPW, (MP < 8 ? MP : 8)>(d, sc, acc);
+    else if (MP == 16 || m <= 16) tc_scale_regions<MP, NCOL, RPW, (MP < 16 ? MP : 16)>(d, sc, acc);
+    else tc_scale_regions<MP, NCOL, RPW, MP>(d, sc, acc);
+}
+
+// Persistent kernel: clusters of `split` CTAs walk the 128-row tiles; CTA
+// rank s of a cluster handles K range s of every tile.  Warps 0..CW-1 are
+// consumers: warp w holds rows 32(w%4) .. 32(w%4)+31 of the tile (its TMEM
+// lane quarter) and K-steps KPW*(w/4) .. KPW*(w/4)+KPW-1 of every unit, with
+// their accumulator regions; warp CW is the producer (TMA or plain staging of
+// weights and inputs), warp CW+1 the MMA issuer and owner of the tensor
+// memory.  The warps of one lane quarter accumulate separately; at the end of
+// a tile their partials are added in warp-group order.
+template <int WT, int MP>
+__global__ void __launch_bounds__(TcGeom<WT, MP>::THREADS, 1)
+rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
+    using G = TcGeom<WT, MP>;
+    using F = TcFmt<WT>;
+    constexpr int NS = G::NS, UPC = F::kUPC, KPW = G::KPW, RK = G::RK, RPW = G::RPW;
+    constexpr int CV = G::CV, BOX = G::BOX, ROWS = 128;
+    constexpr int CW = G::CW, PRODUCER = CW, ISSUER = CW + 1;
+    constexpr uint32_t XPAD = (MP * CV * 4 + 127u) & ~127u;
+    constexpr uint32_t WSTAGE = ROWS * BOX;
+    constexpr uint32_t STAGE = WSTAGE + XPAD;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t S = a.split;
+    const int D = static_cast<int>(a.stages);
+    const uint32_t m = a.m;
+    const uint32_t s = S > 1 ? cluster_rank() : 0u;
+    const uint32_t cid = blockIdx.x / S;
+    const uint32_t ncl = gridDim.x / S;
+    uint8_t* btiles = smem + D * STAGE;                                    // [2][BCHUNK]
+    // [2][GROUPS-1][4][MP][32] by row-block parity: the partials of warp
+    // groups 1.. of each lane quarter; with split > 1 the cross-range partials
+    // of a row block reuse its buffer's group 1 slots (a group 0 warp reads
+    // every slot of its quarter before it writes that one, and the buffer of
+    // the same parity is written again only after the next row block's
+    // cluster barrier, which every reader of the partials has passed)
+    float* pairs = reinterpret_cast<float*>(btiles + 2 * G::BCHUNK);
+    constexpr uint32_t part_floats = 4u * MP * 32u;
+    constexpr uint32_t pair_floats = (G::GROUPS - 1) * part_floats;
+    float* parts = pairs;
+    float* scl = pairs + 2 * pair_floats;                                  // [CW][NS][RPW][32] region scales
+    uint64_t* full = reinterpret_cast<uint64_t*>(scl + CW * NS * RPW * 32);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* afull = empty + kMaxStages;
+    uint64_t* dfull = afull + 4;
+    uint64_t* drain = dfull + 4;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+    const uint32_t c0 = static_cast<uint32_t>((static_cast<uint64_t>(s) * a.nchunk) / S);
+    const uint32_t c1 = static_cast<uint32_t>((static_cast<uint64_t>(s + 1) * a.nchunk) / S);
+    const int nck = static_cast<int>(c1 - c0);
+    const uint32_t nblocks = a.cpb * a.batch;
+
+    auto block_origin = [&](uint32_t rb, uint32_t& b, uint32_t& row0) {
+        b = rb / a.cpb;
+        row0 = (rb - b * a.cpb) * static_cast<uint32_t>(ROWS);
+    };
+
+    const uint32_t fb = smem_u32(full), eb = smem_u32(empty), ab = smem_u32(afull), db = smem_u32(dfull);
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < D; ++t) {
+            mbar_init(fb + 8 * t, a.aligned ? 1u : 32u);
+            mbar_init(eb + 8 * t, static_cast<uint32_t>(CW));
+        }
+        for (int t = 0; t < NS; ++t) {
+            mbar_init(ab + 8 * t, static_cast<uint32_t>(CW));
+            mbar_init(db + 8 * t, 1u);
+        }
+        mbar_init(smem_u32(drain), 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // the B tiles' rows m..MP-1 stay zero for the whole launch
+    for (int i = threadIdx.x; i < 2 * G::BCHUNK / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(btiles)[i] = make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (a.pdl && a.aligned && warp == PRODUCER && lane == 0 && cid < nblocks) {
+        uint32_t b, row0;
+        block_origin(cid, b, row0);
+        const int32_t grow = static_cast<int32_t>(static_cast<uint64_t>(b) * a.n + row0);
+        const int npf = min(nck, static_cast<int>(kPrefetchBytes / WSTAGE) + 1);
+        for (int q = 0; q < npf; ++q)
+            tma_prefetch_2d(&wmap, static_cast<int32_t>(Stage<WT>::gofs(c0 + static_cast<uint32_t>(q)) / 2), grow);
+    }
+    pdl_wait();
+    // tensor memory, once the previous kernel of the stream (which may have
+    // held some) has completed
+    if (warp == ISSUER) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "n"(G::TCOLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // the same value in every lane, and known to the compiler to be so
+    const uint32_t tmem = __shfl_sync(0xFFFFFFFFu, *tslot, 0);
+
+    if (warp == PRODUCER) {
+        // ------------------------------------------------ producer
+        pdl_launch_dependents();
+        uint32_t i = 0;
+        bool stop = false;
+        uint32_t t = 0;
+        const bool skip_first = (a.test_flags & kTestSkipFirstStage) != 0u;
+        for (uint32_t rb = cid; rb < nblocks; rb += ncl, ++t) {
+            uint32_t b, row0;
+            block_origin(rb, b, row0);
+            const uint64_t grow0 = static_cast<uint64_t>(b) * a.n + row0;
+            if (a.aligned) {
+                if (lane == 0 && !stop) {
+                    for (int q = 0; q < nck; ++q, ++i) {
+                        const int st = static_cast<int>(i % D);
+                        if (i >= static_cast<uint32_t>(D) &&
+                            !mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1), a.wait_ns)) {
+                            report_timeout(a.status, kStatusWaitTimeout);
+                            stop = true;
+                            break;
+                        }
+                        if (skip_first && i == 0) continue;
+                        const uint32_t cc = c0 + static_cast<uint32_t>(q);
+                        uint8_t* sp = smem + st * STAGE;
+                        mbar_expect_tx(fb + 8 * st, WSTAGE + m * CV * 4u);
+                        tma_load_2d(smem_u32(sp), &wmap, static_cast<int32_t>(Stage<WT>::gofs(cc) / 2),
+                                    static_cast<int32_t>(grow0), fb + 8 * st);
+                        tma_load_3d(smem_u32(sp + WSTAGE), &xmap, static_cast<int32_t>(cc * CV),
+                                    a.x_bm ? static_cast<int32_t>(b) : 0, a.x_bm ? 0 : static_cast<int32_t>(b),
+                                    fb + 8 * st);
+                    }
+                }
+            } else if (!stop) {
+                const int nrows = static_cast<int>(min(static_cast<uint32_t>(ROWS), a.n - row0));
+                const uint8_t* wrow_ptr = a.w + grow0 * a.row_bytes;
+                const float* xb = a.x + static_cast<uint64_t>(b) * a.xbs;
+                for (int q = 0; q < nck; ++q, ++i) {
+                    const int st = static_cast<int>(i % D);
+                    if (i >= static_cast<uint32_t>(D) &&
+                        !__all_sync(0xFFFFFFFFu,
+                                    mbar_wait(eb + 8 * st, static_cast<uint32_t>((i / D - 1) & 1), a.wait_ns))) {
+                        if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t cc = c0 + static_cast<uint32_t>(q);
+                    uint8_t* sp = smem + st * STAGE;
+                    stage_w_plain<WT>(sp, wrow_ptr, a.row_bytes, nrows, cc, a.k, lane);
+                    stage_x_plain_m<CV>(reinterpret_cast<float*>(sp + WSTAGE), xb, a.xrs, m, cc, a.k, lane);
+                    mbar_arrive(fb + 8 * st);
+                }
+            }
+            __syncwarp();
+            if (S > 1) {
+                if (t > 0) cluster_wait();
+                cluster_arrive();
+            }
+        }
+        if (S > 1 && t > 0) cluster_wait();
+        if (a.aligned && lane == 0) {
+            const uint32_t issued = i;
+            for (uint32_t r = issued > static_cast<uint32_t>(D) ? issued - D : 0u; r < issued; ++r)
+                if (!(skip_first && r == 0))
+                    (void)mbar_wait(fb + 8 * (r % D), static_cast<uint32_t>((r / D) & 1), a.wait_ns);
+        }
+        __syncwarp();
+        if (S > 1) cluster_sync();
+        return;
+    }
+
+    if (warp == ISSUER) {
+        // ------------------------------------------------ MMA issuer
+        // The whole warp walks the units, so every operand is warp-uniform
+        // (the descriptors are a base plus compile-time steps); lane 0 issues.
+        bool failed = false;
+        bool issued_any = false;
+        uint32_t gc = 0;  // chunks over all tiles
+        uint32_t t = 0;
+        constexpr uint32_t idesc = tc_idesc(G::NCOL);
+        const uint64_t bdesc0 = tc_bdesc(__shfl_sync(0xFFFFFFFFu, smem_u32(btiles), 0));
+        for (uint32_t rb = cid; rb < nblocks; rb += ncl, ++t) {
+            for (int q = 0; q < nck && !failed; ++q, ++gc) {
+                const uint64_t bchunk = bdesc0 + static_cast<uint64_t>(((gc & 1u) * G::BCHUNK) >> 4);
+#pragma unroll 1
+                for (int u = 0; u < UPC; ++u) {
+                    const int sl = u % NS;
+                    const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(u / NS);
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(ab + 8 * sl, use & 1u, a.wait_ns))) {
+                        if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ac = tmem + static_cast<uint32_t>(sl * G::ACOLS);
+                    const uint32_t dc = tmem + static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS);
+                    const uint64_t bu = bchunk + static_cast<uint64_t>((4 * u * G::BKSTEP) >> 4);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            tc_mma(dc + static_cast<uint32_t>((k4 / RK) * G::NCOL), ac + 8u * k4,
+                                   bu + static_cast<uint64_t>((k4 * G::BKSTEP) >> 4), idesc, (k4 % RK) != 0);
+                        tc_commit(db + 8 * sl);
+                    }
+                    __syncwarp();
+                    issued_any = true;
+                }
+            }
+            if (S > 1) {
+                if (t > 0) cluster_wait();
+                cluster_arrive();
+            }
+        }
+        if (S > 1 && t > 0) cluster_wait();
+        if (S > 1) cluster_sync();
+        // every MMA this warp issued has completed before the memory goes back
+        if (lane == 0 && issued_any) {
+            tc_commit(smem_u32(drain));
+            if (!mbar_wait(smem_u32(drain), 0u, a.wait_ns)) report_timeout(a.status, kStatusWaitTimeout);
+        }
+        __syncwarp();
+        asm volatile("bar.sync 1, %0;" ::"n"((CW + 1) * 32) : "memory");
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(G::TCOLS) : "memory");
+        return;
+    }
+
+    // ---------------------------------------------------- consumers
+    const int quarter = warp & 3, grp = warp >> 2;
+    const int s0 = grp * KPW;                                              // this warp's first K-step of a unit
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;  // this warp's TMEM lanes
+    float* myscl = scl + warp * (NS * RPW * 32) + lane;                   // [NS][RPW] scales of this lane
+    bool failed = false;
+    uint32_t i = 0;   // stages consumed
+    uint32_t gc = 0;  // chunks over all tiles
+    for (uint32_t rb = cid, t = 0; rb < nblocks; rb += ncl, ++t) {
+        uint32_t b, row0;
+        block_origin(rb, b, row0);
+        const uint32_t wrow0 = row0 + static_cast<uint32_t>(quarter * 32);
+        float acc[MP];
+#pragma unroll
+        for (int j = 0; j < MP; ++j) acc[j] = 0.0f;
+        // the slot's MMAs (use number `use`) have completed: its D is ready, its A is free
+        auto wait_d = [&](int sl, uint32_t use) {
+            if (failed) return;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(db + 8 * sl, use & 1u, a.wait_ns))) {
+                failed = true;
+                if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
+                return;
+            }
+            tc_fence_after();
+        };
+        auto load_d = [&](int sl, uint32_t (&d)[RPW][G::NCOL]) {
+            const uint32_t dc = tmem + lane_base +
+                                static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS + (s0 / RK) * G::NCOL);
+#pragma unroll
+            for (int bb = 0; bb < RPW; ++bb) tmem_ld<G::NCOL>(dc + static_cast<uint32_t>(bb * G::NCOL), d[bb]);
+        };
+        for (int q = 0; q < nck; ++q, ++i, ++gc) {
+            const int st = static_cast<int>(i % D);
+            if (!failed &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, static_cast<uint32_t>((i / D) & 1), a.wait_ns))) {
+                failed = true;
+                if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
+            }
+            if (failed) continue;
+            const uint8_t* sp = smem + st * STAGE;
+            // this chunk's inputs -> B tiles (the MMAs of the chunk two back,
+            // which read this buffer, were all observed complete: every unit
+            // of that chunk has had its epilogue)
+            tc_convert_x<WT, MP>(reinterpret_cast<const float*>(sp + WSTAGE), btiles + (gc & 1u) * G::BCHUNK, m,
+                                 static_cast<int>(threadIdx.x));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            const uint8_t* row = sp + (quarter * 32 + lane) * BOX;
+            const int o = Stage<WT>::sofs(c0 + static_cast<uint32_t>(q));
+#pragma unroll 1
+            for (int u = 0; u < UPC; ++u) {
+                const int sl = u % NS;
+                const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(u / NS);
+                const bool pending = q > 0 || u >= NS;   // slot sl holds an earlier unit of this tile
+                // up to 8 input rows the old unit's D is loaded before this
+                // unit decodes (the load's latency hides behind the decode);
+                // wider tiles load it after, to keep the registers in bounds
+                constexpr bool early = MP <= 8;
+                uint32_t d[RPW][G::NCOL];
+                if (pending) {
+                    wait_d(sl, use - 1u);
+                    if (failed) break;
+                    if constexpr (early) load_d(sl, d);
+                }
+                uint32_t av[8 * KPW];
+                float nsc[RPW];
+                F::template decode<KPW>(row, o, u, s0, av, nsc);
+                tmem_st_cols<KPW>(tmem + lane_base + static_cast<uint32_t>(sl * G::ACOLS + 8 * s0), av);
+                if (pending) {
+                    if constexpr (!early) load_d(sl, d);
+                    tmem_ld_wait();
+                    tc_scale<MP, G::NCOL, RPW>(d, myscl + sl * (RPW * 32), m, acc);
+                }
+#pragma unroll
+                for (int bb = 0; bb < RPW; ++bb) myscl[sl * (RPW * 32) + bb * 32] = nsc[bb];
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ab + 8 * sl);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(eb + 8 * st);
+        }
+        // drain: the last unit of every slot
+        if (nck > 0) {
+#pragma unroll 1
+            for (int sl = 0; sl < NS; ++sl) {
+                wait_d(sl, (gc - 1u) * (UPC / NS) + static_cast<uint32_t>((UPC - NS + sl) / NS));
+                if (failed) break;
+                uint32_t d[RPW][G::NCOL];
+                load_d(sl, d);
+                tmem_ld_wait();
+                tc_scale<MP, G::NCOL, RPW>(d, myscl + sl * (RPW * 32), m, acc);
+            }
+        }
+        // the other warp groups' partials join group 0's, in group order
+        float* pb = pairs + (t & 1u) * pair_floats;
+        if (grp > 0) {
+#pragma unroll
+            for (int j = 0; j < MP; ++j)
+                pb[((grp - 1) * 4 * MP + quarter * MP + j) * 32 + lane] = failed ? __int_as_float(0x7FC00000) : acc[j];
+        }
+        asm volatile("bar.sync 2, %0;" ::"n"(CW * 32) : "memory");
+        float part[1][MP];
+#pragma unroll
+        for (int j = 0; j < MP; ++j) {
+            float v = failed ? __int_as_float(0x7FC00000) : acc[j];
+            if (grp == 0) {
+#pragma unroll
+                for (int g = 1; g < G::GROUPS; ++g) v = __fadd_rn(v, pb[((g - 1) * 4 * MP + quarter * MP + j) * 32 + lane]);
+            }
+            part[0][j] = v;
+        }
+        finish_row_block<1, MP, 32>(part, a, b, wrow0, wrow0 < a.n, lane, 0, lane, quarter, s, S, t, parts,
+                                    pair_floats, [&](int j) { return static_cast<uint32_t>(j) < m; }, grp == 0);
+    }
+    if (S > 1) cluster_sync();
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"((CW + 1) * 32) : "memory");
+}
+
+}  // namespace dev
+}  // namespace rem
+
+// Kernel pointer of rem_tc_kernel<WT, MP>, or nullptr where MP exceeds the
+// format's limit (tc_max_mp).
+namespace rem {
+template <int WT, int MP>
+inline const void* tc_kernel_ptr() {
+    if constexpr (MP > tc_max_mp(WT)) {
+        return nullptr;
+    } else {
+        return reinterpret_cast<const void*>(&dev::rem_tc_kernel<WT, MP>);
+    }
+}
+}  // namespace rem
+
+#define REM_TC_INSTANTIATE(WT, NAME)                                    \
+    namespace rem {                                                     \
+    const void* NAME(int mp) {                                          \
+        return mp == 8 ? tc_kernel_ptr<WT, 8>() : mp == 16 ? tc_kernel_ptr<WT, 16>() : nullptr; \
+    }                                                                   \
+    }

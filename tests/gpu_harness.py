@@ -54,6 +54,21 @@ def run_matvec(w: np.ndarray, wt, n: int, k: int, batch: int, x: np.ndarray, m: 
     return out
 
 
+def run_sched(w: np.ndarray, wt, n: int, k: int, batch: int, x: np.ndarray, m: int, xrs: int, xbs: int,
+              yrs: int, ybs: int, ylen: int, sched=None, w_offset: int = 0, tail: int = 0) -> np.ndarray:
+    """y through rem_matvec_sched as a flat f32 host array of ylen + tail
+    elements; everything the call does not write (strided gaps and the
+    `tail` elements past the last output) keeps the canary."""
+    wh, wp = to_dev_bytes(w, w_offset)
+    xd = to_dev_f32(x)
+    yd = canary(ylen + tail)
+    rem.check(rem.rem_matvec_sched(wp, wt, n, k, batch, xd, m, xrs, xbs, yd, yrs, ybs, sched))
+    torch.cuda.synchronize()
+    out = yd.cpu().numpy()
+    del wh
+    return out
+
+
 def gather_y(yflat: np.ndarray, batch: int, m: int, n: int, yrs: int, ybs: int) -> np.ndarray:
     """[batch, m, n] view of a strided flat output."""
     b = np.arange(batch)[:, None, None] * ybs
@@ -79,3 +94,37 @@ def assert_close_to_oracle(y_gpu: np.ndarray, y_ref: np.ndarray, a_ref: np.ndarr
         detail = [(tuple(int(t) for t in b), float(y_gpu[tuple(b)]), float(y_ref[tuple(b)]),
                    float(a_ref[tuple(b)])) for b in bad]
         raise AssertionError(f"{what}: {int((~ok).sum())} outputs outside 1e-4*A + 1e-7, e.g. {detail}")
+
+
+def adversarial_blocks(fmt, rows, k, seed):
+    """Random bytes with finite fp16 scale fields (normal and subnormal)."""
+    rb = oracle.row_bytes(fmt, k)
+    b = _inputs().uniform_bytes(rows * rb, seed).reshape(rows, rb)
+    if fmt == "f16":
+        h = b.view(np.uint16)
+        h[(h & 0x7C00) == 0x7C00] &= 0x3FFF   # no inf / NaN
+        return b
+    if fmt == "bf16":
+        h = b.view(np.uint16)
+        h[(h & 0x7F80) == 0x7F80] &= 0xBFFF   # no inf / NaN
+        return b
+    if fmt == "f32":
+        u = b.view(np.uint32)
+        u[(u & 0x7F800000) == 0x7F800000] &= 0xBFFFFFFF
+        return b
+    g = np.random.Generator(np.random.PCG64(seed + 1))
+    bb = oracle.block_bytes(fmt)
+    nb = rb // bb
+    blocks = b.reshape(rows, nb, bb)
+    fields = {"q8_0": [0], "q5_0": [0], "q4_K": [0, 2], "q6_K": [208]}[fmt]
+    for off in fields:
+        h = g.integers(0, 0x7C00, size=(rows, nb)).astype(np.uint16)   # finite, positive
+        h |= (g.integers(0, 2, size=(rows, nb)) << 15).astype(np.uint16)
+        h[:, ::7] &= 0x03FF                                            # some subnormal scales
+        blocks[:, :, off:off + 2] = h.view(np.uint8).reshape(rows, nb, 2)
+    return b
+
+
+def _inputs():
+    from quantized_few_row_gb300 import inputs
+    return inputs

@@ -32,7 +32,7 @@ def test_header_declares_the_binding_names():
 def test_exports_every_declared_symbol(lib):
     for name in _declared():
         assert getattr(lib, name) is not None
-    assert rem.rem_version() == 1
+    assert rem.rem_version() == 2
 
 
 @pytest.mark.parametrize("wt,k,expect", [
@@ -209,3 +209,55 @@ def test_affine_types_need_the_affine_entry(lib):
     assert rem.rem_dequantize(W, rem.A8_G32, 4, 256, Y, stream=0) == rem.REM_EINVAL
     assert rem.rem_quantize(X, rem.A8_G32, 4, 256, W, stream=0) == rem.REM_EINVAL
     assert rem.rem_row_bytes(rem.A4_G32, 4096) == 2048 and rem.rem_row_bytes(rem.A8_G128, 4096) == 4096
+
+
+@pytest.mark.parametrize("wt,rows,k,expect", [
+    ("q6_K", 128256, 4096, rem.ENGINE_TC), ("q8_0", 4096, 4096, rem.ENGINE_TC), ("q5_0", 16384, 4096, rem.ENGINE_TC),
+    ("q4_K", 14336, 4096, rem.ENGINE_SIMT), ("f16", 256, 512, rem.ENGINE_SIMT), ("bf16", 64, 256, rem.ENGINE_SIMT),
+    ("f32", 64, 256, rem.ENGINE_SIMT), (rem.A4_G64, 64, 256, rem.ENGINE_SIMT),
+])
+def test_engine_from_shape(lib, wt, rows, k, expect):
+    assert rem.rem_engine_of(wt, rows, k) == expect
+    assert rem.rem_engine_of(wt, rows, k) == expect     # no state
+
+
+def test_engine_degenerate(lib):
+    assert rem.rem_engine_of(99, 64, 256) == -1
+    assert rem.rem_engine_of("q8_0", 0, 256) == -1
+    assert rem.rem_engine_of("q8_0", 64, 0) == -1
+
+
+def _sched(sched, **kw):
+    a = dict(W=W, wtype="q8_0", n=64, k=256, batch=1, x=X, m=2, x_row_stride=256, x_batch_stride=0,
+             y=Y, y_row_stride=64, y_batch_stride=0)
+    a.update(kw)
+    return rem.rem_matvec_sched(a["W"], a["wtype"], a["n"], a["k"], a["batch"], a["x"], a["m"],
+                                a["x_row_stride"], a["x_batch_stride"], a["y"], a["y_row_stride"],
+                                a["y_batch_stride"], sched, stream=0)
+
+
+@pytest.mark.parametrize("sched,kw,msg", [
+    (rem.Schedule(layout=4), {}, "layout (4)"),
+    (rem.Schedule(layout=-2), {}, "layout (-2)"),
+    (rem.Schedule(engine=2), {}, "engine (2)"),
+    (rem.Schedule(engine=rem.ENGINE_TC), dict(wtype="q4_K"), "tensor-core engine takes"),
+    (rem.Schedule(engine=rem.ENGINE_TC), dict(wtype="f16"), "tensor-core engine takes"),
+    (rem.Schedule(split=17), {}, "split (17)"),
+    (rem.Schedule(), dict(m=0), "m (0) must be >= 1"),
+    (rem.Schedule(), dict(m=20, y_row_stride=63), "overlap"),
+], ids=["layout4", "layout-2", "engine2", "tc_q4k", "tc_f16", "split", "m0", "overlap"])
+def test_schedule_rules(lib, sched, kw, msg):
+    """rem_matvec_sched refuses schedule fields out of range and the
+    tensor-core engine on a format it does not take, before any CUDA call."""
+    assert _sched(sched, **kw) == rem.REM_EINVAL
+    assert msg in rem.rem_last_error(), rem.rem_last_error()
+
+
+def test_few_row_entry_points_keep_eight_rows(lib):
+    """rem_matvec_ex and rem_matvec_axpby take at most 8 input rows on either
+    engine (the page's per-dispatch limit); more rows go through
+    rem_matvec_many or rem_matvec_sched."""
+    for wt in ("q8_0", "q6_K", "q4_K"):
+        k = 256
+        assert _ex(wtype=wt, m=9, k=k, x_row_stride=k) == rem.REM_EINVAL
+        assert "1..=8" in rem.rem_last_error(), rem.rem_last_error()

@@ -1,7 +1,9 @@
 """GPU parity at the benchmark's full sizes, called the way bench.py calls the
-library (rem_matvec, inferred strides, the automatic schedule), checked on
-sampled outputs the oracle computes row by row, plus bitwise row exactness
-between m = 1 and the larger m on those samples.
+library (rem_matvec, inferred strides, the automatic schedule): every output
+of every m against the oracle (one f64 run over all rows at the largest m;
+the oracle's row j does not depend on m), a canary past the end of y that no
+call may touch, and bitwise row exactness between m = 1 and the larger m on
+every row.
 
 Workloads (all seeded and synthetic, W ~ N(0, 0.02) quantized by the
 oracle's quantizer, x ~ N(0, 1)): F16 256x512 m=1; Q8_0 4096x4096 m=1..8;
@@ -59,16 +61,26 @@ def _weights(fmt, rows, k, seed, slab=8192):
     return w
 
 
-def _sample_rows(batch, n, count, seed):
-    g = np.random.Generator(np.random.PCG64(seed))
-    picks = set(int(i) for i in g.integers(0, batch * n, count))
-    for b in (0, batch - 1):
-        picks.update({b * n, b * n + 1, b * n + n - 1})
-    return np.array(sorted(picks), dtype=np.uint64)
+TAIL = 256   # canary floats past the last output
+
+
+def _all_rows(batch, n):
+    return np.arange(batch * n, dtype=np.uint64)
+
+
+def _check_all(y, y_ref, a_ref, batch, n, m, yrs, ybs, what):
+    """Every output (b, j, i), j < m, of a flat y against the oracle's
+    [rows, mmax] arrays."""
+    r = _all_rows(batch, n).astype(np.int64)
+    bi, ii = r // n, r % n
+    got = np.stack([y[bi * ybs + j * yrs + ii] for j in range(m)], axis=1)
+    ok = oracle.within_tolerance(got, y_ref[:, :m], a_ref[:, :m])
+    assert ok.all(), (what, m, int((~ok).sum()), np.argwhere(~ok)[:5].tolist())
+    return got
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=[f"{c[0]}_{c[1]}x{c[2]}_b{c[3]}" for c in CONFIGS])
-def test_full_size_sampled_parity(cfg):
+def test_full_size_parity_every_output(cfg):
     fmt, n, k, batch, ms, grouped, ci = cfg
     w = _weights(fmt, batch * n, k, 1000 + ci)
     mmax = max(ms)
@@ -81,63 +93,59 @@ def test_full_size_sampled_parity(cfg):
         x = inputs.normal((batch, mmax, k), 2000 + ci, inputs.X_STD)
         xrs, xbs, yrs, ybs = k, mmax * k, n, mmax * n
     xd = torch.from_numpy(np.ascontiguousarray(x).reshape(-1)).to(dev)
-    rows = _sample_rows(batch, n, 48, 5000 + ci)
-    bi, ii = rows // n, rows % n
-    outs = {}
+    y_ref, a_ref = oracle.matvec_rows(w, fmt, n, k, x, mmax, xrs, xbs, _all_rows(batch, n))   # [rows, mmax]
+    first = None
     for m in ms:
-        yd = H.canary(batch * mmax * n)
+        yd = H.canary(batch * mmax * n + TAIL)
         rem.check(rem.rem_matvec(wd, fmt, n, k, batch, xd, m, xbs, yd, ybs))
         torch.cuda.synchronize()
         y = yd.cpu().numpy()
-        y_ref, a_ref = oracle.matvec_rows(w, fmt, n, k, x, m, xrs, xbs, rows)   # [rows, m]
-        got = np.stack([y[bi.astype(np.int64) * ybs + j * yrs + ii.astype(np.int64)] for j in range(m)], axis=1)
-        ok = oracle.within_tolerance(got, y_ref, a_ref)
-        assert ok.all(), (fmt, m, int((~ok).sum()))
-        outs[m] = got
-    # row exactness on the samples: input row 0 of every m equals the m = 1 call
-    if 1 in outs:
-        for m, got in outs.items():
-            assert np.array_equal(got[:, 0].view(np.uint32), outs[1][:, 0].view(np.uint32)), m
+        assert np.all(y[batch * mmax * n:] == H.CANARY), (fmt, m, "wrote past the end of y")
+        got = _check_all(y, y_ref, a_ref, batch, n, m, yrs, ybs, fmt)
+        # row exactness on every row: input row 0 of every m equals the first m's
+        if first is None:
+            first = got[:, 0].copy()
+        assert np.array_equal(got[:, 0].view(np.uint32), first.view(np.uint32)), m
 
 
 def test_full_size_many_rows_and_bias():
     """Q4_K 14336x4096 at m = 16, 32 (rem_matvec_many) and Q8_0 4096x4096 m = 8
-    plus a bias vector (rem_matvec_axpby, alpha = beta = 1), on sampled outputs."""
+    plus a bias vector (rem_matvec_axpby, alpha = beta = 1), every output."""
     dev = H.dev()
     fmt, n, k = "q4_K", 14336, 4096
     w = _weights(fmt, n, k, 1009)
     wd = torch.from_numpy(w.reshape(-1)).to(dev)
     x = inputs.activations(32, k, 2009)
     xd = H.to_dev_f32(x)
-    rows = _sample_rows(1, n, 48, 5009)
+    y_ref, a_ref = oracle.matvec_rows(w, fmt, n, k, x, 32, k, 0, _all_rows(1, n))
     for m in (16, 32):
-        yd = H.canary(m * n)
+        yd = H.canary(m * n + TAIL)
         rem.check(rem.rem_matvec_many(wd, fmt, n, k, 1, xd, m, k, 0, yd, n, 0, 0))
         torch.cuda.synchronize()
-        y = yd.cpu().numpy().reshape(m, n)
-        y_ref, a_ref = oracle.matvec_rows(w, fmt, n, k, x, m, k, 0, rows)
-        got = y[:, rows.astype(np.int64)].T
-        assert oracle.within_tolerance(got, y_ref, a_ref).all(), m
+        y = yd.cpu().numpy()
+        assert np.all(y[m * n:] == H.CANARY)
+        _check_all(y, y_ref, a_ref, 1, n, m, n, 0, "q4_K many")
     fmt, n, k, m = "q8_0", 4096, 4096, 8
     w = _weights(fmt, n, k, 1010)
     wd = torch.from_numpy(w.reshape(-1)).to(dev)
     x = inputs.activations(m, k, 2010)
     bias = inputs.activations(1, n, 3010)[0]
     xd, bd = H.to_dev_f32(x), H.to_dev_f32(bias)
-    yd = H.canary(m * n)
+    yd = H.canary(m * n + TAIL)
     rem.check(rem.rem_matvec_axpby(wd, fmt, n, k, 1, xd, m, k, 0, yd, n, 0, 1.0, 1.0, bd, 0, n))
     torch.cuda.synchronize()
-    rows = _sample_rows(1, n, 48, 5010)
-    y_ref, a_ref = oracle.matvec_rows(w, fmt, n, k, x, m, k, 0, rows)
-    got = yd.cpu().numpy().reshape(m, n)[:, rows.astype(np.int64)].T
-    ref = y_ref + bias[rows.astype(np.int64)].astype(np.float64)[:, None]
-    tol = 1e-4 * a_ref + 1e-7 + 2.0 ** -22 * (np.abs(y_ref) + np.abs(bias[rows.astype(np.int64)])[:, None])
+    yall = yd.cpu().numpy()
+    assert np.all(yall[m * n:] == H.CANARY)
+    y_ref, a_ref = oracle.matvec_rows(w, fmt, n, k, x, m, k, 0, _all_rows(1, n))
+    got = yall[:m * n].reshape(m, n).T
+    ref = y_ref + bias.astype(np.float64)[:, None]
+    tol = 1e-4 * a_ref + 1e-7 + 2.0 ** -22 * (np.abs(y_ref) + np.abs(bias)[:, None])
     assert np.all(np.abs(got - ref) <= tol)
 
 
 def test_full_size_affine_sampled():
     """Affine 4-bit codes in groups of 64, 14336x4096, m = 1..8 through
-    rem_matvec_affine (the bench's affine workload shape), sampled rows."""
+    rem_matvec_affine (the bench's affine workload shape), every output."""
     bits, gs, n, k = 4, 64, 14336, 4096
     wt = rem.affine_wtype(bits, gs)
     g = np.random.Generator(np.random.PCG64(1013))
@@ -154,15 +162,15 @@ def test_full_size_affine_sampled():
     bd = torch.from_numpy(bi.view(np.int16).reshape(-1)).to(dev)
     x = inputs.activations(8, k, 2013)
     xd = H.to_dev_f32(x)
-    rows = _sample_rows(1, n, 48, 5013)
+    y_ref, a_ref = oracle.affine_matvec_rows(codes, sc, bi, bits, gs, n, k, x, 8, k, 0, _all_rows(1, n))
     first = None
     for m in range(1, 9):
-        yd = H.canary(m * n)
+        yd = H.canary(m * n + TAIL)
         rem.check(rem.rem_matvec_affine(cd, sd, bd, wt, n, k, 1, xd, m, k, 0, yd, n, 0, 0))
         torch.cuda.synchronize()
-        got = yd.cpu().numpy().reshape(m, n)[:, rows.astype(np.int64)].T
-        y_ref, a_ref = oracle.affine_matvec_rows(codes, sc, bi, bits, gs, n, k, x, m, k, 0, rows)
-        assert oracle.within_tolerance(got, y_ref, a_ref).all(), m
+        y = yd.cpu().numpy()
+        assert np.all(y[m * n:] == H.CANARY)
+        got = _check_all(y, y_ref, a_ref, 1, n, m, n, 0, "affine")
         if first is None:
             first = got[:, 0].copy()
         assert np.array_equal(got[:, 0].view(np.uint32), first.view(np.uint32)), m

@@ -1,6 +1,8 @@
-"""Lane layouts of the mat-vec kernel: one weight row per lane, two rows per
-lane, and two lane groups that each hold two rows and half of the input rows
-(include/rem.h, "Environment"; REM_LAYOUT pins one).  The arithmetic of every
+"""Lane layouts of the lanes-over-rows (SIMT) engine: one weight row per
+lane, two rows per lane, and two lane groups that each hold two rows and half
+of the input rows (include/rem.h, rem_schedule.layout; the tests pin one with
+rem_set_thread_schedule, and pin the SIMT engine for the formats whose
+default engine is the tensor cores).  The arithmetic of every
 output is fixed by row exactness (module doc "Row exactness" of mlx-native
 0.18.0 src/ops/row_exact_matvec.rs), so every layout must give the same bits,
 and those bits must match the oracle.  The cases cover ragged row counts, odd
@@ -8,7 +10,6 @@ m (the second lane group repeats one input row), split 1 and split > 1,
 batch-major and token-major inputs, the alpha/beta epilogue, affine weights
 and the plain (non-TMA) staging path."""
 import contextlib
-import os
 
 import numpy as np
 import pytest
@@ -34,15 +35,20 @@ def _lib():
 
 @contextlib.contextmanager
 def pinned(layout):
-    old = os.environ.get("REM_LAYOUT")
-    os.environ["REM_LAYOUT"] = str(layout)
+    rem.check(rem.rem_set_thread_schedule(rem.Schedule(layout=layout, engine=rem.ENGINE_SIMT)))
     try:
         yield
     finally:
-        if old is None:
-            del os.environ["REM_LAYOUT"]
-        else:
-            os.environ["REM_LAYOUT"] = old
+        rem.check(rem.rem_set_thread_schedule(None))
+
+
+@contextlib.contextmanager
+def simt():
+    rem.check(rem.rem_set_thread_schedule(rem.Schedule(engine=rem.ENGINE_SIMT)))
+    try:
+        yield
+    finally:
+        rem.check(rem.rem_set_thread_schedule(None))
 
 
 def layouts(m, fmt="q8_0"):
@@ -94,8 +100,9 @@ def test_layouts_bitwise_equal_and_match_oracle(fmt, n, k, batch, m, split, tm, 
                              w_offset=off)
         got[lay] = H.gather_y(y, batch, m, n, yrs, ybs)
         H.assert_close_to_oracle(got[lay], y_ref, a_ref, f"layout {lay}")
-    auto = H.gather_y(H.run_matvec(w, fmt, n, k, batch, x, m, xrs, xbs, yrs, ybs, batch * m * n, split=split,
-                                   w_offset=off), batch, m, n, yrs, ybs)
+    with simt():
+        auto = H.gather_y(H.run_matvec(w, fmt, n, k, batch, x, m, xrs, xbs, yrs, ybs, batch * m * n, split=split,
+                                       w_offset=off), batch, m, n, yrs, ybs)
     for lay, y in got.items():
         assert np.array_equal(y.view(np.uint32), got[0].view(np.uint32)), f"layout {lay} differs from layout 0"
     assert np.array_equal(auto.view(np.uint32), got[0].view(np.uint32))
@@ -104,11 +111,13 @@ def test_layouts_bitwise_equal_and_match_oracle(fmt, n, k, batch, m, split, tm, 
         xj = x.reshape(-1)
         if tm:
             x1 = xj[j * xrs:j * xrs + batch * k].reshape(1, batch * k)
-            y1 = H.run_matvec(w, fmt, n, k, batch, x1, 1, batch * k, k, batch * n, n, batch * n, split=split)
+            with simt():
+                y1 = H.run_matvec(w, fmt, n, k, batch, x1, 1, batch * k, k, batch * n, n, batch * n, split=split)
             y1 = H.gather_y(y1, batch, 1, n, batch * n, n)
         else:
             x1 = x.reshape(batch, m, k)[:, j, :].copy()
-            y1 = H.run_matvec(w, fmt, n, k, batch, x1, 1, k, k, n, n, batch * n, split=split)
+            with simt():
+                y1 = H.run_matvec(w, fmt, n, k, batch, x1, 1, k, k, n, n, batch * n, split=split)
             y1 = H.gather_y(y1, batch, 1, n, n, n)
         assert np.array_equal(y1[:, 0].view(np.uint32), got[0][:, j].view(np.uint32)), f"row {j}"
 
@@ -167,8 +176,9 @@ def test_pinned_layout_without_kernel_is_a_launch_error():
     yd = H.canary(2 * n)
     with pinned(2):   # two lane groups exist from m = 2 only
         rc = rem.rem_matvec_ex(wp, "q8_0", n, k, 1, xd, 1, k, 0, yd, n, 0, 0, 0)
+        err = rem.rem_last_error()
     assert rc == rem.REM_ELAUNCH
-    assert "REM_LAYOUT" in rem.rem_last_error()
+    assert "lane layout 2" in err
     torch.cuda.synchronize()
     assert np.all(yd.cpu().numpy() == H.CANARY)
     with pinned(1):   # two rows per lane exist at every m

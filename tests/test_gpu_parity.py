@@ -36,40 +36,11 @@ def _lib():
 
 # ---------------------------------------------------------------- decode / quantize
 
-def _adversarial_blocks(fmt, rows, k, seed):
-    """Random bytes with finite fp16 scale fields (normal and subnormal)."""
-    rb = oracle.row_bytes(fmt, k)
-    b = inputs.uniform_bytes(rows * rb, seed).reshape(rows, rb)
-    if fmt == "f16":
-        h = b.view(np.uint16)
-        h[(h & 0x7C00) == 0x7C00] &= 0x3FFF   # no inf / NaN
-        return b
-    if fmt == "bf16":
-        h = b.view(np.uint16)
-        h[(h & 0x7F80) == 0x7F80] &= 0xBFFF   # no inf / NaN
-        return b
-    if fmt == "f32":
-        u = b.view(np.uint32)
-        u[(u & 0x7F800000) == 0x7F800000] &= 0xBFFFFFFF
-        return b
-    g = np.random.Generator(np.random.PCG64(seed + 1))
-    bb = oracle.block_bytes(fmt)
-    nb = rb // bb
-    blocks = b.reshape(rows, nb, bb)
-    fields = {"q8_0": [0], "q5_0": [0], "q4_K": [0, 2], "q6_K": [208]}[fmt]
-    for off in fields:
-        h = g.integers(0, 0x7C00, size=(rows, nb)).astype(np.uint16)   # finite, positive
-        h |= (g.integers(0, 2, size=(rows, nb)) << 15).astype(np.uint16)
-        h[:, ::7] &= 0x03FF                                            # some subnormal scales
-        blocks[:, :, off:off + 2] = h.view(np.uint8).reshape(rows, nb, 2)
-    return b
-
-
 @pytest.mark.parametrize("fmt", FMTS)
 def test_dequantize_bit_exact(fmt):
     k = {"f16": 520, "q8_0": 1024, "q5_0": 1024, "q4_K": 1024, "q6_K": 1024, "bf16": 520, "f32": 520}[fmt]
     rows = 37
-    for w in (oracle.quantize(inputs.weights(rows, k, 101), fmt), _adversarial_blocks(fmt, rows, k, 102)):
+    for w in (oracle.quantize(inputs.weights(rows, k, 101), fmt), H.adversarial_blocks(fmt, rows, k, 102)):
         ref = oracle.dequantize(w, fmt, rows, k)
         wh, wp = H.to_dev_bytes(w)
         out = H.canary(rows * k)
