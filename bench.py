@@ -5,10 +5,12 @@ Metric: achieved HBM GB/s (algorithmic weight + x + y bytes per call, over
 the device time of the calls) and us per call, m = 1..8.  One "step" is one
 pass of the whole path over the workload: one call per listed m.
 
-Default workload: Q8_0 weights n = 4096, k = 4096, batch 1, m swept 1..8
-(W ~ N(0, 0.02) quantized to Q8_0, x ~ N(0, 1)), synthetic and seeded.
-Weights are read cold: every call uses the next copy of a ring of weight
-copies totalling >= 4x the L2 size.
+Default workload: Q6_K weights n = 128256, k = 4096 (431 MB, the largest
+configuration that fits one GPU), batch 1, m in {1, 4, 8} (W ~ N(0, 0.02)
+quantized to Q6_K, x ~ N(0, 1)), synthetic and seeded.  Weights are read
+cold: every call uses the next copy of a ring of weight copies totalling
+>= 4x the L2 size.  The same line carries per-m tables of the other
+configurations (key "workloads"; --no-extra skips them).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -42,8 +44,11 @@ WORKLOADS = {
     "q8_0_n16384_k4096_m1-8": ("q8_0", 16384, 4096, 1, list(range(1, 9)), False, 6),
     "q4_K_n28672_k4096_m1-8": ("q4_K", 28672, 4096, 1, list(range(1, 9)), False, 7),
     "q5_0_grouped_b32_n1024_k4096_m8": ("q5_0", 1024, 4096, 32, [8], True, 8),
-    # more than 8 input rows (rem_matvec_many: groups of 8, one pass over W each)
+    # more than 8 input rows (rem_matvec_many: one pass over W per group of 8 rows on the SIMT
+    # engine, of 16 rows on the tensor-core engine)
     "q4_K_n14336_k4096_m16,32": ("q4_K", 14336, 4096, 1, [16, 32], False, 9),
+    "q8_0_n16384_k4096_m16,32": ("q8_0", 16384, 4096, 1, [16, 32], False, 14),
+    "q6_K_n128256_k4096_m16": ("q6_K", 128256, 4096, 1, [16], False, 15),
     # dense weights under the same row contract
     "bf16_n8192_k4096_m1-8": ("bf16", 8192, 4096, 1, list(range(1, 9)), False, 11),
     "f32_n4096_k4096_m1-8": ("f32", 4096, 4096, 1, list(range(1, 9)), False, 12),
@@ -54,7 +59,13 @@ WORKLOADS = {
 }
 # workloads that run the epilogue alpha * W.x + beta * c with c a bias vector
 EPILOGUE = {"q8_0_n4096_k4096_m1-8_bias": (1.0, 1.0)}
-DEFAULT = "q8_0_n4096_k4096_m1-8"
+# the largest configuration that fits one GPU (431 MB of Q6_K weights)
+DEFAULT = "q6_K_n128256_k4096_m1,4,8"
+# the other configurations timed in the same run, one per-m table each
+EXTRA = ["f16_n256_k512_m1", "q8_0_n4096_k4096_m1-8", "q4_K_n14336_k4096_m1-8", "q5_0_grouped_b16_n1024_k4096_m8",
+         "f16_n8192_k4096_m1-8", "q8_0_n16384_k4096_m1-8", "q4_K_n28672_k4096_m1-8", "q5_0_grouped_b32_n1024_k4096_m8",
+         "q4_K_n14336_k4096_m16,32", "q8_0_n16384_k4096_m16,32", "q6_K_n128256_k4096_m16",
+         "bf16_n8192_k4096_m1-8", "f32_n4096_k4096_m1-8", "a4_g64_n14336_k4096_m1-8", "q8_0_n4096_k4096_m1-8_bias"]
 METRIC = "achieved HBM GB/s (% of GB300 peak) and us/call, m=1..8 quantized mat-vec"
 
 
@@ -184,79 +195,181 @@ def job_throughput(bytes_per_step: int, steps: int, seconds: float, world: int) 
     return world * bytes_per_step * steps / seconds / 1e9
 
 
+class Workload:
+    """One configuration on the device: weights quantized on the device (a ring
+    of copies totalling >= 4x the L2 size, so calls read them cold), inputs,
+    outputs, and call(slot, m) through the library's public C ABI."""
+
+    def __init__(self, name, dev, rem, inputs, l2):
+        import torch
+        fmt, n, k, batch, ms, grouped, ci = WORKLOADS[name]
+        self.name, self.fmt, self.n, self.k, self.batch, self.ms, self.grouped = name, fmt, n, k, batch, ms, grouped
+        self.rem = rem
+        self.rb = rem.rem_row_bytes(fmt, k)
+        wbytes = self.rb * n * batch
+        self.wbytes = wbytes
+        mmax = max(ms)
+        gs = affine_group_size(fmt)
+        self.gs = gs
+        ring = max(1, math.ceil(4 * l2 / wbytes))
+        if gs:
+            # affine: random codes, f16 scales ~ 0.02*3/15 and biases ~ -0.02*3 per group (device-side, seeded)
+            g = torch.Generator(device=dev)
+            g.manual_seed(1000 + ci)
+            w0 = torch.randint(0, 256, (wbytes,), dtype=torch.uint8, device=dev, generator=g)
+            ng = batch * n * (k // gs)
+            scales = (torch.rand(ng, device=dev, generator=g) * 0.004 + 0.002).half()
+            biases = (torch.rand(ng, device=dev, generator=g) * -0.06).half()
+            ring = max(1, math.ceil(4 * l2 / (wbytes + 4 * ng)))
+        else:
+            # weights: N(0, 0.02) drawn on the device, quantized by the library
+            wf = inputs.torch_normal((batch * n, k), 1000 + ci, inputs.W_STD, dev)
+            w0 = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+            rem.check(rem.rem_quantize(wf, fmt, batch * n, k, w0))
+            del wf
+        self.ring = ring
+        self.wring = [w0] + [w0.clone() for _ in range(ring - 1)]
+        self.sring = [scales] + [scales.clone() for _ in range(ring - 1)] if gs else None
+        self.bring = [biases] + [biases.clone() for _ in range(ring - 1)] if gs else None
+        if grouped:   # token-major: x [m, batch*k], y [m, batch*n]
+            self.x = inputs.torch_normal((mmax, batch * k), 2000 + ci, inputs.X_STD, dev)
+            self.y = torch.empty((mmax, batch * n), dtype=torch.float32, device=dev)
+            self.xbs, self.ybs = k, n
+        else:         # batch-major: x [batch, m, k]
+            self.x = inputs.torch_normal((batch, mmax, k), 2000 + ci, inputs.X_STD, dev)
+            self.y = torch.empty((batch, mmax, n), dtype=torch.float32, device=dev)
+            self.xbs, self.ybs = mmax * k, mmax * n
+        self.epi = EPILOGUE.get(name)
+        self.bias = inputs.torch_normal((batch, n), 3000 + ci, inputs.X_STD, dev) if self.epi else None
+        self.engine = rem.rem_engine_of(fmt, batch * n, k)
+        torch.cuda.synchronize()
+
+    def call(self, slot, m, stream=None, xv=None, yv=None):
+        """One library call for m input rows on ring slot `slot`; xv / yv: a
+        packed per-call segment ([batch, m, k] batch-major or [m, batch*k]
+        token-major) instead of the resident buffers."""
+        rem, fmt, n, k, batch = self.rem, self.fmt, self.n, self.k, self.batch
+        xs, ys = (self.x, self.y) if xv is None else (xv, yv)
+        if xv is None:
+            xb, yb = self.xbs, self.ybs
+        else:
+            xb, yb = (k, n) if self.grouped else (m * k, m * n)
+        w = self.wring[slot]
+        if self.gs:
+            return rem.rem_matvec_affine(w, self.sring[slot], self.bring[slot], fmt, n, k, batch, xs, m, k, xb, ys,
+                                         n, yb, 0, stream)
+        if self.epi:
+            return rem.rem_matvec_axpby(w, fmt, n, k, batch, xs, m, k, xb, ys, n, yb, self.epi[0], self.epi[1],
+                                        self.bias, 0, n, stream)
+        if m > 8:
+            xrs, yrs = (batch * k, batch * n) if self.grouped else (k, n)
+            return rem.rem_matvec_many(w, fmt, n, k, batch, xs, m, xrs, xb, ys, yrs, yb, 0, stream)
+        return rem.rem_matvec(w, fmt, n, k, batch, xs, m, xb, ys, yb, stream)
+
+    def bytes(self, m):
+        extra = 4 * self.batch * self.n if self.epi else 0     # the bias vector, read once per call
+        return call_bytes(self.fmt, self.n, self.k, self.batch, m, self.rb) + extra
+
+    def launches(self, m):
+        per = 8 if self.engine != 1 else 16
+        return (m + per - 1) // per
+
+    def free(self):
+        self.wring = self.sring = self.bring = None
+        self.x = self.y = self.bias = None
+
+
+def time_per_m(wl, stream, budget_s=2e-3):
+    """Device microseconds per call for each m: a CUDA graph of one call per
+    ring slot (cold weights), replayed until about budget_s of work is timed
+    with events on the launching stream.  Also returns the same on one weight
+    copy (warm, for comparison only) and the plan of the last call."""
+    import torch
+    per_m, warm, plans = {}, {}, {}
+    for m in wl.ms:
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for slot in range(wl.ring):
+                    wl.rem.check(wl.call(slot, m))
+            plans[m] = wl.rem.rem_last_plan()
+            for _ in range(3):
+                g.replay()
+            stream.synchronize()
+            t0 = time.perf_counter()
+            g.replay()
+            stream.synchronize()
+            one = max(1e-6, time.perf_counter() - t0)
+            reps = max(3, min(2000, int(budget_s / one) + 3))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        per_m[m] = e0.elapsed_time(e1) * 1e3 / (reps * wl.ring)
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for _ in range(16):
+                    wl.rem.check(wl.call(0, m))
+            for _ in range(2):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(10):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        warm[m] = e0.elapsed_time(e1) * 1e3 / (10 * 16)
+    return per_m, warm, plans
+
+
+def per_m_table(wl, per_m, hbm, fp32_peak):
+    out = {}
+    for m in wl.ms:
+        b = wl.bytes(m)
+        gbs = b / (per_m[m] * 1e-6) / 1e9
+        tfl = 2.0 * m * wl.batch * wl.n * wl.k / (per_m[m] * 1e-6) / 1e12
+        out[str(m)] = {"us": round(per_m[m], 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+                       "fp32_tflops": round(tfl, 2), "fp32_frac": round(tfl / fp32_peak, 4)}
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
     import quantized_few_row_gb300 as rem
     from quantized_few_row_gb300 import inputs
 
-    fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload]
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     rem.build()
     rem.load()
-    rb = rem.rem_row_bytes(fmt, k)
-    wbytes = rb * n * batch
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-    ring = max(1, math.ceil(4 * l2 / wbytes))
-    mmax = max(ms)
-
-    # weights: N(0, 0.02) drawn on the device, quantized by the library
-    wf = inputs.torch_normal((batch * n, k), 1000 + ci, inputs.W_STD, dev)
-    gs = affine_group_size(fmt)
-    if gs:
-        # affine: random codes, f16 scales ~ 0.02*3/15 and biases ~ -0.02*3 per group (device-side, seeded)
-        del wf
-        g = torch.Generator(device=dev)
-        g.manual_seed(1000 + ci)
-        w0 = torch.randint(0, 256, (wbytes,), dtype=torch.uint8, device=dev, generator=g)
-        ng = batch * n * (k // gs)
-        scales = (torch.rand(ng, device=dev, generator=g) * 0.004 + 0.002).half()
-        biases = (torch.rand(ng, device=dev, generator=g) * -0.06).half()
-        ring = max(1, math.ceil(4 * l2 / (wbytes + 4 * ng)))
-    else:
-        w0 = torch.empty(wbytes, dtype=torch.uint8, device=dev)
-        rem.check(rem.rem_quantize(wf, fmt, batch * n, k, w0))
-        del wf
-    wring = [w0] + [w0.clone() for _ in range(ring - 1)]
-    sring = [scales] + [scales.clone() for _ in range(ring - 1)] if gs else None
-    bring = [biases] + [biases.clone() for _ in range(ring - 1)] if gs else None
-    if grouped:   # token-major: x [m, batch*k], y [m, batch*n]
-        x = inputs.torch_normal((mmax, batch * k), 2000 + ci, inputs.X_STD, dev)
-        y = torch.empty((mmax, batch * n), dtype=torch.float32, device=dev)
-        xbs, ybs = k, n
-    else:         # batch-major: x [batch, m, k]
-        x = inputs.torch_normal((batch, mmax, k), 2000 + ci, inputs.X_STD, dev)
-        y = torch.empty((batch, mmax, n), dtype=torch.float32, device=dev)
-        xbs, ybs = mmax * k, mmax * n
-    torch.cuda.synchronize()
-
-    epi = EPILOGUE.get(args.workload)
-    bias = inputs.torch_normal((batch, n), 3000 + ci, inputs.X_STD, dev) if epi else None
-
-    def call(slot, m, stream=None, xv=None, yv=None):
-        # xv/yv: a packed per-call segment ([batch, m, k] batch-major or [m, batch*k] token-major)
-        xs, ys = (x, y) if xv is None else (xv, yv)
-        if xv is None:
-            xb, yb = xbs, ybs
-        else:
-            xb, yb = (k, n) if grouped else (m * k, m * n)
-        if gs:
-            return rem.rem_matvec_affine(wring[slot], sring[slot], bring[slot], fmt, n, k, batch, xs, m, k, xb, ys,
-                                         n, yb, 0, stream)
-        if epi:
-            return rem.rem_matvec_axpby(wring[slot], fmt, n, k, batch, xs, m, k, xb, ys, n, yb, epi[0], epi[1],
-                                        bias, 0, n, stream)
-        if m > 8:
-            xrs, yrs = (batch * k, batch * n) if grouped else (k, n)
-            return rem.rem_matvec_many(wring[slot], fmt, n, k, batch, xs, m, xrs, xb, ys, yrs, yb, 0, stream)
-        return rem.rem_matvec(wring[slot], fmt, n, k, batch, xs, m, xb, ys, yb, stream)
+    wl = Workload(args.workload, dev, rem, inputs, l2)
+    ms = wl.ms
+    fmt, n, k, batch = wl.fmt, wl.n, wl.k, wl.batch
+    ring = wl.ring
 
     # first calls outside any capture (device set-up, schedule caches)
     for m in ms:
-        rem.check(call(0, m))
+        rem.check(wl.call(0, m))
     torch.cuda.synchronize()
+    # host cost of a call (argument checks, plan and tensor-map caches, the
+    # launch) through the Python binding, on a stream that is not captured
+    side = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(side):
+        for m in ms:
+            rem.check(wl.call(0, m, side))
+        side.synchronize()
+        reps = 200
+        t0 = time.perf_counter()
+        for i in range(reps):
+            rem.check(wl.call(0, ms[i % len(ms)], side))
+        host_us = (time.perf_counter() - t0) * 1e6 / reps
+        side.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
     C = len(ms)
@@ -267,7 +380,7 @@ def run_ours(args, rank, world, local_rank):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
                 for c, m in enumerate(ms):
-                    rem.check(call((sidx * C + c) % ring, m))
+                    rem.check(wl.call((sidx * C + c) % ring, m))
             graphs.append(g)
     torch.cuda.synchronize()
 
@@ -292,46 +405,11 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
 
-    extra = 4 * batch * n if epi else 0     # the bias vector, read once per call
-    step_bytes = sum(call_bytes(fmt, n, k, batch, m, rb) + extra for m in ms)
+    step_bytes = sum(wl.bytes(m) for m in ms)
     value = job_throughput(step_bytes, args.steps, elapsed, world)
 
-    # per-m device time (cold ring, graph of one call per ring slot)
-    per_m = {}
-    for m in ms:
-        with torch.cuda.stream(stream):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-                for slot in range(ring):
-                    rem.check(call(slot, m))
-            reps = max(3, int(2e-3 / max(1e-9, elapsed / max(1, args.steps) / C) / ring) + 3)
-            for _ in range(2):
-                g.replay()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-        stream.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * ring)
-        per_m[m] = us
-    # warm, for comparison only: the same weight copy on every call (L2-resident below ~126 MB)
-    per_m_warm = {}
-    for m in ms:
-        with torch.cuda.stream(stream):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-                for _ in range(16):
-                    rem.check(call(0, m))
-            for _ in range(2):
-                g.replay()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(10):
-                g.replay()
-            e1.record(stream)
-        stream.synchronize()
-        per_m_warm[m] = e0.elapsed_time(e1) * 1e3 / (10 * 16)
+    # per-m device time (cold ring, graph of one call per ring slot), and warm for comparison
+    per_m, per_m_warm, plans = time_per_m(wl, stream)
     clk = clocks.stop(busy_mhz_floor=0.0)
 
     # end to end through the public binding: each step's inputs (one x segment per call, packed) go
@@ -343,7 +421,7 @@ def run_ours(args, rank, world, local_rank):
         yoff.append(yoff[-1] + batch * m * n)
     xh = torch.empty(xoff[-1], dtype=torch.float32).pin_memory()
     for i, m in enumerate(ms):
-        src = x[:m].reshape(-1) if grouped else x[:, :m].reshape(-1)
+        src = wl.x[:m].reshape(-1) if wl.grouped else wl.x[:, :m].reshape(-1)
         xh[xoff[i]:xoff[i + 1]].copy_(src.cpu())
     yh = torch.empty(yoff[-1], dtype=torch.float32).pin_memory()
     xp = torch.empty(xoff[-1], dtype=torch.float32, device=dev)
@@ -360,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
     for s in range(e2e_steps):
         xp.copy_(xh, non_blocking=True)
         for i, m in enumerate(ms):
-            rem.check(call(slot % ring, m, cur, xp[xoff[i]:xoff[i + 1]], yp[yoff[i]:yoff[i + 1]]))
+            rem.check(wl.call(slot % ring, m, cur, xp[xoff[i]:xoff[i + 1]], yp[yoff[i]:yoff[i + 1]]))
             slot += 1
         yh.copy_(yp, non_blocking=True)
     t1.record(cur)
@@ -369,24 +447,20 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = job_throughput(step_bytes, e2e_steps, e2e_elapsed, world)
     # the packed path computes what the device-resident layout does, bit for bit (same W, same split)
     for i, m in enumerate(ms):
-        rem.check(call(0, m))
-        ref = (y[:m] if grouped else y[:, :m]).reshape(-1).cpu()
+        rem.check(wl.call(0, m))
+        ref = (wl.y[:m] if wl.grouped else wl.y[:, :m]).reshape(-1).cpu()
         if not torch.equal(ref.view(torch.int32), yh[yoff[i]:yoff[i + 1]].view(torch.int32)):
             raise RuntimeError(f"end-to-end outputs for m={m} differ from the device-resident call")
 
     hbm, sm_max, peak_kind = peaks()
     fp32_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12   # TFLOP/s, plain FMA pipe
-    per_m_out = {}
-    for m in ms:
-        b = call_bytes(fmt, n, k, batch, m, rb) + extra
-        gbs = b / (per_m[m] * 1e-6) / 1e9
-        tfl = 2.0 * m * batch * n * k / (per_m[m] * 1e-6) / 1e12
-        per_m_out[str(m)] = {"us": round(per_m[m], 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
-                             "fp32_tflops": round(tfl, 2), "fp32_frac": round(tfl / fp32_peak, 4)}
-    per_step_launches = sum((m + 7) // 8 for m in ms)   # a call of m > 8 rows runs ceil(m/8) launches
+    per_step_launches = sum(wl.launches(m) for m in ms)
     launches = args.steps * per_step_launches
     avg_launch_s = elapsed / launches
     achieved = (step_bytes / per_step_launches) / avg_launch_s / 1e9
+    kernel_s = sum(per_m[m] for m in ms) * 1e-6
+    achieved_kernel = step_bytes / kernel_s / 1e9
+    engine = {0: "simt (lanes over rows, FP32 pipe)", 1: "tc (tcgen05 tensor cores)"}.get(wl.engine, "?")
     res = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -401,22 +475,55 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "f32 accumulate over %s weights" % fmt,
         "data": "synthetic (seeded W ~ N(0,0.02) quantized on device, x ~ N(0,1))",
         "config": {"workload": args.workload, "format": fmt, "n": n, "k": k, "batch": batch, "m": ms,
-                   "token_major": grouped, "l2": f"cold: weight ring of {ring} copies x {wbytes} B (>= 4x L2)",
+                   "token_major": wl.grouped, "engine": engine,
+                   "l2": f"cold: weight ring of {ring} copies x {wl.wbytes} B (>= 4x L2)",
                    "timed": "CUDA graphs of one step each, events on the launching stream",
                    "parallelism": f"replicas x{world}"},
         "per_m_us": {str(m): round(per_m[m], 3) for m in ms},
         "per_m_warm_us": {str(m): round(per_m_warm[m], 3) for m in ms},
-        "per_m": per_m_out,
+        "per_m": per_m_table(wl, per_m, hbm, fp32_peak),
+        "plans": {str(m): plans[m] for m in ms},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(args.workload),
-                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "rem_mv_kernel (all m of the step)",
+                     "frac": round(achieved / hbm, 4),
+                     "basis": "step: algorithmic bytes of the step's launches over the timed graph replays "
+                              "(gaps between replays included)",
+                     "achieved_kernel": round(achieved_kernel, 1), "frac_kernel": round(achieved_kernel / hbm, 4),
+                     "basis_kernel": "kernel: the same bytes over the sum of the per-m CUDA-event launch times "
+                                     "(graphs of back-to-back calls on cold weights)",
+                     "traffic": profiled_traffic(args.workload),
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "rem_tc_kernel / rem_mv_kernel (all m of the step)",
                      "fp32_peak_tflops": round(fp32_peak, 1)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "path": "packed step inputs pinned -> device (1 copy), one library call per m, packed outputs -> pinned host (1 copy), un-captured"},
+        "host_us_per_call": round(host_us, 2),
+        "host_us_basis": "wall time per library call through the Python (ctypes) binding, stream not captured",
         "gpu_launches": launches,
         "clocks": clk,
     }
+    wl.free()
+    del graphs
+    torch.cuda.empty_cache()
+
+    # the other configurations, one table each (per-m device time on cold weights)
+    if not args.no_extra:
+        extra = {}
+        for name in EXTRA:
+            if name == args.workload:
+                continue
+            w2 = Workload(name, dev, rem, inputs, l2)
+            for m in w2.ms:
+                rem.check(w2.call(0, m))
+            torch.cuda.synchronize()
+            pm, warm, pl = time_per_m(w2, stream, budget_s=1e-3)
+            extra[name] = {"engine": {0: "simt", 1: "tc"}.get(w2.engine, "?"),
+                           "weight_bytes": w2.wbytes,
+                           "per_m": per_m_table(w2, pm, hbm, fp32_peak),
+                           "per_m_warm_us": {str(m): round(warm[m], 3) for m in w2.ms}}
+            w2.free()
+            del w2
+            torch.cuda.empty_cache()
+        res["workloads"] = extra
     return res
 
 
@@ -513,6 +620,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="time only the selected workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
