@@ -189,19 +189,16 @@ __host__ __device__ constexpr int tc_tmem_cols(int wt, int mp) {
 // x box) | input box (mp x chunk floats, padded to 128 B)], two B tiles of a
 // chunk (bf16, 2*mp rows x chunk values), two buffers of partials (the warp
 // groups past the first of each lane quarter, x 4 quarters x mp x 32 floats;
-// the cross-range partials reuse them), the scales of the regions in flight
-// (consumer warps x slots x regions per warp x 32 floats), the mbarriers and
-// the tensor-memory address, plus slack to align the base to 128 bytes.
+// the cross-range partials reuse them), the mbarriers and the tensor-memory
+// address, plus slack to align the base to 128 bytes.
 inline uint32_t tc_smem_bytes(int wt, int mp, int stages, int split) {
     const uint32_t xpad = ((uint32_t)mp * chunk_values(wt) * 4u + 127u) & ~127u;
     const uint32_t stage = (uint32_t)kTcRows * chunk_box(wt) + xpad;
     const uint32_t btiles = 2u * (uint32_t)(chunk_values(wt) / 16) * 64u * (uint32_t)mp;
     const uint32_t groups = (uint32_t)tc_consumer_warps(mp) / 4u;
     const uint32_t pbuf = 2u * (groups - 1u) * 4u * (uint32_t)mp * 32u * 4u;
-    const uint32_t rpw = (uint32_t)(tc_kpw(mp) / tc_region_ksteps(wt, mp));
-    const uint32_t scales = (uint32_t)tc_consumer_warps(mp) * (uint32_t)tc_slots(wt, mp) * rpw * 32u * 4u;
     (void)split;
-    return (uint32_t)stages * stage + btiles + pbuf + scales + 8u * (4 * kMaxStages + 1) + 16u + 128u;
+    return (uint32_t)stages * stage + btiles + pbuf + 8u * (4 * kMaxStages + 1) + 16u + 128u;
 }
 const void* tc_kernel(int wt, int mp);
 const void* tc_kernel_q8_0(int mp);

@@ -164,154 +164,178 @@ __device__ __forceinline__ void row_words(const uint8_t* row, uint32_t (&w)[N]) 
 
 // ---------------------------------------------------------------- formats
 
-// Per format: kUPC units of 64 values (4 K-steps of 16) per staged chunk, the
-// permutation of the 16 values of a K-step in A's columns (kPerm: 0 = natural
-// order, 1 = values 4g, 4g+2, 4g+1, 4g+3 for each group g of 4: the pairs a
-// byte-parallel decode produces), and decode<KPW>(row, o, u, s0, a, scale):
-// K-steps s0 .. s0+KPW-1 of unit u of a chunk staged at byte o of the row ->
-// 8*KPW columns of bf16 pairs (K-step s0 + s in columns 8s..8s+7) and the
-// scales of its accumulator regions (one per K-step, or one per scale block
-// when a warp decodes all of a block's K-steps).  Every decode reads its
-// words with 16-byte loads at compile-time positions, so the few (o, block)
-// combinations of a format are separate bodies; the rest is runtime
-// arithmetic.
+// Int8 codes: bytes 0 and 2 (pair 0) and 1 and 3 (pair 1) of v as exact
+// bfloat16 pairs.  The low 7 bits go in as 128 + (q & 127) and the sign bit
+// as the subtrahend 128 or 256, so one subtraction gives q exactly.
+__device__ __forceinline__ void s8_bf16(uint32_t v, uint32_t& p0, uint32_t& p1) {
+    p0 = bf16x2_sub(lop_and_or(v, 0x007F007Fu, 0x43004300u), lop_and_or(v, 0x00800080u, 0x43004300u));
+    const uint32_t w = v >> 8;
+    p1 = bf16x2_sub(lop_and_or(w, 0x007F007Fu, 0x43004300u), lop_and_or(w, 0x00800080u, 0x43004300u));
+}
+
+// Per format:
+//   kUPC         units per staged chunk; a unit is one K-step of 16 values
+//                for each of the 4 warp groups (4 MMAs);
+//   kPerm        order of the 16 values of a K-step in A's columns (0 =
+//                natural, 1 = values 4i, 4i+2, 4i+1, 4i+3 for each group i of
+//                4: the byte pairs a byte-parallel decode yields);
+//   kstep(u, g)  the K-step of the chunk whose codes warp group g decodes in
+//                unit u, i.e. the B tile that the MMA of A columns 8g..8g+7
+//                of that unit reads;
+//   Regs         the words a consumer lane keeps from one load to the units
+//                that decode them (kLoad(u): a load at unit u; kLastLoad: the
+//                unit after whose load the staged weights are no longer read);
+//   load<U>      16-byte shared loads at compile-time positions; a switch
+//                picks the body for the runtime byte position (chunk offset o,
+//                warp group g);
+//   decode<U>    unit U's 16 codes of the lane's row as 8 bfloat16 pairs, and
+//                their scale.
+// The mapping keeps every byte a group needs for the chunk in one place, so
+// each staged byte is read about once per lane.
 template <int WT> struct TcFmt;
 
 // Q8_0: a chunk is 4 blocks (d f16 | 32 int8), 128 values at byte o = 0 or 8
-// of the staged window; unit u is blocks 2u, 2u+1, K-step s0 of it the codes
-// 16(s0%2) .. 16(s0%2)+15 of block 2u + s0/2.
+// of the staged window.  Warp group g decodes block g: its first 16 codes in
+// unit 0 and the other 16 in unit 1 (K-step 2g + u).
 template <> struct TcFmt<kQ8_0> {
-    static constexpr int kUPC = 2, kPerm = 0;
-    // NW code words of block B (at byte P of the row) from word W0 of its codes
-    template <int P, int W0, int NW>
-    __device__ __forceinline__ static void codes(const uint8_t* row, uint32_t* a, float& scale) {
-        uint32_t dw[1], q[NW + 1];
+    static constexpr int kUPC = 2, kPerm = 1, kLastLoad = 0;
+    __host__ __device__ static constexpr int kstep(int u, int g) { return 2 * g + u; }
+    __host__ __device__ static constexpr bool kLoad(int u) { return u == 0; }
+    struct Regs {
+        uint32_t q[8];  // the 32 codes
+        float d;
+    };
+    template <int P>
+    __device__ __forceinline__ static void block(const uint8_t* row, Regs& r) {
+        uint32_t dw[1];
         row_words<P, 1>(row, dw);
-        row_words<P + 4 * W0, NW + 1>(row, q);           // the words straddle: codes follow d (2 bytes)
-        scale = h2f(dw[0]);
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            const uint32_t v = __byte_perm(q[i], q[i + 1], 0x5432);
-            const float2 w01 = bytes01_s(v), w23 = bytes01_s(v >> 16);
-            a[2 * i] = bf16x2_rn(w01.x, w01.y);
-            a[2 * i + 1] = bf16x2_rn(w23.x, w23.y);
+        row_words<P + 2, 8>(row, r.q);
+        r.d = h2f(dw[0]);
+    }
+    template <int U>
+    __device__ __forceinline__ static void load(const uint8_t* row, int o, int g, Regs& r) {
+        switch ((o ? 4 : 0) + g) {
+        case 0: block<0>(row, r); break;
+        case 1: block<34>(row, r); break;
+        case 2: block<68>(row, r); break;
+        case 3: block<102>(row, r); break;
+        case 4: block<8>(row, r); break;
+        case 5: block<42>(row, r); break;
+        case 6: block<76>(row, r); break;
+        default: block<110>(row, r); break;
         }
     }
-    template <int KPW>
-    __device__ __forceinline__ static void decode(const uint8_t* row, int o, int u, int s0, uint32_t (&a)[8 * KPW],
-                                                  float (&scale)[1]) {
-        // KPW 1: (o, block, half) -> 16 bodies; KPW 2: (o, block) -> 8
-        const int sel = KPW == 1 ? (o ? 8 : 0) + 2 * (2 * u + (s0 >> 1)) + (s0 & 1) : (o ? 4 : 0) + 2 * u + (s0 >> 1);
-#define REM_Q8_CASE(I, P, W0) case I: codes<P, W0, 4 * KPW>(row, a, scale[0]); break;
-        if constexpr (KPW == 1) {
-            switch (sel) {
-            REM_Q8_CASE(0, 0, 0) REM_Q8_CASE(1, 0, 4) REM_Q8_CASE(2, 34, 0) REM_Q8_CASE(3, 34, 4)
-            REM_Q8_CASE(4, 68, 0) REM_Q8_CASE(5, 68, 4) REM_Q8_CASE(6, 102, 0) REM_Q8_CASE(7, 102, 4)
-            REM_Q8_CASE(8, 8, 0) REM_Q8_CASE(9, 8, 4) REM_Q8_CASE(10, 42, 0) REM_Q8_CASE(11, 42, 4)
-            REM_Q8_CASE(12, 76, 0) REM_Q8_CASE(13, 76, 4) REM_Q8_CASE(14, 110, 0) default: codes<110, 4, 4>(row, a, scale[0]); break;
-            }
-        } else {
-            switch (sel) {
-            REM_Q8_CASE(0, 0, 0) REM_Q8_CASE(1, 34, 0) REM_Q8_CASE(2, 68, 0) REM_Q8_CASE(3, 102, 0)
-            REM_Q8_CASE(4, 8, 0) REM_Q8_CASE(5, 42, 0) REM_Q8_CASE(6, 76, 0) default: codes<110, 0, 8>(row, a, scale[0]); break;
-            }
-        }
-#undef REM_Q8_CASE
+    template <int U>
+    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[8], float& scale) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s8_bf16(r.q[4 * U + i], a[2 * i], a[2 * i + 1]);
+        scale = r.d;
     }
 };
 
 // Q5_0: a chunk is 8 blocks (d f16 | qh u32 | 16 nibble bytes), 256 values
-// at byte 0 of the staged row; unit u is blocks 2u, 2u+1, K-step s0 of it the
-// low (s0 even: values 0..15) or high (s0 odd: values 16..31) nibbles of
-// block 2u + s0/2; bit 4 of value e is bit e of qh.
+// at byte 0 of the staged row.  Warp group g decodes block g in units 0 and 1
+// and block g + 4 in units 2 and 3: the low nibbles (values 0..15) in the
+// even unit, the high ones (values 16..31) in the odd one; bit 4 of value e
+// is bit e of qh.
 template <> struct TcFmt<kQ5_0> {
-    static constexpr int kUPC = 4, kPerm = 1;
-    template <int P, int KH0, int NK>
-    __device__ __forceinline__ static void block(const uint8_t* row, uint32_t* a, float& scale) {
+    static constexpr int kUPC = 4, kPerm = 1, kLastLoad = 2;
+    __host__ __device__ static constexpr int kstep(int u, int g) { return 2 * (g + 4 * (u >> 1)) + (u & 1); }
+    __host__ __device__ static constexpr bool kLoad(int u) { return (u & 1) == 0; }
+    struct Regs {
+        uint32_t qs[4], qh;
+        float d;
+    };
+    template <int P>
+    __device__ __forceinline__ static void block(const uint8_t* row, Regs& r) {
         uint32_t q[6];
-        row_words<P, 6>(row, q);    // d | qh | qs (22 bytes, plus 2)
-        scale = h2f(q[0]);
-        const uint32_t qh = __byte_perm(q[0], q[1], 0x5432);
+        row_words<P, 6>(row, q);  // d | qh | qs (22 bytes, plus 2)
+        r.d = h2f(q[0]);
+        r.qh = __byte_perm(q[0], q[1], 0x5432);
 #pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-            constexpr int dummy = 0;
-            (void)dummy;
-            const int kh = KH0 + kk;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t qs = __byte_perm(q[1 + i], q[2 + i], 0x5432);  // bytes 4i..4i+3 of qs
-                const uint32_t nib = kh ? (qs >> 4) : qs;
-                const uint32_t v = lop_and_or(nib, 0x0F0F0F0Fu, spread4((qh >> (16 * kh + 4 * i)) & 0xFu));
-                codes_bf16(v, 0x001F001Fu, 0x43104310u, a[8 * kk + 2 * i], a[8 * kk + 2 * i + 1]);
-            }
+        for (int i = 0; i < 4; ++i) r.qs[i] = __byte_perm(q[1 + i], q[2 + i], 0x5432);
+    }
+    template <int U>
+    __device__ __forceinline__ static void load(const uint8_t* row, int, int g, Regs& r) {
+        switch (g + 4 * (U >> 1)) {
+        case 0: block<0>(row, r); break;
+        case 1: block<22>(row, r); break;
+        case 2: block<44>(row, r); break;
+        case 3: block<66>(row, r); break;
+        case 4: block<88>(row, r); break;
+        case 5: block<110>(row, r); break;
+        case 6: block<132>(row, r); break;
+        default: block<154>(row, r); break;
         }
     }
-    template <int KPW>
-    __device__ __forceinline__ static void decode(const uint8_t* row, int, int u, int s0, uint32_t (&a)[8 * KPW],
-                                                  float (&scale)[1]) {
-        const int blk = 2 * u + (s0 >> 1);
-#define REM_Q5_CASE(B) \
-        case B: if constexpr (KPW == 1) { if (s0 & 1) block<22 * B, 1, 1>(row, a, scale[0]); else block<22 * B, 0, 1>(row, a, scale[0]); } \
-                else block<22 * B, 0, 2>(row, a, scale[0]); break;
-        switch (blk) {
-            REM_Q5_CASE(0) REM_Q5_CASE(1) REM_Q5_CASE(2) REM_Q5_CASE(3) REM_Q5_CASE(4) REM_Q5_CASE(5) REM_Q5_CASE(6)
-            default: if constexpr (KPW == 1) { if (s0 & 1) block<154, 1, 1>(row, a, scale[0]); else block<154, 0, 1>(row, a, scale[0]); }
-                     else block<154, 0, 2>(row, a, scale[0]);
-                     break;
+    template <int U>
+    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[8], float& scale) {
+        constexpr int kh = U & 1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t nib = kh ? (r.qs[i] >> 4) : r.qs[i];
+            const uint32_t v = lop_and_or(nib, 0x0F0F0F0Fu, spread4((r.qh >> (16 * kh + 4 * i)) & 0xFu));
+            codes_bf16(v, 0x001F001Fu, 0x43104310u, a[2 * i], a[2 * i + 1]);
         }
-#undef REM_Q5_CASE
+        scale = r.d;
     }
 };
 
 // Q6_K: a chunk is one super-block (ql u8[128] | qh u8[64] | sc int8[16] | d
 // f16) at byte o (even, < 16) of the staged window; its K-steps are the 16
-// sub-blocks in order, each one scale block.  Sub-block s = 8h + 2t + g holds
-// values 128h + 32t + 16g + l' (l' < 16): low bits from ql[64h + 32(t&1) +
-// 16g + l'] (the low nibble for t < 2, the high one for t >= 2), high bits
-// 2t, 2t+1 of qh[32h + 16g + l'], scale d * sc[s].  Unit u holds sub-blocks
-// 4u..4u+3 (h = u/2, t = 2(u%2) + s0/2 for its K-step s0): a warp's K-steps
-// s0 .. s0+KPW-1 read ql bytes 64h + 16 s0 on and qh bytes 32h + 16(s0%2) on,
-// both at 16-byte aligned row offsets.
+// sub-blocks in order, each one scale block.  Sub-block s = 8h + 2t + e holds
+// values 128h + 32t + 16e + l (l < 16): low bits from ql[64h + 32(t&1) + 16e
+// + l] (the low nibble for t < 2, the high one for t >= 2), high bits 2t,
+// 2t+1 of qh[32h + 16e + l], scale d * sc[s].  Warp group g = 2h + e decodes
+// sub-block 8h + 2u + e in unit u = t, so the 48 code bytes it loads once
+// (two 16-byte runs of ql, one of qh) serve all four of its units.
 template <> struct TcFmt<kQ6_K> {
-    static constexpr int kUPC = 4, kPerm = 1;
-    template <int O, int KPW>
-    __device__ __forceinline__ static void body(const uint8_t* row, int u, int s0, uint32_t (&a)[8 * KPW],
-                                                float (&scale)[KPW]) {
-        const int h = u >> 1, odd = u & 1, t2 = s0 >> 1;      // t = 2*odd + t2
-        uint32_t ql[4 * KPW], qh[4 * KPW], sc4[4], dw[1];
-        row_words<O, 4 * KPW>(row + 64 * h + 16 * s0, ql);
-        row_words<O + 128, 4 * KPW>(row + 32 * h + 16 * (s0 & 1), qh);
+    static constexpr int kUPC = 4, kPerm = 1, kLastLoad = 0;
+    __host__ __device__ static constexpr int kstep(int u, int g) { return 8 * (g >> 1) + 2 * u + (g & 1); }
+    __host__ __device__ static constexpr bool kLoad(int u) { return u == 0; }
+    struct Regs {
+        uint32_t qa[4], qb[4], qh[4];  // ql for t = 0, 2 and t = 1, 3; qh
+        uint32_t sc0, sc1;             // sc[8h + e + 2t] at bits 0..7 (t = 0, 2) and 16..23 (t = 1, 3)
+        float d;
+    };
+    template <int O>
+    __device__ __forceinline__ static void body(const uint8_t* row, int g, Regs& r) {
+        const int h = g >> 1, e = g & 1;
+        uint32_t sc4[4], dw[1];
+        row_words<O, 4>(row + 64 * h + 16 * e, r.qa);
+        row_words<O + 32, 4>(row + 64 * h + 16 * e, r.qb);
+        row_words<O + 128, 4>(row + 32 * h + 16 * e, r.qh);
         row_words<O + 192, 4>(row, sc4);
         row_words<O + 208, 1>(row, dw);
-        const float d = h2f(dw[0]);
-        const uint32_t scw = (u == 0 ? sc4[0] : u == 1 ? sc4[1] : u == 2 ? sc4[2] : sc4[3]) >> (8 * s0);
-#pragma unroll
-        for (int k = 0; k < KPW; ++k) scale[k] = __fmul_rn(d, k == 0 ? sbyte_f<0>(scw) : sbyte_f<1>(scw));
-        // high bits 2t, 2t+1 of each qh byte -> bits 4, 5: t < 2 shifts left by 4 - 2t, t >= 2 right by 2t - 4
-        if (odd) {
-            const int r = 2 * t2;
-#pragma unroll
-            for (int i = 0; i < 4 * KPW; ++i)
-                codes_bf16(lop_sel(ql[i] >> 4, qh[i] >> r, 0x0F0F0F0Fu), 0x003F003Fu, 0x43204320u, a[2 * i], a[2 * i + 1]);
-        } else {
-            const int l = 4 - 2 * t2;
-#pragma unroll
-            for (int i = 0; i < 4 * KPW; ++i)
-                codes_bf16(lop_sel(ql[i], qh[i] << l, 0x0F0F0F0Fu), 0x003F003Fu, 0x43204320u, a[2 * i], a[2 * i + 1]);
+        r.sc0 = (h ? sc4[2] : sc4[0]) >> (8 * e);
+        r.sc1 = (h ? sc4[3] : sc4[1]) >> (8 * e);
+        r.d = h2f(dw[0]);
+    }
+    template <int U>
+    __device__ __forceinline__ static void load(const uint8_t* row, int o, int g, Regs& r) {
+        switch (o) {
+        case 0: body<0>(row, g, r); break;
+        case 2: body<2>(row, g, r); break;
+        case 4: body<4>(row, g, r); break;
+        case 6: body<6>(row, g, r); break;
+        case 8: body<8>(row, g, r); break;
+        case 10: body<10>(row, g, r); break;
+        case 12: body<12>(row, g, r); break;
+        default: body<14>(row, g, r); break;
         }
     }
-    template <int KPW>
-    __device__ __forceinline__ static void decode(const uint8_t* row, int o, int u, int s0, uint32_t (&a)[8 * KPW],
-                                                  float (&scale)[KPW]) {
-        switch (o) {
-        case 0: body<0, KPW>(row, u, s0, a, scale); break;
-        case 2: body<2, KPW>(row, u, s0, a, scale); break;
-        case 4: body<4, KPW>(row, u, s0, a, scale); break;
-        case 6: body<6, KPW>(row, u, s0, a, scale); break;
-        case 8: body<8, KPW>(row, u, s0, a, scale); break;
-        case 10: body<10, KPW>(row, u, s0, a, scale); break;
-        case 12: body<12, KPW>(row, u, s0, a, scale); break;
-        default: body<14, KPW>(row, u, s0, a, scale); break;
+    template <int U>
+    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[8], float& scale) {
+        const uint32_t scw = U < 2 ? r.sc0 : r.sc1;
+        scale = __fmul_rn(r.d, (U & 1) ? sbyte_f<2>(scw) : sbyte_f<0>(scw));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t ql = (U & 1) ? r.qb[i] : r.qa[i];
+            // high bits 2t, 2t+1 of each qh byte -> bits 4, 5
+            uint32_t v;
+            if constexpr (U < 2) v = lop_sel(ql, r.qh[i] << (4 - 2 * U), 0x0F0F0F0Fu);
+            else v = lop_sel(ql >> 4, r.qh[i] >> (2 * U - 4), 0x0F0F0F0Fu);
+            codes_bf16(v, 0x003F003Fu, 0x43204320u, a[2 * i], a[2 * i + 1]);
         }
     }
 };
@@ -340,6 +364,7 @@ struct TcGeom {
     static constexpr int THREADS = tc_threads(MP);
     static_assert(F::kUPC == tc_units_per_chunk(WT), "units per chunk");
     static_assert(F::kUPC % NS == 0, "units per chunk must be a multiple of the slots");
+    static_assert(KPW == 1 && RK == 1 && RPW == 1, "one K-step and one accumulator region per warp and unit");
     static_assert(NS * (ACOLS + DCOLS) <= TCOLS, "slots exceed the tensor memory");
 };
 
@@ -416,34 +441,31 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
     }
 }
 
-// Scaling of a warp's RPW accumulator regions whose D columns were loaded
-// into d: per region c = D_hi + D_lo for input rows 0..NJ-1 (NJ >= m; the
-// rest of acc stays zero and is never stored) and acc = fma(scale, c, acc),
-// in region order.
-template <int MP, int NCOL, int RPW, int NJ>
-__device__ __forceinline__ void tc_scale_regions(const uint32_t (&d)[RPW][NCOL], const float* sc, float (&acc)[MP]) {
+// One accumulator region of a warp, its D columns loaded into d: c = D_hi +
+// D_lo for input rows 0..NJ-1 (NJ >= m; the rest of acc stays zero and is
+// never stored) and acc = fma(scale, c, acc).  Each column is computed on its
+// own, so skipping the columns past m changes no bit of the others.
+template <int MP, int NJ>
+__device__ __forceinline__ void tc_scale_cols(const uint32_t (&d)[2 * MP], float scale, float (&acc)[MP]) {
 #pragma unroll
-    for (int b = 0; b < RPW; ++b)
-#pragma unroll
-        for (int j = 0; j < NJ; ++j)
-            acc[j] = __fmaf_rn(sc[b * 32], __fadd_rn(__uint_as_float(d[b][j]), __uint_as_float(d[b][MP + j])), acc[j]);
+    for (int j = 0; j < NJ; ++j)
+        acc[j] = __fmaf_rn(scale, __fadd_rn(__uint_as_float(d[j]), __uint_as_float(d[MP + j])), acc[j]);
 }
-template <int MP, int NCOL, int RPW>
-__device__ __forceinline__ void tc_scale(const uint32_t (&d)[RPW][NCOL], const float* sc, uint32_t m, float (&acc)[MP]) {
-    if (m <= 1) tc_scale_regions<MP, NCOL, RPW, 1>(d, sc, acc);
-    else if (m <= 2) tc_scale_regions<MP, NCOL, RPW, 2>(d, sc, acc);
-    else if (m <= 4) tc_scale_regions<MP, NCOL, RPW, 4>(d, sc, acc);
-    else if (MP == 8 || m <= 8) tc_scale_regions<MP, NCOL, RPW, (MP < 8 ? MP : 8)>(d, sc, acc);
-    else if (MP == 16 || m <= 16) tc_scale_regions<MP, NCOL, RPW, (MP < 16 ? MP : 16)>(d, sc, acc);
-    else tc_scale_regions<MP, NCOL, RPW, MP>(d, sc, acc);
+template <int MP>
+__device__ __forceinline__ void tc_scale(const uint32_t (&d)[2 * MP], float scale, uint32_t m, float (&acc)[MP]) {
+    if (m <= 1) tc_scale_cols<MP, 1>(d, scale, acc);
+    else if (m <= 2) tc_scale_cols<MP, 2>(d, scale, acc);
+    else if (m <= 4) tc_scale_cols<MP, 4>(d, scale, acc);
+    else if (MP == 8 || m <= 8) tc_scale_cols<MP, (MP < 8 ? MP : 8)>(d, scale, acc);
+    else tc_scale_cols<MP, MP>(d, scale, acc);
 }
 
 // Persistent kernel: clusters of `split` CTAs walk the 128-row tiles; CTA
 // rank s of a cluster handles K range s of every tile.  Warps 0..CW-1 are
 // consumers: warp w holds rows 32(w%4) .. 32(w%4)+31 of the tile (its TMEM
-// lane quarter) and K-steps KPW*(w/4) .. KPW*(w/4)+KPW-1 of every unit, with
-// their accumulator regions; warp CW is the producer (TMA or plain staging of
-// weights and inputs), warp CW+1 the MMA issuer and owner of the tensor
+// lane quarter) and, as warp group g = w/4, K-step kstep(u, g) of every unit u
+// with its accumulator region; warp CW is the producer (TMA or plain staging
+// of weights and inputs), warp CW+1 the MMA issuer and owner of the tensor
 // memory.  The warps of one lane quarter accumulate separately; at the end of
 // a tile their partials are added in warp-group order.
 template <int WT, int MP>
@@ -451,7 +473,7 @@ __global__ void __launch_bounds__(TcGeom<WT, MP>::THREADS, 1)
 rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
     using G = TcGeom<WT, MP>;
     using F = TcFmt<WT>;
-    constexpr int NS = G::NS, UPC = F::kUPC, KPW = G::KPW, RK = G::RK, RPW = G::RPW;
+    constexpr int NS = G::NS, UPC = F::kUPC;
     constexpr int CV = G::CV, BOX = G::BOX, ROWS = 128;
     constexpr int CW = G::CW, PRODUCER = CW, ISSUER = CW + 1;
     constexpr uint32_t XPAD = (MP * CV * 4 + 127u) & ~127u;
@@ -479,8 +501,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     constexpr uint32_t part_floats = 4u * MP * 32u;
     constexpr uint32_t pair_floats = (G::GROUPS - 1) * part_floats;
     float* parts = pairs;
-    float* scl = pairs + 2 * pair_floats;                                  // [CW][NS][RPW][32] region scales
-    uint64_t* full = reinterpret_cast<uint64_t*>(scl + CW * NS * RPW * 32);
+    uint64_t* full = reinterpret_cast<uint64_t*>(pairs + 2 * pair_floats);
     uint64_t* empty = full + kMaxStages;
     uint64_t* afull = empty + kMaxStages;
     uint64_t* dfull = afull + 4;
@@ -619,29 +640,28 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         for (uint32_t rb = cid; rb < nblocks; rb += ncl, ++t) {
             for (int q = 0; q < nck && !failed; ++q, ++gc) {
                 const uint64_t bchunk = bdesc0 + static_cast<uint64_t>(((gc & 1u) * G::BCHUNK) >> 4);
-#pragma unroll 1
-                for (int u = 0; u < UPC; ++u) {
-                    const int sl = u % NS;
-                    const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(u / NS);
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(ab + 8 * sl, use & 1u, a.wait_ns))) {
+                static_for<0, UPC>([&](auto u_) {
+                    constexpr int U = decltype(u_)::value, SL = U % NS;
+                    if (failed) return;
+                    const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(U / NS);
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(ab + 8 * SL, use & 1u, a.wait_ns))) {
                         if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
                         failed = true;
-                        break;
+                        return;
                     }
                     tc_fence_after();
-                    const uint32_t ac = tmem + static_cast<uint32_t>(sl * G::ACOLS);
-                    const uint32_t dc = tmem + static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS);
-                    const uint64_t bu = bchunk + static_cast<uint64_t>((4 * u * G::BKSTEP) >> 4);
+                    const uint32_t ac = tmem + static_cast<uint32_t>(SL * G::ACOLS);
+                    const uint32_t dc = tmem + static_cast<uint32_t>(NS * G::ACOLS + SL * G::DCOLS);
                     if (lane == 0) {
 #pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            tc_mma(dc + static_cast<uint32_t>((k4 / RK) * G::NCOL), ac + 8u * k4,
-                                   bu + static_cast<uint64_t>((k4 * G::BKSTEP) >> 4), idesc, (k4 % RK) != 0);
-                        tc_commit(db + 8 * sl);
+                        for (int g = 0; g < 4; ++g)
+                            tc_mma(dc + static_cast<uint32_t>(g * G::NCOL), ac + 8u * g,
+                                   bchunk + static_cast<uint64_t>((F::kstep(U, g) * G::BKSTEP) >> 4), idesc, false);
+                        tc_commit(db + 8 * SL);
                     }
                     __syncwarp();
                     issued_any = true;
-                }
+                });
             }
             if (S > 1) {
                 if (t > 0) cluster_wait();
@@ -664,9 +684,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 
     // ---------------------------------------------------- consumers
     const int quarter = warp & 3, grp = warp >> 2;
-    const int s0 = grp * KPW;                                              // this warp's first K-step of a unit
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;  // this warp's TMEM lanes
-    float* myscl = scl + warp * (NS * RPW * 32) + lane;                   // [NS][RPW] scales of this lane
     bool failed = false;
     uint32_t i = 0;   // stages consumed
     uint32_t gc = 0;  // chunks over all tiles
@@ -677,6 +695,9 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         float acc[MP];
 #pragma unroll
         for (int j = 0; j < MP; ++j) acc[j] = 0.0f;
+        float psc[NS];  // scales of the units in flight, by slot
+#pragma unroll
+        for (int j = 0; j < NS; ++j) psc[j] = 0.0f;
         // the slot's MMAs (use number `use`) have completed: its D is ready, its A is free
         auto wait_d = [&](int sl, uint32_t use) {
             if (failed) return;
@@ -687,11 +708,8 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             }
             tc_fence_after();
         };
-        auto load_d = [&](int sl, uint32_t (&d)[RPW][G::NCOL]) {
-            const uint32_t dc = tmem + lane_base +
-                                static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS + (s0 / RK) * G::NCOL);
-#pragma unroll
-            for (int bb = 0; bb < RPW; ++bb) tmem_ld<G::NCOL>(dc + static_cast<uint32_t>(bb * G::NCOL), d[bb]);
+        auto load_d = [&](int sl, uint32_t (&d)[G::NCOL]) {
+            tmem_ld<G::NCOL>(tmem + lane_base + static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS + grp * G::NCOL), d);
         };
         for (int q = 0; q < nck; ++q, ++i, ++gc) {
             const int st = static_cast<int>(i % D);
@@ -710,51 +728,52 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             const uint8_t* row = sp + (quarter * 32 + lane) * BOX;
             const int o = Stage<WT>::sofs(c0 + static_cast<uint32_t>(q));
-#pragma unroll 1
-            for (int u = 0; u < UPC; ++u) {
-                const int sl = u % NS;
-                const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(u / NS);
-                const bool pending = q > 0 || u >= NS;   // slot sl holds an earlier unit of this tile
-                // up to 8 input rows the old unit's D is loaded before this
-                // unit decodes (the load's latency hides behind the decode);
-                // wider tiles load it after, to keep the registers in bounds
-                constexpr bool early = MP <= 8;
-                uint32_t d[RPW][G::NCOL];
-                if (pending) {
-                    wait_d(sl, use - 1u);
-                    if (failed) break;
-                    if constexpr (early) load_d(sl, d);
+            typename F::Regs R;
+            static_for<0, UPC>([&](auto u_) {
+                constexpr int U = decltype(u_)::value, SL = U % NS;
+                if (failed) return;
+                if constexpr (F::kLoad(U)) F::template load<U>(row, o, grp, R);
+                if constexpr (U == F::kLastLoad) {
+                    // the staged weights and inputs of this chunk are all read
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(eb + 8 * st);
                 }
-                uint32_t av[8 * KPW];
-                float nsc[RPW];
-                F::template decode<KPW>(row, o, u, s0, av, nsc);
-                tmem_st_cols<KPW>(tmem + lane_base + static_cast<uint32_t>(sl * G::ACOLS + 8 * s0), av);
+                const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(U / NS);
+                const bool pending = q > 0 || U >= NS;  // slot SL holds an earlier unit of this tile
+                // the old unit's D is read after this unit's codes are
+                // stored, so the decode does not hold its registers
                 if (pending) {
-                    if constexpr (!early) load_d(sl, d);
+                    wait_d(SL, use - 1u);
+                    if (failed) return;
+                }
+                uint32_t av[8];
+                float nsc;
+                F::template decode<U>(R, av, nsc);
+                tmem_st_cols<1>(tmem + lane_base + static_cast<uint32_t>(SL * G::ACOLS + 8 * grp), av);
+                if (pending) {
+                    uint32_t d[G::NCOL];
+                    load_d(SL, d);
                     tmem_ld_wait();
-                    tc_scale<MP, G::NCOL, RPW>(d, myscl + sl * (RPW * 32), m, acc);
+                    tc_scale<MP>(d, psc[SL], m, acc);
                 }
-#pragma unroll
-                for (int bb = 0; bb < RPW; ++bb) myscl[sl * (RPW * 32) + bb * 32] = nsc[bb];
+                psc[SL] = nsc;
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(ab + 8 * sl);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(eb + 8 * st);
+                if (lane == 0) mbar_arrive(ab + 8 * SL);
+            });
         }
         // drain: the last unit of every slot
         if (nck > 0) {
-#pragma unroll 1
-            for (int sl = 0; sl < NS; ++sl) {
-                wait_d(sl, (gc - 1u) * (UPC / NS) + static_cast<uint32_t>((UPC - NS + sl) / NS));
-                if (failed) break;
-                uint32_t d[RPW][G::NCOL];
-                load_d(sl, d);
+            static_for<0, NS>([&](auto s_) {
+                constexpr int SL = decltype(s_)::value;
+                wait_d(SL, (gc - 1u) * (UPC / NS) + static_cast<uint32_t>((UPC - NS + SL) / NS));
+                if (failed) return;
+                uint32_t d[G::NCOL];
+                load_d(SL, d);
                 tmem_ld_wait();
-                tc_scale<MP, G::NCOL, RPW>(d, myscl + sl * (RPW * 32), m, acc);
-            }
+                tc_scale<MP>(d, psc[SL], m, acc);
+            });
         }
         // the other warp groups' partials join group 0's, in group order
         float* pb = pairs + (t & 1u) * pair_floats;
