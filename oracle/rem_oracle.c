@@ -545,24 +545,37 @@ int rem_oracle_matvec_rows(const uint8_t* w, int wtype, uint32_t n, uint32_t k,
 /* ------------------------------------------------------------------ */
 /* Affine quantization (nuvec-core 0.6.0 src/gpu.rs: Quantize /         */
 /* Dequantize / QuantizedMatmul in QuantMode::Affine with (group_size,  */
-/* bits), and pack_factor: 32/bits codes per 32-bit word for 4 and 8    */
-/* bits).  The pages give no element formula or layout; the reading:    */
-/*   codes   rows x (k*bits/32) uint32 words; code i of a row sits at   */
-/*           bits [bits*(i % (32/bits)), +bits) of word i / (32/bits)   */
-/*           (lowest bits first);                                       */
+/* bits), and pack_factor: values per packing unit -- 8 for 3 and 5     */
+/* bits, 4 for 6 bits, 32/bits for 4 and 8 bits -- so a packing unit is */
+/* a whole number of bytes (3, 5, 3, 4, 4).  The pages give no element  */
+/* formula or bit order; the reading:                                   */
+/*   codes   rows x (k*bits/32) uint32 words, little-endian: a row's    */
+/*           codes are one bit stream, byte j holding stream bits       */
+/*           8j .. 8j+7 (bit 0 lowest), and code i occupies stream bits */
+/*           [bits*i, bits*i + bits), lowest bit first (for 4 and 8     */
+/*           bits: word i / (32/bits), bits bits*(i % (32/bits)));      */
 /*   scales, biases  rows x (k/group_size) binary16, one per group;     */
 /*   w = fl(fl(scale*q) + bias), the product rounded, then the add.     */
 /* ------------------------------------------------------------------ */
 
 static int affine_ok(int bits, int gs, uint32_t k) {
-    return (bits == 4 || bits == 8) && (gs == 32 || gs == 64 || gs == 128) && k > 0 && k % (uint32_t)gs == 0;
+    return (bits == 3 || bits == 4 || bits == 5 || bits == 6 || bits == 8) && (gs == 32 || gs == 64 || gs == 128) &&
+           k > 0 && k % (uint32_t)gs == 0;
+}
+
+/* Code i of a row whose code bytes (k*bits/8 of them) start at cb. */
+static uint32_t affine_code(const uint8_t* cb, int bits, uint32_t k, uint32_t i) {
+    const uint64_t bit = (uint64_t)bits * i, nbytes = (uint64_t)k * (uint64_t)bits / 8;
+    uint32_t v = cb[bit / 8];
+    if (bit / 8 + 1 < nbytes) v |= (uint32_t)cb[bit / 8 + 1] << 8;
+    return (v >> (bit % 8)) & ((1u << bits) - 1u);
 }
 
 static void deq_affine_row(const uint32_t* codes, const uint16_t* sc, const uint16_t* bi, int bits, int gs,
                            uint32_t k, float* out) {
-    const uint32_t per = 32u / (uint32_t)bits, mask = (1u << bits) - 1u;
+    const uint8_t* cb = (const uint8_t*)codes;
     for (uint32_t i = 0; i < k; ++i) {
-        uint32_t q = (codes[i / per] >> (bits * (i % per))) & mask;
+        uint32_t q = affine_code(cb, bits, k, i);
         float s = rem_oracle_h2f(sc[i / (uint32_t)gs]), b = rem_oracle_h2f(bi[i / (uint32_t)gs]);
         float p = s * (float)q;
         out[i] = p + b;
@@ -586,11 +599,12 @@ int rem_oracle_affine_dequantize(const uint32_t* codes, const uint16_t* scales, 
 int rem_oracle_affine_quantize(const float* src, int bits, int gs, uint32_t rows, uint32_t k, uint32_t* codes,
                                uint16_t* scales, uint16_t* biases) {
     if (!affine_ok(bits, gs, k)) return -1;
-    const uint32_t per = 32u / (uint32_t)bits, qmax = (1u << bits) - 1u;
+    const uint32_t qmax = (1u << bits) - 1u;
     const uint64_t cw = (uint64_t)k * bits / 32, ng = k / (uint32_t)gs;
     for (uint32_t r = 0; r < rows; ++r) {
         const float* v = src + (uint64_t)r * k;
         uint32_t* cr = codes + r * cw;
+        uint8_t* cb = (uint8_t*)cr;
         for (uint64_t w = 0; w < cw; ++w) cr[w] = 0;
         for (uint64_t g = 0; g < ng; ++g) {
             const float* vg = v + g * gs;
@@ -610,8 +624,11 @@ int rem_oracle_affine_quantize(const float* src, int bits, int gs, uint32_t rows
                     if (q < 0) q = 0;
                     if (q > (long)qmax) q = (long)qmax;
                 }
-                uint64_t i = g * gs + (uint64_t)e;
-                cr[i / per] |= (uint32_t)q << (bits * (i % per));
+                /* code i -> stream bits [bits*i, bits*i + bits) */
+                uint64_t bit = (g * gs + (uint64_t)e) * (uint64_t)bits;
+                uint32_t sh = (uint32_t)q << (bit % 8);
+                cb[bit / 8] |= (uint8_t)(sh & 0xFFu);
+                if (sh >> 8) cb[bit / 8 + 1] |= (uint8_t)(sh >> 8);
             }
         }
     }

@@ -438,7 +438,47 @@ def test_affine_decode_hand_derived(orc, bits, gs, k, codes_at, scales, biases, 
         assert got[i] == np.float32(expect.get(i, base)), (i, got[i])
 
 
-@pytest.mark.parametrize("bits,gs", [(4, 32), (4, 64), (4, 128), (8, 32), (8, 64), (8, 128)])
+def _affine_bytes_case(bits, k, byte_map):
+    """Codes of one row from explicit byte values {byte index: value}; the
+    row's uint32 words are those bytes read little-endian."""
+    b = np.zeros(k * bits // 8, dtype=np.uint8)
+    for j, v in byte_map.items():
+        b[j] = v
+    return b.view("<u4").astype(np.uint32).reshape(1, -1)
+
+
+@pytest.mark.parametrize("bits,gs,k,byte_map,scales,biases,expect", [
+    # 3 bits, 8 codes per 3-byte packing unit; code i at stream bits 3i .. 3i+2
+    (3, 32, 32, {0: 0x05}, [0x3C00], [0x0000], {0: 5.0}),                 # bits 0-2 = 101
+    (3, 32, 32, {0: 0xC0, 1: 0x01}, [0x3C00], [0x0000], {2: 7.0}),        # bits 6, 7 | 8
+    (3, 32, 32, {2: 0x80}, [0x3C00], [0x0000], {7: 4.0}),                 # bit 23 = top bit of code 7
+    (3, 32, 32, {3: 0x03}, [0x3C00], [0x0000], {8: 3.0}),                 # second unit starts at byte 3
+    (3, 32, 32, {3: 0x80, 4: 0x01}, [0x3C00], [0x0000], {10: 6.0}),       # bits 30 (0), 31 (1), 32 (1)
+    (3, 32, 32, {11: 0xE0}, [0x3C00], [0x0000], {31: 7.0}),               # bits 93-95
+    # 5 bits, 8 codes per 5-byte unit
+    (5, 32, 32, {0: 0xE0, 1: 0x03}, [0x3C00], [0x0000], {1: 31.0}),       # bits 5-9
+    (5, 32, 32, {4: 0x88}, [0x3C00], [0x0000], {7: 17.0}),                # bits 35 and 39 of 35-39
+    (5, 32, 32, {5: 0x01}, [0x3800], [0xC000], {8: -1.5}),                # 0.5*1 - 2, the rest -2
+    (5, 32, 32, {19: 0xF8}, [0x3C00], [0x0000], {31: 31.0}),              # bits 155-159
+    # 6 bits, 4 codes per 3-byte unit
+    (6, 32, 32, {0: 0xC0, 1: 0x0F}, [0x3C00], [0x0000], {1: 63.0}),       # bits 6-11
+    (6, 32, 32, {2: 0x84}, [0x3C00], [0x0000], {3: 33.0}),                # bits 18 and 23 of 18-23
+    (6, 32, 32, {3: 0x02}, [0x3C00], [0x0000], {4: 2.0}),                 # second unit starts at byte 3
+    (6, 32, 32, {4: 0x0C}, [0x3C00], [0x0000], {5: 48.0}),                # bits 34, 35 of 30-35
+    (6, 32, 32, {23: 0xFC}, [0x3C00], [0x0000], {31: 63.0}),              # bits 186-191
+    (6, 32, 64, {30: 0x21}, [0x3C00, 0x4000], [0x0000, 0x3C00], {40: 67.0}),   # group 1: 2*33 + 1
+])
+def test_affine_decode_hand_derived_bytes(orc, bits, gs, k, byte_map, scales, biases, expect):
+    codes = _affine_bytes_case(bits, k, byte_map)
+    sc = np.array([scales], dtype=np.uint16).reshape(1, -1)
+    bi = np.array([biases], dtype=np.uint16).reshape(1, -1)
+    got = orc.affine_dequantize(codes, sc, bi, bits, gs, 1, k)[0]
+    for i in range(k):
+        base = float(orc.h2f(np.array([biases[i // gs]], np.uint16))[0])
+        assert got[i] == np.float32(expect.get(i, base)), (i, got[i])
+
+
+@pytest.mark.parametrize("bits,gs", [(b, g) for b in (3, 4, 5, 6, 8) for g in (32, 64, 128)])
 def test_affine_round_trip_bound(orc, bits, gs):
     k, rows = 512, 6
     v = inputs.weights(rows, k, 60)
@@ -455,7 +495,7 @@ def test_affine_round_trip_bound(orc, bits, gs):
     assert np.all(err <= bound)
 
 
-@pytest.mark.parametrize("bits,gs", [(4, 64), (8, 32)])
+@pytest.mark.parametrize("bits,gs", [(4, 64), (8, 32), (3, 32), (5, 128), (6, 64)])
 def test_affine_brute_force_rational(orc, bits, gs):
     n, k, m = 3, 128, 4
     c, s, b = orc.affine_quantize(inputs.weights(n, k, 61), bits, gs)
