@@ -56,6 +56,8 @@ WORKLOADS = {
     "a4_g64_n14336_k4096_m1-8": ("a4_g64", 14336, 4096, 1, list(range(1, 9)), False, 13),
     # fused epilogue y = W.x + bias (rem_matvec_axpby, one bias vector for all rows)
     "q8_0_n4096_k4096_m1-8_bias": ("q8_0", 4096, 4096, 1, list(range(1, 9)), False, 10),
+    # profiling size of the Q6_K path: 215 MB of weights (above the L2), for ncu captures
+    "q6_K_n65536_k4096_m1,8": ("q6_K", 65536, 4096, 1, [1, 8], False, 16),
 }
 # workloads that run the epilogue alpha * W.x + beta * c with c a bias vector
 EPILOGUE = {"q8_0_n4096_k4096_m1-8_bias": (1.0, 1.0)}

@@ -276,9 +276,11 @@ int rem_set_thread_schedule(const rem_schedule* sched);
 
 /*
  * rem_engine_of -- the engine the default schedule uses for `rows`
- * (= batch*n) weight rows of k elements: REM_ENGINE_TC for Q8_0, Q5_0 and
- * Q6_K, REM_ENGINE_SIMT otherwise; -1 for an unknown wtype or rows == 0 or
- * k == 0.  Host only; makes no CUDA call.
+ * (= batch*n) weight rows of k elements: REM_ENGINE_TC for Q6_K (whose
+ * sub-block decode is the costliest on the FP32 pipe), REM_ENGINE_SIMT
+ * otherwise (Q8_0 and Q5_0 take the tensor-core engine only when a schedule
+ * asks for it); -1 for an unknown wtype or rows == 0 or k == 0.  Host only;
+ * makes no CUDA call.
  */
 int rem_engine_of(int wtype, uint32_t rows, uint32_t k);
 

@@ -326,12 +326,16 @@ uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
 }
 
 // The engine (and with it the arithmetic) of a weight shape: the tensor-core
-// kernel for the block-scaled formats, the lanes-over-rows kernel otherwise.
-// Like the split, it depends on (wtype, rows, k) only.
+// kernel for Q6_K, the lanes-over-rows kernel otherwise.  Q6_K's sub-block
+// decode is what limits the lanes-over-rows kernel from m = 2 up (at 128256 x
+// 4096 it takes 107, 271 and 512 us at m = 1, 4 and 8 against 192, 202 and
+// 214 us on the tensor cores); for Q8_0 and Q5_0 the lanes-over-rows kernel
+// is as fast or faster at m = 8 and well ahead at m = 1.  Like the split, it
+// depends on (wtype, rows, k) only.
 int auto_engine(int wt, uint64_t rows, uint32_t k) {
     (void)rows;
     (void)k;
-    return tc_format(wt) ? REM_ENGINE_TC : REM_ENGINE_SIMT;
+    return wt == kQ6_K ? REM_ENGINE_TC : REM_ENGINE_SIMT;
 }
 
 // Input rows one launch of an engine takes.

@@ -212,7 +212,8 @@ def test_affine_types_need_the_affine_entry(lib):
 
 
 @pytest.mark.parametrize("wt,rows,k,expect", [
-    ("q6_K", 128256, 4096, rem.ENGINE_TC), ("q8_0", 4096, 4096, rem.ENGINE_TC), ("q5_0", 16384, 4096, rem.ENGINE_TC),
+    ("q6_K", 128256, 4096, rem.ENGINE_TC), ("q6_K", 256, 512, rem.ENGINE_TC), ("q8_0", 4096, 4096, rem.ENGINE_SIMT),
+    ("q5_0", 16384, 4096, rem.ENGINE_SIMT),
     ("q4_K", 14336, 4096, rem.ENGINE_SIMT), ("f16", 256, 512, rem.ENGINE_SIMT), ("bf16", 64, 256, rem.ENGINE_SIMT),
     ("f32", 64, 256, rem.ENGINE_SIMT), (rem.A4_G64, 64, 256, rem.ENGINE_SIMT),
 ])

@@ -312,17 +312,23 @@ def test_tc_many_rows_one_pass_per_group(fmt):
     rows, each row bitwise the row of an m = 1 call."""
     n, k, m = 130, 512, 40
     w, x = H.contiguous(fmt, n, k, m, 762, 763)
-    assert rem.rem_engine_of(fmt, n, k) == rem.ENGINE_TC
-    wh, wp = H.to_dev_bytes(w)
-    xd = H.to_dev_f32(x)
-    yd = H.canary(m * n + 16)
-    rem.check(rem.rem_matvec_many(wp, fmt, n, k, 1, xd, m, k, 0, yd, n, 0, 0))
-    torch.cuda.synchronize()
-    y = yd.cpu().numpy()
-    assert np.all(y[m * n:] == H.CANARY)
-    y = y[:m * n].reshape(m, n)
-    y_ref, a_ref = oracle.matvec(w, fmt, n, k, 1, x, m, k, 0)
-    H.assert_close_to_oracle(y[None], y_ref, a_ref, f"{fmt} many")
-    for j in (0, 17, 39):
-        one = H.run_matvec(w, fmt, n, k, 1, x[j:j + 1], 1, k, 0, n, 0, n, use_ex=False)
-        assert np.array_equal(y[j].view(np.uint32), one.view(np.uint32)), j
+    # the thread's default schedule takes every call of this test to the
+    # tensor cores (Q6_K goes there by default; Q8_0 and Q5_0 on request)
+    rem.check(rem.rem_set_thread_schedule(rem.Schedule(engine=rem.ENGINE_TC)))
+    try:
+        wh, wp = H.to_dev_bytes(w)
+        xd = H.to_dev_f32(x)
+        yd = H.canary(m * n + 16)
+        rem.check(rem.rem_matvec_many(wp, fmt, n, k, 1, xd, m, k, 0, yd, n, 0, 0))
+        torch.cuda.synchronize()
+        assert "engine=tc" in rem.rem_last_plan()
+        y = yd.cpu().numpy()
+        assert np.all(y[m * n:] == H.CANARY)
+        y = y[:m * n].reshape(m, n)
+        y_ref, a_ref = oracle.matvec(w, fmt, n, k, 1, x, m, k, 0)
+        H.assert_close_to_oracle(y[None], y_ref, a_ref, f"{fmt} many")
+        for j in (0, 17, 39):
+            one = H.run_matvec(w, fmt, n, k, 1, x[j:j + 1], 1, k, 0, n, 0, n, use_ex=False)
+            assert np.array_equal(y[j].view(np.uint32), one.view(np.uint32)), j
+    finally:
+        rem.check(rem.rem_set_thread_schedule(None))
