@@ -72,11 +72,16 @@ typedef enum {
     REM_BF16 = 6,  /* row-major [batch*n, k] bfloat16 (upper half of binary32) */
     /* affine group quantization (the Affine mode of nuvec-core 0.6.0
        src/gpu.rs, with (group_size, bits) and pack_factor): codes
-       [batch*n, k*bits/32] uint32 words, lowest bits first; scales and biases
-       [batch*n, k/group] binary16 in their own arrays; w = scale*q + bias.
-       Only through rem_matvec_affine / rem_dequantize_affine.           */
-    REM_A4_G32 = 7, REM_A4_G64 = 8, REM_A4_G128 = 9,   /* 4-bit codes  */
-    REM_A8_G32 = 10, REM_A8_G64 = 11, REM_A8_G128 = 12 /* 8-bit codes  */
+       [batch*n, k*bits/32] uint32 words holding one little-endian bit
+       stream per row, code i at stream bits [bits*i, bits*i + bits), lowest
+       first; scales and biases [batch*n, k/group] binary16 in their own
+       arrays; w = scale*q + bias.  Only through rem_matvec_affine /
+       rem_dequantize_affine.                                             */
+    REM_A4_G32 = 7, REM_A4_G64 = 8, REM_A4_G128 = 9,    /* 4-bit codes */
+    REM_A8_G32 = 10, REM_A8_G64 = 11, REM_A8_G128 = 12, /* 8-bit codes */
+    REM_A3_G32 = 13, REM_A3_G64 = 14, REM_A3_G128 = 15, /* 3-bit codes, 8 per 3-byte packing unit */
+    REM_A5_G32 = 16, REM_A5_G64 = 17, REM_A5_G128 = 18, /* 5-bit codes, 8 per 5-byte packing unit */
+    REM_A6_G32 = 19, REM_A6_G64 = 20, REM_A6_G128 = 21  /* 6-bit codes, 4 per 3-byte packing unit */
 } rem_wtype;
 
 /* Status codes. */
@@ -206,15 +211,19 @@ int rem_matvec_axpby(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t 
  * rem_matvec_affine -- y[b, j, :] = W[b] . x[b, j, :] for affine group-quantized
  * W (next step 2 of the few-row path: the Affine quantized matmul of nuvec-core
  * 0.6.0 src/gpu.rs).  The page fixes the (group_size, bits) parameters and the
- * packing factor (32/bits codes per 32-bit word for 4 and 8 bits); the
+ * packing factor (pack_factor: 8 codes per packing unit for 3 and 5 bits, 4
+ * for 6 bits, 32/bits for 4 and 8 bits, so every unit is whole bytes); the
  * element formula and layout are the plain reading of that mode:
- *   codes    batch*n rows of k*bits/32 uint32 words; code i of a row at bits
- *            [bits*(i % (32/bits)), +bits) of word i / (32/bits); 4-byte
- *            aligned (16-byte aligned rows use TMA staging)
+ *   codes    batch*n rows of k*bits/32 uint32 words, little-endian; a row's
+ *            codes are one bit stream (byte j = stream bits 8j .. 8j+7) and
+ *            code i sits at stream bits [bits*i, bits*i + bits), lowest bit
+ *            first (for 4 and 8 bits: bits [bits*(i % (32/bits)), +bits) of
+ *            word i / (32/bits)); 4-byte aligned (16-byte aligned rows use
+ *            TMA staging)
  *   scales, biases   batch*n rows of k/group binary16 values, 2-byte aligned
  *   w[r, i] = fl(fl(scale[r, i/group] * q) + bias[r, i/group])
- * wtype is one of REM_A4_G32 .. REM_A8_G128; k must be a multiple of the group
- * size.  Other arguments as rem_matvec_ex (split 0 = automatic).  Row
+ * wtype is one of REM_A4_G32 .. REM_A6_G128; k must be a multiple of the
+ * group size.  Other arguments as rem_matvec_ex (split 0 = automatic).  Row
  * exactness holds as for the other formats.
  */
 int rem_matvec_affine(const void* codes, const uint16_t* scales, const uint16_t* biases, int wtype,

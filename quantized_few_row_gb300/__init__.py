@@ -18,7 +18,8 @@ import os
 
 __all__ = [
     "F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16", "A4_G32", "A4_G64", "A4_G128", "A8_G32", "A8_G64",
-    "A8_G128", "WTYPES", "affine_wtype", "rem_matvec_affine", "rem_dequantize_affine", "REM_OK", "REM_EINVAL", "REM_ELAUNCH", "REM_ECUDA",
+    "A8_G128", "A3_G32", "A3_G64", "A3_G128", "A5_G32", "A5_G64", "A5_G128", "A6_G32", "A6_G64", "A6_G128",
+    "WTYPES", "affine_wtype", "rem_matvec_affine", "rem_dequantize_affine", "REM_OK", "REM_EINVAL", "REM_ELAUNCH", "REM_ECUDA",
     "RemError", "build", "library_path", "load", "rem_matvec", "rem_matvec_ex", "rem_matvec_many",
     "rem_matvec_axpby", "rem_row_bytes",
     "rem_split_factor", "rem_dequantize", "rem_quantize", "rem_last_error", "rem_version", "check",
@@ -28,9 +29,11 @@ __all__ = [
 
 F16, Q8_0, Q4_K, Q6_K, Q5_0, F32, BF16 = 0, 1, 2, 3, 4, 5, 6
 A4_G32, A4_G64, A4_G128, A8_G32, A8_G64, A8_G128 = 7, 8, 9, 10, 11, 12
+A3_G32, A3_G64, A3_G128, A5_G32, A5_G64, A5_G128, A6_G32, A6_G64, A6_G128 = 13, 14, 15, 16, 17, 18, 19, 20, 21
 WTYPES = {"f16": F16, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q5_0": Q5_0, "f32": F32, "bf16": BF16,
           "a4_g32": A4_G32, "a4_g64": A4_G64, "a4_g128": A4_G128, "a8_g32": A8_G32, "a8_g64": A8_G64,
-          "a8_g128": A8_G128}
+          "a8_g128": A8_G128, "a3_g32": A3_G32, "a3_g64": A3_G64, "a3_g128": A3_G128, "a5_g32": A5_G32,
+          "a5_g64": A5_G64, "a5_g128": A5_G128, "a6_g32": A6_G32, "a6_g64": A6_G64, "a6_g128": A6_G128}
 
 
 def affine_wtype(bits: int, group_size: int) -> int:

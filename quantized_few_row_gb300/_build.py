@@ -16,7 +16,9 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "librem.so")
 BUILD = os.path.join(PKG, "_build")
 SOURCES = ["rem_host.cu", "rem_aux.cu", "rem_tc_q8_0.cu", "rem_tc_q5_0.cu", "rem_tc_q6_k.cu"] + [f"rem_mv_{f}_{p}.cu" for f in ("f16", "q8_0", "q5_0", "q4_k", "q6_k", "f32", "bf16", "a4g32", "a4g64",
-                                                      "a4g128", "a8g32", "a8g64", "a8g128")
+                                                      "a4g128", "a8g32", "a8g64", "a8g128", "a3g32", "a3g64",
+                                                      "a3g128", "a5g32", "a5g64", "a5g128", "a6g32", "a6g64",
+                                                      "a6g128")
                                             for p in ("a", "b")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

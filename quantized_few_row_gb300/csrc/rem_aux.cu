@@ -283,7 +283,8 @@ __global__ void quant_kernel(const float* __restrict__ src, int wt, uint64_t row
     }
 }
 
-// Affine: one thread per group; w = fl(fl(scale * q) + bias), codes lowest-first in 32-bit words.
+// Affine: one thread per group; w = fl(fl(scale * q) + bias); a row's codes
+// are one little-endian bit stream, code i at bits [bits*i, bits*i + bits).
 __global__ void dequant_affine_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
                                       const uint16_t* __restrict__ biases, int bits, int gs, uint64_t rows,
                                       uint32_t k, float* __restrict__ out) {
@@ -291,12 +292,15 @@ __global__ void dequant_affine_kernel(const uint32_t* __restrict__ codes, const 
     const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (tid >= rows * ng) return;
     const uint64_t r = tid / ng, g = tid - r * ng;
-    const uint32_t per = 32u / static_cast<uint32_t>(bits), mask = (1u << bits) - 1u;
-    const uint32_t* cr = codes + r * (static_cast<uint64_t>(k) * bits / 32u);
+    const uint32_t mask = (1u << bits) - 1u;
+    const uint64_t nbytes = static_cast<uint64_t>(k) * bits / 8u;
+    const uint8_t* cb = reinterpret_cast<const uint8_t*>(codes) + r * nbytes;
     const float sc = h2f(scales[tid]), bi = h2f(biases[tid]);
     for (int e = 0; e < gs; ++e) {
-        const uint64_t i = g * gs + e;
-        const uint32_t q = (cr[i / per] >> (bits * (i % per))) & mask;
+        const uint64_t i = g * gs + e, bit = i * static_cast<uint64_t>(bits);
+        uint32_t v = cb[bit / 8];
+        if (bit / 8 + 1 < nbytes) v |= static_cast<uint32_t>(cb[bit / 8 + 1]) << 8;
+        const uint32_t q = (v >> (bit % 8)) & mask;
         out[r * k + i] = __fadd_rn(__fmul_rn(sc, static_cast<float>(q)), bi);
     }
 }

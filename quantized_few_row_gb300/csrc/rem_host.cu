@@ -40,8 +40,10 @@ int fail(int code, const char* fmt, ...) {
 bool valid_wt(int wt) { return wt >= 0 && wt < kNumWt; }
 
 const char* wt_name(int wt) {
-    static const char* names[] = {"F16", "Q8_0", "Q4_K", "Q6_K", "Q5_0", "F32", "BF16", "A4G32", "A4G64",
-                                  "A4G128", "A8G32", "A8G64", "A8G128"};
+    static const char* names[] = {"F16",   "Q8_0",  "Q4_K",  "Q6_K",   "Q5_0",  "F32",   "BF16",  "A4G32",
+                                  "A4G64", "A4G128", "A8G32", "A8G64", "A8G128", "A3G32", "A3G64", "A3G128",
+                                  "A5G32", "A5G64",  "A5G128", "A6G32", "A6G64", "A6G128"};
+    static_assert(sizeof(names) / sizeof(names[0]) == kNumWt, "one name per weight type");
     return valid_wt(wt) ? names[wt] : "?";
 }
 
@@ -887,6 +889,15 @@ const void* mv_kernel(int wt, int m, int layout) {
     case kA8G32: return lo ? mv_kernel_a8g32_a(m, layout) : mv_kernel_a8g32_b(m, layout);
     case kA8G64: return lo ? mv_kernel_a8g64_a(m, layout) : mv_kernel_a8g64_b(m, layout);
     case kA8G128: return lo ? mv_kernel_a8g128_a(m, layout) : mv_kernel_a8g128_b(m, layout);
+    case kA3G32: return lo ? mv_kernel_a3g32_a(m, layout) : mv_kernel_a3g32_b(m, layout);
+    case kA3G64: return lo ? mv_kernel_a3g64_a(m, layout) : mv_kernel_a3g64_b(m, layout);
+    case kA3G128: return lo ? mv_kernel_a3g128_a(m, layout) : mv_kernel_a3g128_b(m, layout);
+    case kA5G32: return lo ? mv_kernel_a5g32_a(m, layout) : mv_kernel_a5g32_b(m, layout);
+    case kA5G64: return lo ? mv_kernel_a5g64_a(m, layout) : mv_kernel_a5g64_b(m, layout);
+    case kA5G128: return lo ? mv_kernel_a5g128_a(m, layout) : mv_kernel_a5g128_b(m, layout);
+    case kA6G32: return lo ? mv_kernel_a6g32_a(m, layout) : mv_kernel_a6g32_b(m, layout);
+    case kA6G64: return lo ? mv_kernel_a6g64_a(m, layout) : mv_kernel_a6g64_b(m, layout);
+    case kA6G128: return lo ? mv_kernel_a6g128_a(m, layout) : mv_kernel_a6g128_b(m, layout);
     default: return nullptr;
     }
 }

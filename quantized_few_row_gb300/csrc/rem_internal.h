@@ -9,14 +9,22 @@ namespace rem {
 
 enum Wt : int {
     kF16 = 0, kQ8_0 = 1, kQ4_K = 2, kQ6_K = 3, kQ5_0 = 4, kF32 = 5, kBF16 = 6,
-    // affine group quantization: 4- or 8-bit codes, binary16 scale and bias per group of 32/64/128
+    // affine group quantization: 3-, 4-, 5-, 6- or 8-bit codes, binary16 scale and bias per group of
+    // 32/64/128 values
     kA4G32 = 7, kA4G64 = 8, kA4G128 = 9, kA8G32 = 10, kA8G64 = 11, kA8G128 = 12,
-    kNumWt = 13
+    kA3G32 = 13, kA3G64 = 14, kA3G128 = 15, kA5G32 = 16, kA5G64 = 17, kA5G128 = 18,
+    kA6G32 = 19, kA6G64 = 20, kA6G128 = 21,
+    kNumWt = 22
 };
-__host__ __device__ constexpr bool is_affine(int wt) { return wt >= kA4G32 && wt <= kA8G128; }
-__host__ __device__ constexpr int affine_bits(int wt) { return wt <= kA4G128 ? 4 : 8; }
+__host__ __device__ constexpr bool is_affine(int wt) {
+    return (wt >= kA4G32 && wt <= kA8G128) || (wt >= kA3G32 && wt <= kA6G128);
+}
+__host__ __device__ constexpr int affine_bits(int wt) {
+    return wt <= kA4G128 ? 4 : wt <= kA8G128 ? 8 : wt <= kA3G128 ? 3 : wt <= kA5G128 ? 5 : 6;
+}
+// the affine types come in triples of group sizes 32, 64, 128
 __host__ __device__ constexpr int affine_group(int wt) {
-    return (wt == kA4G32 || wt == kA8G32) ? 32 : (wt == kA4G64 || wt == kA8G64) ? 64 : 128;
+    return 32 << ((wt - (wt >= kA3G32 ? kA3G32 : kA4G32)) % 3);
 }
 
 constexpr int kMaxRows = 8;        // ROW_EXACT_MATVEC_MAX_ROWS
@@ -39,19 +47,22 @@ __host__ __device__ constexpr int block_bytes(int wt) {
 
 // Staging geometry.  A "chunk" is the slice of one weight row a lane decodes
 // between two pipeline waits: 72 F16 or BF16 values, 36 F32 values, 4 Q8_0
-// blocks, 8 Q5_0 blocks, one Q4_K / Q6_K super-block, or 128 bytes of affine
-// codes (256 4-bit / 128 8-bit values, staged as a 144-byte window).  A warp stages the same chunk of its 32*NR0
+// blocks, 8 Q5_0 blocks, one Q4_K / Q6_K super-block, 128 bytes of 4- or
+// 8-bit affine codes (256 / 128 values, staged as a 144-byte window), or 256
+// 3-, 5- or 6-bit affine codes (96, 160 or 192 bytes, staged as 112-, 176-
+// or 208-byte windows).  A warp stages the same chunk of its 32*NR0
 // rows as one 2-D TMA box, one row every `box` bytes.  Box widths are odd
 // multiples of 16 bytes, so 32 lanes reading 16 bytes each at the same
 // offset of their own rows hit distinct bank quads (4 wavefronts, the
 // minimum).  Q8_0 and Q6_K stage the 16-byte aligned window (144 / 240
 // bytes) around their 136 / 210 chunk bytes.
 __host__ __device__ constexpr int chunk_values(int wt) {
-    return is_affine(wt) ? 1024 / affine_bits(wt)
+    return is_affine(wt) ? ((affine_bits(wt) == 4 || affine_bits(wt) == 8) ? 1024 / affine_bits(wt) : 256)
            : (wt == kF16 || wt == kBF16) ? 72 : wt == kF32 ? 36 : wt == kQ8_0 ? 128 : 256;
 }
 __host__ __device__ constexpr int chunk_box(int wt) {
-    return (is_affine(wt) || wt == kF16 || wt == kBF16 || wt == kF32 || wt == kQ8_0 || wt == kQ4_K) ? 144
+    return is_affine(wt) ? (affine_bits(wt) == 3 ? 112 : affine_bits(wt) == 5 ? 176 : affine_bits(wt) == 6 ? 208 : 144)
+           : (wt == kF16 || wt == kBF16 || wt == kF32 || wt == kQ8_0 || wt == kQ4_K) ? 144
            : wt == kQ5_0 ? 176 : 240;
 }
 
@@ -125,6 +136,15 @@ REM_DECLARE_PARTS(mv_kernel_a4g128)
 REM_DECLARE_PARTS(mv_kernel_a8g32)
 REM_DECLARE_PARTS(mv_kernel_a8g64)
 REM_DECLARE_PARTS(mv_kernel_a8g128)
+REM_DECLARE_PARTS(mv_kernel_a3g32)
+REM_DECLARE_PARTS(mv_kernel_a3g64)
+REM_DECLARE_PARTS(mv_kernel_a3g128)
+REM_DECLARE_PARTS(mv_kernel_a5g32)
+REM_DECLARE_PARTS(mv_kernel_a5g64)
+REM_DECLARE_PARTS(mv_kernel_a5g128)
+REM_DECLARE_PARTS(mv_kernel_a6g32)
+REM_DECLARE_PARTS(mv_kernel_a6g64)
+REM_DECLARE_PARTS(mv_kernel_a6g128)
 #undef REM_DECLARE_PARTS
 
 // Dynamic shared memory of one CTA; the kernel lays it out the same way:

@@ -203,13 +203,17 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // Staged bytes per row (the TMA box width) and the byte position inside the
 // staged row where chunk `cc` starts.
-// Affine codes (the primary template): chunk cc is the 128 bytes at 128*cc
-// (256 4-bit or 128 8-bit values), staged as a 144-byte window (an odd
-// number of 16-byte units keeps the 32 lanes' reads on distinct bank quads).
+// Affine codes (the primary template): chunk cc is the kBytes bytes at
+// kBytes*cc -- 128 bytes of 4- or 8-bit codes (256 / 128 values) staged as a
+// 144-byte window, or 256 codes of 3, 5 or 6 bits (96, 160, 192 bytes)
+// staged as 112-, 176- or 208-byte windows (an odd number of 16-byte units
+// keeps the 32 lanes' reads on distinct bank quads).
 template <int WT> struct Stage {
     static_assert(is_affine(WT), "no staging geometry for this weight type");
-    static constexpr int kValues = 1024 / affine_bits(WT), kBox = 144;
-    __device__ static uint32_t gofs(uint32_t cc) { return cc * 128u; }
+    static constexpr int kValues = chunk_values(WT), kBox = chunk_box(WT);
+    static constexpr uint32_t kBytes = static_cast<uint32_t>(kValues * affine_bits(WT) / 8);
+    static_assert(kBytes % 16 == 0 && kBytes <= static_cast<uint32_t>(kBox), "chunk bytes");
+    __device__ static uint32_t gofs(uint32_t cc) { return cc * kBytes; }
     __device__ static int sofs(uint32_t) { return 0; }
 };
 template <> struct Stage<kF16> {
@@ -711,6 +715,28 @@ __device__ __forceinline__ void affine_codes(uint32_t v, float2& w01, float2& w2
     }
 }
 
+// Affine, 3, 5 or 6 bits: the four codes at bits 0, BITS, 2*BITS and 3*BITS
+// of v (a window of the row's bit stream) as exact floats: each field goes
+// in as mantissa bits under the exponent that puts its lowest bit at 2^0
+// (2^23 for bit 0, 2^(23-BITS) for bit BITS), and the exponent's value is
+// subtracted; the upper pair is read the same way from v >> 2*BITS.
+template <int BITS>
+__device__ __forceinline__ void affine_codes_n(uint32_t v, float2& w01, float2& w23) {
+    constexpr uint32_t M = (1u << BITS) - 1u;
+    constexpr uint32_t E1 = static_cast<uint32_t>(150 - BITS) << 23;
+    const float2 bias = make_float2(-8388608.0f, -static_cast<float>(1u << (23 - BITS)));
+    const uint32_t u = v >> (2 * BITS);
+    w01 = add2(make_float2(fbits(lop_and_or(v, M, 0x4B000000u)), fbits(lop_and_or(v, M << BITS, E1))), bias);
+    w23 = add2(make_float2(fbits(lop_and_or(u, M, 0x4B000000u)), fbits(lop_and_or(u, M << BITS, E1))), bias);
+}
+
+// Word W (0..7) of two 16-byte lines.
+template <int W>
+__device__ __forceinline__ uint32_t word8(const uint4& a, const uint4& b) {
+    if constexpr (W < 4) return word_of<W>(a);
+    else return word_of<W - 4>(b);
+}
+
 // Affine chunk: every weight is dequantized on its own, w = fl(fl(scale*q) +
 // bias); scale*q (a binary16 times a code of at most 8 bits) is exact in
 // binary32, so that is fma(scale, q, bias) bit for bit.  Then acc += w*x.
@@ -743,17 +769,43 @@ __device__ __forceinline__ void chunk_affine(const uint8_t* const (&rows)[NR0], 
             sc2[i] = make_float2(sc, sc);
             bi2[i] = make_float2(bi, bi);
         }
-        // code words are read as 16-byte lines when the chain first needs
-        // them (a group's codes are a whole number of lines)
-        uint4 cv[NR0];
-        chain_acc<M, NR0, GS / 4, CV>(acc, xl + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
-            constexpr int Q = g * (GS / 4) + decltype(qc)::value;
-            constexpr int WI = BITS == 8 ? Q : Q / 2;  // code word of values 4Q..4Q+3
-            if constexpr ((WI & 3) == 0 && (BITS == 8 || (Q & 1) == 0)) cv[i] = lds16(rows[i] + 4 * WI);
-            affine_codes<BITS, Q>(word_of<WI & 3>(cv[i]), w01, w23);
-            w01 = fma2(sc2[i], w01, bi2[i]);
-            w23 = fma2(sc2[i], w23, bi2[i]);
-        });
+        if constexpr (BITS == 4 || BITS == 8) {
+            // code words are read as 16-byte lines when the chain first needs
+            // them (a group's codes are a whole number of lines)
+            uint4 cv[NR0];
+            chain_acc<M, NR0, GS / 4, CV>(acc, xl + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
+                constexpr int Q = g * (GS / 4) + decltype(qc)::value;
+                constexpr int WI = BITS == 8 ? Q : Q / 2;  // code word of values 4Q..4Q+3
+                if constexpr ((WI & 3) == 0 && (BITS == 8 || (Q & 1) == 0)) cv[i] = lds16(rows[i] + 4 * WI);
+                affine_codes<BITS, Q>(word_of<WI & 3>(cv[i]), w01, w23);
+                w01 = fma2(sc2[i], w01, bi2[i]);
+                w23 = fma2(sc2[i], w23, bi2[i]);
+            });
+        } else {
+            // 3, 5 or 6 bits: 32 values (4*BITS bytes, from byte 4*BITS*SG of
+            // the chunk) lie in at most two 16-byte lines, read when the
+            // chain reaches them; quad QQ of the 32 takes the 4*BITS stream
+            // bits from bit 4*BITS*QQ on, one word or a funnel shift of two
+            uint4 la[NR0], lb[NR0];
+            chain_acc<M, NR0, GS / 4, CV>(acc, xl + GS * g, [&](auto qc, int i, float2& w01, float2& w23) {
+                constexpr int Q = g * (GS / 4) + decltype(qc)::value;  // quad of the chunk
+                constexpr int SG = Q / 8, QQ = Q % 8;
+                constexpr int L0 = (4 * BITS * SG) / 16, L1 = (4 * BITS * SG + 4 * BITS - 1) / 16;
+                static_assert(L1 <= L0 + 1, "32 values span at most two lines");
+                if constexpr (QQ == 0) {
+                    la[i] = lds16(rows[i] + 16 * L0);
+                    if constexpr (L1 > L0) lb[i] = lds16(rows[i] + 16 * L1);
+                }
+                constexpr int B = 32 * BITS * SG + 4 * BITS * QQ - 128 * L0;  // first bit, from line L0
+                constexpr int WI = B / 32, S = B % 32;
+                uint32_t v;
+                if constexpr (S + 4 * BITS <= 32) v = word8<WI>(la[i], lb[i]) >> S;
+                else v = __funnelshift_r(word8<WI>(la[i], lb[i]), word8<WI + 1>(la[i], lb[i]), S);
+                affine_codes_n<BITS>(v, w01, w23);
+                w01 = fma2(sc2[i], w01, bi2[i]);
+                w23 = fma2(sc2[i], w23, bi2[i]);
+            });
+        }
     });
 }
 
@@ -796,8 +848,8 @@ __device__ __forceinline__ void stage_w_plain(uint8_t* dst_rows, const uint8_t* 
     constexpr int BOX = Stage<WT>::kBox;
     uint32_t first, len;  // byte range of the chunk inside the row
     if constexpr (is_affine(WT)) {
-        first = cc * 128u;
-        len = static_cast<uint32_t>(min(static_cast<uint64_t>(128u), row_bytes - first));
+        first = cc * Stage<WT>::kBytes;
+        len = static_cast<uint32_t>(min(static_cast<uint64_t>(Stage<WT>::kBytes), row_bytes - first));
     } else if constexpr (WT == kF16 || WT == kBF16) {
         first = cc * 144u;
         len = 2u * min(72u, k - cc * 72u);

@@ -1,0 +1,4 @@
+// Instantiates rem_mv_kernel<kA5G128, M, NR0, H> for M = 1..4.
+#include "rem_mv.cuh"
+
+REM_INSTANTIATE(rem::kA5G128, mv_kernel_a5g128_a, 1, 4)

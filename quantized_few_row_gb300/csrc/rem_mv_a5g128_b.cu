@@ -1,0 +1,4 @@
+// Instantiates rem_mv_kernel<kA5G128, M, NR0, H> for M = 5..8.
+#include "rem_mv.cuh"
+
+REM_INSTANTIATE(rem::kA5G128, mv_kernel_a5g128_b, 5, 4)

@@ -1,0 +1,4 @@
+// Instantiates rem_mv_kernel<kA6G64, M, NR0, H> for M = 5..8.
+#include "rem_mv.cuh"
+
+REM_INSTANTIATE(rem::kA6G64, mv_kernel_a6g64_b, 5, 4)

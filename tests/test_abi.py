@@ -209,6 +209,9 @@ def test_affine_types_need_the_affine_entry(lib):
     assert rem.rem_dequantize(W, rem.A8_G32, 4, 256, Y, stream=0) == rem.REM_EINVAL
     assert rem.rem_quantize(X, rem.A8_G32, 4, 256, W, stream=0) == rem.REM_EINVAL
     assert rem.rem_row_bytes(rem.A4_G32, 4096) == 2048 and rem.rem_row_bytes(rem.A8_G128, 4096) == 4096
+    # 3, 5 and 6 bits: k*bits/8 bytes (packing units of 3, 5 and 3 bytes)
+    assert rem.rem_row_bytes(rem.A3_G32, 4096) == 1536 and rem.rem_row_bytes(rem.A5_G64, 4096) == 2560
+    assert rem.rem_row_bytes(rem.A6_G128, 4096) == 3072 and rem.rem_row_bytes(rem.A3_G128, 128) == 48
 
 
 @pytest.mark.parametrize("wt,rows,k,expect", [
