@@ -173,12 +173,13 @@ __host__ __device__ constexpr bool tc_format(int wt) { return wt == kQ8_0 || wt 
 __host__ __device__ constexpr int tc_max_mp(int) { return 16; }
 // K-steps (16 values) per scale block: Q6_K sub-blocks of 16, Q8_0 / Q5_0 blocks of 32.
 __host__ __device__ constexpr int tc_kpb(int wt) { return wt == kQ6_K ? 1 : 2; }
-// K-steps of a 64-value unit each consumer warp decodes: one (16 consumer
-// warps, four per lane quarter of the tile).  Every tile width takes the same
+// K-steps of a 64-value unit each consumer warp decodes: two (8 consumer
+// warps, two per lane quarter of the tile).  Every tile width takes the same
 // warp assignment, so the arithmetic of an output does not depend on it.
-__host__ __device__ constexpr int tc_kpw(int) { return 1; }
+__host__ __device__ constexpr int tc_kpw(int) { return 2; }
 __host__ __device__ constexpr int tc_consumer_warps(int mp) { return 4 * (4 / tc_kpw(mp)); }
-__host__ __device__ constexpr int tc_threads(int mp) { return (tc_consumer_warps(mp) + 2) * 32; }
+// consumers, the producer and two MMA warps
+__host__ __device__ constexpr int tc_threads(int mp) { return (tc_consumer_warps(mp) + 3) * 32; }
 // K-steps one accumulator region covers (the MMAs of a scale block's
 // K-steps accumulate when one warp reads them all) and regions per unit.
 __host__ __device__ constexpr int tc_region_ksteps(int wt, int mp) {
@@ -218,7 +219,8 @@ inline uint32_t tc_smem_bytes(int wt, int mp, int stages, int split) {
     const uint32_t groups = (uint32_t)tc_consumer_warps(mp) / 4u;
     const uint32_t pbuf = 2u * (groups - 1u) * 4u * (uint32_t)mp * 32u * 4u;
     (void)split;
-    return (uint32_t)stages * stage + btiles + pbuf + 8u * (4 * kMaxStages + 1) + 16u + 128u;
+    // mbarriers: full and empty per stage, A full and D full per slot (4 + 4), a drain per MMA warp
+    return (uint32_t)stages * stage + btiles + pbuf + 8u * (4 * kMaxStages + 2) + 16u + 128u;
 }
 const void* tc_kernel(int wt, int mp);
 const void* tc_kernel_q8_0(int mp);

@@ -173,38 +173,48 @@ __device__ __forceinline__ void s8_bf16(uint32_t v, uint32_t& p0, uint32_t& p1) 
     p1 = bf16x2_sub(lop_and_or(w, 0x007F007Fu, 0x43004300u), lop_and_or(w, 0x00800080u, 0x43004300u));
 }
 
-// Per format:
-//   kUPC         units per staged chunk; a unit is one K-step of 16 values
-//                for each of the 4 warp groups (4 MMAs);
+// Per format.  A unit is one K-step of 16 values in each of the 4 MMA slots
+// of a slot's A columns; warp group g of a lane quarter decodes slots 2g and
+// 2g+1 (A columns 16g .. 16g+15) of every unit.
+//   kUPC         units per staged chunk;
 //   kPerm        order of the 16 values of a K-step in A's columns (0 =
 //                natural, 1 = values 4i, 4i+2, 4i+1, 4i+3 for each group i of
 //                4: the byte pairs a byte-parallel decode yields);
-//   kstep(u, g)  the K-step of the chunk whose codes warp group g decodes in
-//                unit u, i.e. the B tile that the MMA of A columns 8g..8g+7
-//                of that unit reads;
+//   kRK          K-steps per accumulator region: 2 where a warp's two
+//                K-steps are the halves of one 32-value scale block (their
+//                MMAs accumulate into one region, read and scaled once), else 1;
+//   kstep(u, s)  the K-step of the chunk in MMA slot s of unit u (the B tile
+//                that MMA reads);
 //   Regs         the words a consumer lane keeps from one load to the units
 //                that decode them (kLoad(u): a load at unit u; kLastLoad: the
 //                unit after whose load the staged weights are no longer read);
 //   load<U>      16-byte shared loads at compile-time positions; a switch
 //                picks the body for the runtime byte position (chunk offset o,
 //                warp group g);
-//   decode<U>    unit U's 16 codes of the lane's row as 8 bfloat16 pairs, and
-//                their scale.
-// The mapping keeps every byte a group needs for the chunk in one place, so
-// each staged byte is read about once per lane.
+//   decode<U>    unit U's 32 codes of the lane's row (slots 2g, 2g+1) as 16
+//                bfloat16 pairs, and the scales of its 2 / kRK regions.
+// The mapping keeps the bytes a warp needs together, so each staged byte is
+// read about once per lane.
 template <int WT> struct TcFmt;
 
 // Q8_0: a chunk is 4 blocks (d f16 | 32 int8), 128 values at byte o = 0 or 8
-// of the staged window.  Warp group g decodes block g: its first 16 codes in
-// unit 0 and the other 16 in unit 1 (K-step 2g + u).
+// of the staged window.  Warp group g decodes block 2u + g in unit u: its
+// halves are K-steps 4u + 2g and 4u + 2g + 1, one scale block.
 template <> struct TcFmt<kQ8_0> {
-    static constexpr int kUPC = 2, kPerm = 1, kLastLoad = 0;
-    __host__ __device__ static constexpr int kstep(int u, int g) { return 2 * g + u; }
-    __host__ __device__ static constexpr bool kLoad(int u) { return u == 0; }
+    static constexpr int kUPC = 2, kPerm = 1, kLastLoad = 1, kRK = 2;
+    __host__ __device__ static constexpr int kstep(int u, int s) { return 4 * u + s; }
+    __host__ __device__ static constexpr bool kLoad(int) { return true; }
     struct Regs {
         uint32_t q[8];  // the 32 codes
         float d;
     };
+    // An empty asm that "changes" the words, so no decode from them is
+    // computed ahead of the point it is called at (register lifetimes stay
+    // one unit long).
+    __device__ __forceinline__ static void pin(Regs& r) {
+        asm volatile("" : "+r"(r.q[0]), "+r"(r.q[1]), "+r"(r.q[2]), "+r"(r.q[3]), "+r"(r.q[4]), "+r"(r.q[5]),
+                     "+r"(r.q[6]), "+r"(r.q[7]), "+f"(r.d));
+    }
     template <int P>
     __device__ __forceinline__ static void block(const uint8_t* row, Regs& r) {
         uint32_t dw[1];
@@ -214,7 +224,7 @@ template <> struct TcFmt<kQ8_0> {
     }
     template <int U>
     __device__ __forceinline__ static void load(const uint8_t* row, int o, int g, Regs& r) {
-        switch ((o ? 4 : 0) + g) {
+        switch ((o ? 4 : 0) + 2 * U + g) {
         case 0: block<0>(row, r); break;
         case 1: block<34>(row, r); break;
         case 2: block<68>(row, r); break;
@@ -226,26 +236,29 @@ template <> struct TcFmt<kQ8_0> {
         }
     }
     template <int U>
-    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[8], float& scale) {
+    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[16], float (&scale)[1]) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s8_bf16(r.q[4 * U + i], a[2 * i], a[2 * i + 1]);
-        scale = r.d;
+        for (int i = 0; i < 8; ++i) s8_bf16(r.q[i], a[2 * i], a[2 * i + 1]);
+        scale[0] = r.d;
     }
 };
 
 // Q5_0: a chunk is 8 blocks (d f16 | qh u32 | 16 nibble bytes), 256 values
-// at byte 0 of the staged row.  Warp group g decodes block g in units 0 and 1
-// and block g + 4 in units 2 and 3: the low nibbles (values 0..15) in the
-// even unit, the high ones (values 16..31) in the odd one; bit 4 of value e
-// is bit e of qh.
+// at byte 0 of the staged row.  Warp group g decodes block 2u + g in unit u:
+// the low nibbles (values 0..15, K-step 4u + 2g) and the high ones (values
+// 16..31, K-step 4u + 2g + 1) of the same bytes; bit 4 of value e is bit e
+// of qh.
 template <> struct TcFmt<kQ5_0> {
-    static constexpr int kUPC = 4, kPerm = 1, kLastLoad = 2;
-    __host__ __device__ static constexpr int kstep(int u, int g) { return 2 * (g + 4 * (u >> 1)) + (u & 1); }
-    __host__ __device__ static constexpr bool kLoad(int u) { return (u & 1) == 0; }
+    static constexpr int kUPC = 4, kPerm = 1, kLastLoad = 3, kRK = 2;
+    __host__ __device__ static constexpr int kstep(int u, int s) { return 4 * u + s; }
+    __host__ __device__ static constexpr bool kLoad(int) { return true; }
     struct Regs {
         uint32_t qs[4], qh;
         float d;
     };
+    __device__ __forceinline__ static void pin(Regs& r) {
+        asm volatile("" : "+r"(r.qs[0]), "+r"(r.qs[1]), "+r"(r.qs[2]), "+r"(r.qs[3]), "+r"(r.qh), "+f"(r.d));
+    }
     template <int P>
     __device__ __forceinline__ static void block(const uint8_t* row, Regs& r) {
         uint32_t q[6];
@@ -257,7 +270,7 @@ template <> struct TcFmt<kQ5_0> {
     }
     template <int U>
     __device__ __forceinline__ static void load(const uint8_t* row, int, int g, Regs& r) {
-        switch (g + 4 * (U >> 1)) {
+        switch (2 * U + g) {
         case 0: block<0>(row, r); break;
         case 1: block<22>(row, r); break;
         case 2: block<44>(row, r); break;
@@ -269,15 +282,16 @@ template <> struct TcFmt<kQ5_0> {
         }
     }
     template <int U>
-    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[8], float& scale) {
-        constexpr int kh = U & 1;
+    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[16], float (&scale)[1]) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t nib = kh ? (r.qs[i] >> 4) : r.qs[i];
-            const uint32_t v = lop_and_or(nib, 0x0F0F0F0Fu, spread4((r.qh >> (16 * kh + 4 * i)) & 0xFu));
-            codes_bf16(v, 0x001F001Fu, 0x43104310u, a[2 * i], a[2 * i + 1]);
-        }
-        scale = r.d;
+        for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t nib = kh ? (r.qs[i] >> 4) : r.qs[i];
+                const uint32_t v = lop_and_or(nib, 0x0F0F0F0Fu, spread4((r.qh >> (16 * kh + 4 * i)) & 0xFu));
+                codes_bf16(v, 0x001F001Fu, 0x43104310u, a[8 * kh + 2 * i], a[8 * kh + 2 * i + 1]);
+            }
+        scale[0] = r.d;
     }
 };
 
@@ -286,29 +300,40 @@ template <> struct TcFmt<kQ5_0> {
 // sub-blocks in order, each one scale block.  Sub-block s = 8h + 2t + e holds
 // values 128h + 32t + 16e + l (l < 16): low bits from ql[64h + 32(t&1) + 16e
 // + l] (the low nibble for t < 2, the high one for t >= 2), high bits 2t,
-// 2t+1 of qh[32h + 16e + l], scale d * sc[s].  Warp group g = 2h + e decodes
-// sub-block 8h + 2u + e in unit u = t, so the 48 code bytes it loads once
-// (two 16-byte runs of ql, one of qh) serve all four of its units.
+// 2t+1 of qh[32h + 16e + l], scale d * sc[s].  Warp group g = h decodes
+// sub-blocks 8h + 2u + e (e = 0, 1; MMA slots 2h + e) in unit u = t, so the
+// 96 code bytes it loads once (four 16-byte runs of ql, two of qh) serve all
+// four of its units.
 template <> struct TcFmt<kQ6_K> {
-    static constexpr int kUPC = 4, kPerm = 1, kLastLoad = 0;
-    __host__ __device__ static constexpr int kstep(int u, int g) { return 8 * (g >> 1) + 2 * u + (g & 1); }
+    static constexpr int kUPC = 4, kPerm = 1, kLastLoad = 0, kRK = 1;
+    __host__ __device__ static constexpr int kstep(int u, int s) { return 8 * (s >> 1) + 2 * u + (s & 1); }
     __host__ __device__ static constexpr bool kLoad(int u) { return u == 0; }
     struct Regs {
-        uint32_t qa[4], qb[4], qh[4];  // ql for t = 0, 2 and t = 1, 3; qh
-        uint32_t sc0, sc1;             // sc[8h + e + 2t] at bits 0..7 (t = 0, 2) and 16..23 (t = 1, 3)
+        uint32_t qa[2][4], qb[2][4], qh[2][4];  // per e: ql for t = 0, 2 and t = 1, 3; qh
+        uint32_t sc0, sc1;                      // sc[8h .. 8h+3] and sc[8h+4 .. 8h+7]
         float d;
     };
+    __device__ __forceinline__ static void pin(Regs& r) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            asm volatile("" : "+r"(r.qa[e][0]), "+r"(r.qa[e][1]), "+r"(r.qa[e][2]), "+r"(r.qa[e][3]), "+r"(r.qb[e][0]),
+                         "+r"(r.qb[e][1]), "+r"(r.qb[e][2]), "+r"(r.qb[e][3]), "+r"(r.qh[e][0]), "+r"(r.qh[e][1]),
+                         "+r"(r.qh[e][2]), "+r"(r.qh[e][3]));
+        asm volatile("" : "+r"(r.sc0), "+r"(r.sc1), "+f"(r.d));
+    }
     template <int O>
-    __device__ __forceinline__ static void body(const uint8_t* row, int g, Regs& r) {
-        const int h = g >> 1, e = g & 1;
+    __device__ __forceinline__ static void body(const uint8_t* row, int h, Regs& r) {
         uint32_t sc4[4], dw[1];
-        row_words<O, 4>(row + 64 * h + 16 * e, r.qa);
-        row_words<O + 32, 4>(row + 64 * h + 16 * e, r.qb);
-        row_words<O + 128, 4>(row + 32 * h + 16 * e, r.qh);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            row_words<O, 4>(row + 64 * h + 16 * e, r.qa[e]);
+            row_words<O + 32, 4>(row + 64 * h + 16 * e, r.qb[e]);
+            row_words<O + 128, 4>(row + 32 * h + 16 * e, r.qh[e]);
+        }
         row_words<O + 192, 4>(row, sc4);
         row_words<O + 208, 1>(row, dw);
-        r.sc0 = (h ? sc4[2] : sc4[0]) >> (8 * e);
-        r.sc1 = (h ? sc4[3] : sc4[1]) >> (8 * e);
+        r.sc0 = h ? sc4[2] : sc4[0];
+        r.sc1 = h ? sc4[3] : sc4[1];
         r.d = h2f(dw[0]);
     }
     template <int U>
@@ -325,18 +350,21 @@ template <> struct TcFmt<kQ6_K> {
         }
     }
     template <int U>
-    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[8], float& scale) {
-        const uint32_t scw = U < 2 ? r.sc0 : r.sc1;
-        scale = __fmul_rn(r.d, (U & 1) ? sbyte_f<2>(scw) : sbyte_f<0>(scw));
+    __device__ __forceinline__ static void decode(const Regs& r, uint32_t (&a)[16], float (&scale)[2]) {
+        const uint32_t scw = U < 2 ? r.sc0 : r.sc1;  // sc[8h + 2t + e] is byte 2(t%2) + e of it
+        scale[0] = __fmul_rn(r.d, (U & 1) ? sbyte_f<2>(scw) : sbyte_f<0>(scw));
+        scale[1] = __fmul_rn(r.d, (U & 1) ? sbyte_f<3>(scw) : sbyte_f<1>(scw));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t ql = (U & 1) ? r.qb[i] : r.qa[i];
-            // high bits 2t, 2t+1 of each qh byte -> bits 4, 5
-            uint32_t v;
-            if constexpr (U < 2) v = lop_sel(ql, r.qh[i] << (4 - 2 * U), 0x0F0F0F0Fu);
-            else v = lop_sel(ql >> 4, r.qh[i] >> (2 * U - 4), 0x0F0F0F0Fu);
-            codes_bf16(v, 0x003F003Fu, 0x43204320u, a[2 * i], a[2 * i + 1]);
-        }
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t ql = (U & 1) ? r.qb[e][i] : r.qa[e][i];
+                // high bits 2t, 2t+1 of each qh byte -> bits 4, 5
+                uint32_t v;
+                if constexpr (U < 2) v = lop_sel(ql, r.qh[e][i] << (4 - 2 * U), 0x0F0F0F0Fu);
+                else v = lop_sel(ql >> 4, r.qh[e][i] >> (2 * U - 4), 0x0F0F0F0Fu);
+                codes_bf16(v, 0x003F003Fu, 0x43204320u, a[8 * e + 2 * i], a[8 * e + 2 * i + 1]);
+            }
     }
 };
 
@@ -364,7 +392,7 @@ struct TcGeom {
     static constexpr int THREADS = tc_threads(MP);
     static_assert(F::kUPC == tc_units_per_chunk(WT), "units per chunk");
     static_assert(F::kUPC % NS == 0, "units per chunk must be a multiple of the slots");
-    static_assert(KPW == 1 && RK == 1 && RPW == 1, "one K-step and one accumulator region per warp and unit");
+    static_assert(KPW == 2 && RK == F::kRK && RPW * RK == KPW, "two K-steps per warp and unit, kRK per region");
     static_assert(NS * (ACOLS + DCOLS) <= TCOLS, "slots exceed the tensor memory");
 };
 
@@ -441,41 +469,62 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
     }
 }
 
-// One accumulator region of a warp, its D columns loaded into d: c = D_hi +
-// D_lo for input rows 0..NJ-1 (NJ >= m; the rest of acc stays zero and is
-// never stored) and acc = fma(scale, c, acc).  Each column is computed on its
-// own, so skipping the columns past m changes no bit of the others.
-template <int MP, int NJ>
-__device__ __forceinline__ void tc_scale_cols(const uint32_t (&d)[2 * MP], float scale, float (&acc)[MP]) {
+// The RPW accumulator regions of a warp, their D columns loaded into d
+// (region b at columns b*2*MP on): c = D_hi + D_lo for input rows 0..NJ-1
+// (NJ >= m; the rest of acc stays zero and is never stored) and acc =
+// fma(scale_b, c, acc), region by region.  Columns go in pairs through the
+// f32x2 add and fma, which round each lane as the binary32 ops do; each
+// column is computed on its own, so skipping the columns past m changes no
+// bit of the others.
+template <int MP, int RPW, int NJ>
+__device__ __forceinline__ void tc_scale_cols(const uint32_t (&d)[RPW * 2 * MP], const float (&sc)[RPW],
+                                              float (&acc)[MP]) {
 #pragma unroll
-    for (int j = 0; j < NJ; ++j)
-        acc[j] = __fmaf_rn(scale, __fadd_rn(__uint_as_float(d[j]), __uint_as_float(d[MP + j])), acc[j]);
+    for (int b = 0; b < RPW; ++b) {
+        const float2 s2 = make_float2(sc[b], sc[b]);
+#pragma unroll
+        for (int j = 0; j + 1 < NJ; j += 2) {
+            const float2 c = add2(make_float2(__uint_as_float(d[b * 2 * MP + j]), __uint_as_float(d[b * 2 * MP + j + 1])),
+                                  make_float2(__uint_as_float(d[b * 2 * MP + MP + j]),
+                                              __uint_as_float(d[b * 2 * MP + MP + j + 1])));
+            const float2 r = fma2(s2, c, make_float2(acc[j], acc[j + 1]));
+            acc[j] = r.x;
+            acc[j + 1] = r.y;
+        }
+        if constexpr (NJ & 1)
+            acc[NJ - 1] = __fmaf_rn(sc[b], __fadd_rn(__uint_as_float(d[b * 2 * MP + NJ - 1]),
+                                                     __uint_as_float(d[b * 2 * MP + MP + NJ - 1])),
+                                    acc[NJ - 1]);
+    }
 }
-template <int MP>
-__device__ __forceinline__ void tc_scale(const uint32_t (&d)[2 * MP], float scale, uint32_t m, float (&acc)[MP]) {
-    if (m <= 1) tc_scale_cols<MP, 1>(d, scale, acc);
-    else if (m <= 2) tc_scale_cols<MP, 2>(d, scale, acc);
-    else if (m <= 4) tc_scale_cols<MP, 4>(d, scale, acc);
-    else if (MP == 8 || m <= 8) tc_scale_cols<MP, (MP < 8 ? MP : 8)>(d, scale, acc);
-    else tc_scale_cols<MP, MP>(d, scale, acc);
+template <int MP, int RPW>
+__device__ __forceinline__ void tc_scale(const uint32_t (&d)[RPW * 2 * MP], const float (&sc)[RPW], uint32_t m,
+                                         float (&acc)[MP]) {
+    if (m <= 1) tc_scale_cols<MP, RPW, 1>(d, sc, acc);
+    else if (m <= 2) tc_scale_cols<MP, RPW, 2>(d, sc, acc);
+    else if (m <= 4) tc_scale_cols<MP, RPW, 4>(d, sc, acc);
+    else if (MP == 8 || m <= 8) tc_scale_cols<MP, RPW, (MP < 8 ? MP : 8)>(d, sc, acc);
+    else tc_scale_cols<MP, RPW, MP>(d, sc, acc);
 }
 
 // Persistent kernel: clusters of `split` CTAs walk the 128-row tiles; CTA
 // rank s of a cluster handles K range s of every tile.  Warps 0..CW-1 are
 // consumers: warp w holds rows 32(w%4) .. 32(w%4)+31 of the tile (its TMEM
-// lane quarter) and, as warp group g = w/4, K-step kstep(u, g) of every unit u
-// with its accumulator region; warp CW is the producer (TMA or plain staging
-// of weights and inputs), warp CW+1 the MMA issuer and owner of the tensor
-// memory.  The warps of one lane quarter accumulate separately; at the end of
-// a tile their partials are added in warp-group order.
+// lane quarter) and, as warp group g = w/4, the K-steps kstep(u, 2g) and
+// kstep(u, 2g+1) of every unit u with their accumulator regions.  Warp CW is
+// the producer (TMA or plain staging of weights and inputs); warps CW+1 and
+// CW+2 issue the MMAs of the even and the odd slots, and warp CW+1 owns the
+// tensor memory.  The warps of one lane quarter accumulate separately; at the
+// end of a tile their partials are added in warp-group order.
 template <int WT, int MP>
 __global__ void __launch_bounds__(TcGeom<WT, MP>::THREADS, 1)
 rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
     using G = TcGeom<WT, MP>;
     using F = TcFmt<WT>;
-    constexpr int NS = G::NS, UPC = F::kUPC;
+    constexpr int NS = G::NS, UPC = F::kUPC, KPW = G::KPW, RK = G::RK, RPW = G::RPW;
     constexpr int CV = G::CV, BOX = G::BOX, ROWS = 128;
-    constexpr int CW = G::CW, PRODUCER = CW, ISSUER = CW + 1;
+    constexpr int CW = G::CW, PRODUCER = CW, ISSUER = CW + 1, ISSUER2 = CW + 2;
+    static_assert(NS % 2 == 0, "the two MMA warps take alternate slots");
     constexpr uint32_t XPAD = (MP * CV * 4 + 127u) & ~127u;
     constexpr uint32_t WSTAGE = ROWS * BOX;
     constexpr uint32_t STAGE = WSTAGE + XPAD;
@@ -505,8 +554,8 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     uint64_t* empty = full + kMaxStages;
     uint64_t* afull = empty + kMaxStages;
     uint64_t* dfull = afull + 4;
-    uint64_t* drain = dfull + 4;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* drain = dfull + 4;   // [2], one per MMA warp
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 2);
     const uint32_t c0 = static_cast<uint32_t>((static_cast<uint64_t>(s) * a.nchunk) / S);
     const uint32_t c1 = static_cast<uint32_t>((static_cast<uint64_t>(s + 1) * a.nchunk) / S);
     const int nck = static_cast<int>(c1 - c0);
@@ -528,6 +577,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             mbar_init(db + 8 * t, 1u);
         }
         mbar_init(smem_u32(drain), 1u);
+        mbar_init(smem_u32(drain + 1), 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // the B tiles' rows m..MP-1 stay zero for the whole launch
@@ -627,10 +677,15 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         return;
     }
 
-    if (warp == ISSUER) {
-        // ------------------------------------------------ MMA issuer
-        // The whole warp walks the units, so every operand is warp-uniform
-        // (the descriptors are a base plus compile-time steps); lane 0 issues.
+    if (warp == ISSUER || warp == ISSUER2) {
+        // ------------------------------------------------ MMA issuers
+        // Two warps issue the MMAs, the first for the even slots, the second
+        // for the odd ones: a commit and the wait on it before a slot is
+        // reused hold up only the units of that warp, so the other warp's
+        // MMAs keep the tensor pipe busy meanwhile.  Each warp walks all the
+        // units, so every operand is warp-uniform (the descriptors are a base
+        // plus compile-time steps); its lane 0 issues.
+        const int par = warp - ISSUER;
         bool failed = false;
         bool issued_any = false;
         uint32_t gc = 0;  // chunks over all tiles
@@ -642,7 +697,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 const uint64_t bchunk = bdesc0 + static_cast<uint64_t>(((gc & 1u) * G::BCHUNK) >> 4);
                 static_for<0, UPC>([&](auto u_) {
                     constexpr int U = decltype(u_)::value, SL = U % NS;
-                    if (failed) return;
+                    if (SL % 2 != par || failed) return;
                     const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(U / NS);
                     if (!__all_sync(0xFFFFFFFFu, mbar_wait(ab + 8 * SL, use & 1u, a.wait_ns))) {
                         if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
@@ -654,9 +709,10 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     const uint32_t dc = tmem + static_cast<uint32_t>(NS * G::ACOLS + SL * G::DCOLS);
                     if (lane == 0) {
 #pragma unroll
-                        for (int g = 0; g < 4; ++g)
-                            tc_mma(dc + static_cast<uint32_t>(g * G::NCOL), ac + 8u * g,
-                                   bchunk + static_cast<uint64_t>((F::kstep(U, g) * G::BKSTEP) >> 4), idesc, false);
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            tc_mma(dc + static_cast<uint32_t>((k4 / RK) * G::NCOL), ac + 8u * k4,
+                                   bchunk + static_cast<uint64_t>((F::kstep(U, k4) * G::BKSTEP) >> 4), idesc,
+                                   (k4 % RK) != 0);
                         tc_commit(db + 8 * SL);
                     }
                     __syncwarp();
@@ -672,13 +728,15 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         if (S > 1) cluster_sync();
         // every MMA this warp issued has completed before the memory goes back
         if (lane == 0 && issued_any) {
-            tc_commit(smem_u32(drain));
-            if (!mbar_wait(smem_u32(drain), 0u, a.wait_ns)) report_timeout(a.status, kStatusWaitTimeout);
+            tc_commit(smem_u32(drain + par));
+            if (!mbar_wait(smem_u32(drain + par), 0u, a.wait_ns)) report_timeout(a.status, kStatusWaitTimeout);
         }
         __syncwarp();
-        asm volatile("bar.sync 1, %0;" ::"n"((CW + 1) * 32) : "memory");
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(G::TCOLS) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"((CW + 2) * 32) : "memory");
+        if (par == 0) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(G::TCOLS) : "memory");
+        }
         return;
     }
 
@@ -695,9 +753,11 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         float acc[MP];
 #pragma unroll
         for (int j = 0; j < MP; ++j) acc[j] = 0.0f;
-        float psc[NS];  // scales of the units in flight, by slot
+        float psc[NS][RPW];  // region scales of the units in flight, by slot
 #pragma unroll
-        for (int j = 0; j < NS; ++j) psc[j] = 0.0f;
+        for (int j = 0; j < NS; ++j)
+#pragma unroll
+            for (int b = 0; b < RPW; ++b) psc[j][b] = 0.0f;
         // the slot's MMAs (use number `use`) have completed: its D is ready, its A is free
         auto wait_d = [&](int sl, uint32_t use) {
             if (failed) return;
@@ -708,8 +768,11 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             }
             tc_fence_after();
         };
-        auto load_d = [&](int sl, uint32_t (&d)[G::NCOL]) {
-            tmem_ld<G::NCOL>(tmem + lane_base + static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS + grp * G::NCOL), d);
+        // the warp's RPW regions of slot sl: regions KPW*grp/RK on, contiguous
+        auto load_d = [&](int sl, uint32_t (&d)[RPW * G::NCOL]) {
+            tmem_ld<RPW * G::NCOL>(tmem + lane_base + static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS +
+                                                                           (KPW * grp / RK) * G::NCOL),
+                                   d);
         };
         for (int q = 0; q < nck; ++q, ++i, ++gc) {
             const int st = static_cast<int>(i % D);
@@ -740,23 +803,28 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 }
                 const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(U / NS);
                 const bool pending = q > 0 || U >= NS;  // slot SL holds an earlier unit of this tile
-                // the old unit's D is read after this unit's codes are
-                // stored, so the decode does not hold its registers
+                // The unit's codes are decoded into registers while the
+                // slot's previous MMAs may still run (the pin keeps the
+                // decode from moving ahead of the previous unit), then the
+                // slot is taken over: its old D read out and scaled, the new
+                // codes stored and the slot handed to the MMA warps.
+                uint32_t av[8 * KPW];
+                float nsc[RPW];
+                F::pin(R);
+                F::template decode<U>(R, av, nsc);
                 if (pending) {
                     wait_d(SL, use - 1u);
                     if (failed) return;
                 }
-                uint32_t av[8];
-                float nsc;
-                F::template decode<U>(R, av, nsc);
-                tmem_st_cols<1>(tmem + lane_base + static_cast<uint32_t>(SL * G::ACOLS + 8 * grp), av);
+                tmem_st_cols<KPW>(tmem + lane_base + static_cast<uint32_t>(SL * G::ACOLS + 8 * KPW * grp), av);
                 if (pending) {
-                    uint32_t d[G::NCOL];
+                    uint32_t d[RPW * G::NCOL];
                     load_d(SL, d);
                     tmem_ld_wait();
-                    tc_scale<MP>(d, psc[SL], m, acc);
+                    tc_scale<MP, RPW>(d, psc[SL], m, acc);
                 }
-                psc[SL] = nsc;
+#pragma unroll
+                for (int bb = 0; bb < RPW; ++bb) psc[SL][bb] = nsc[bb];
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -769,10 +837,10 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 constexpr int SL = decltype(s_)::value;
                 wait_d(SL, (gc - 1u) * (UPC / NS) + static_cast<uint32_t>((UPC - NS + SL) / NS));
                 if (failed) return;
-                uint32_t d[G::NCOL];
+                uint32_t d[RPW * G::NCOL];
                 load_d(SL, d);
                 tmem_ld_wait();
-                tc_scale<MP>(d, psc[SL], m, acc);
+                tc_scale<MP, RPW>(d, psc[SL], m, acc);
             });
         }
         // the other warp groups' partials join group 0's, in group order
@@ -798,7 +866,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     }
     if (S > 1) cluster_sync();
     tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"n"((CW + 1) * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"((CW + 2) * 32) : "memory");
 }
 
 }  // namespace dev
