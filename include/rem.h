@@ -44,8 +44,8 @@
  *   REM_ENGINE_TC    the tensor cores (tcgen05) for Q8_0, Q5_0 and Q6_K: per
  *                    block, the exact codes times each input split into two
  *                    bfloat16 parts, summed in binary32, then scaled by the
- *                    block scale in binary32; up to 16 input rows per pass
- *                    over the weights
+ *                    block scale in binary32; up to 32 input rows per pass
+ *                    over the weights (Q6_K: 16)
  */
 #ifndef REM_H
 #define REM_H
@@ -244,8 +244,8 @@ int rem_dequantize_affine(const void* codes, const uint16_t* scales, const uint1
  * in row_exact_matvec.rs caps one dispatch at 8 rows; the matrix-vector regime
  * extends further, cf. qmv_batch_limit in nuvec-core 0.6.0 src/gpu.rs).  The
  * m input rows run in groups, one launch per group, each reading W once:
- * groups of up to 16 rows on the tensor-core engine (ceil(m/16) passes over
- * W), of up to REM_MAX_ROWS on the SIMT engine (ceil(m/8) passes).  Rows are independent, so row j is bitwise the
+ * groups of up to 32 rows on the tensor-core engine (16 for Q6_K), of up to
+ * REM_MAX_ROWS on the SIMT engine.  Rows are independent, so row j is bitwise the
  * row an m = 1 call with the same split and engine produces.
  *
  *   Arguments as rem_matvec_ex (strides in elements, split 0 = automatic from
@@ -262,7 +262,8 @@ int rem_matvec_many(const void* W, int wtype, uint32_t n, uint32_t k, uint32_t b
 /*
  * rem_matvec_sched -- the product for any m >= 1 with an explicit schedule
  * (NULL = all defaults).  Arguments as rem_matvec_many; the input rows run in
- * launches of up to 8 rows (SIMT engine) or 16 rows (tensor-core engine),
+ * launches of up to 8 rows (SIMT engine) or 32 rows (tensor-core engine;
+ * 16 for Q6_K),
  * each reading W once, all checked before the first launch.
  * Returns REM_EINVAL for a schedule field out of range, for the tensor-core
  * engine on a format it does not take, and for the argument errors of

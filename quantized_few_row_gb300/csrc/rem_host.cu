@@ -476,12 +476,13 @@ int plan_simt(int dev, const DeviceState& ds, int wt, const Shape& s, const Sche
     }
     double best = -1.0;
     int last_cap = 0;
+    const int km = static_cast<int>(s.m);  // the kernel's M
     for (int l = kNumLayouts - 1; l >= 0; --l) {
-        const void* f = mv_kernel(wt, static_cast<int>(s.m), l);
+        const void* f = mv_kernel(wt, km, l);
         if (!f || (sc.layout >= 0 && l != sc.layout)) continue;
         const int nr0 = layout_nr0(l), h = layout_h(l);
         const uint32_t rpw = static_cast<uint32_t>(kLanes * nr0);
-        const int cap = ds.max_threads[wt][s.m][l];
+        const int cap = ds.max_threads[wt][km][l];
         for (int g = kMaxWarps; g >= 1; g /= 2) {
             if (sc.rows_per_cta ? static_cast<uint32_t>(g) * rpw != sc.rows_per_cta
                                 : (g > 4 || static_cast<uint32_t>(g) * rpw > 256u))
@@ -495,7 +496,7 @@ int plan_simt(int dev, const DeviceState& ds, int wt, const Shape& s, const Sche
             const uint64_t per_cta = ((p.nchunk + S - 1) / S) * ((units + 2ull * ds.sms - 1) / (2ull * ds.sms));
             const int dmax = static_cast<int>(std::min<uint64_t>(kMaxStages, std::max<uint64_t>(2, per_cta)));
             for (int d = 1; d <= dmax; ++d) {
-                const int sm = static_cast<int>(mv_smem_bytes(wt, nr0, h, g, d, static_cast<int>(s.m), S));
+                const int sm = static_cast<int>(mv_smem_bytes(wt, nr0, h, g, d, km, S));
                 if (sm > ds.smem_optin) continue;
                 cfg.blockDim = dim3(static_cast<unsigned>((g + 1) * 32));
                 cfg.dynamicSmemBytes = static_cast<size_t>(sm);
@@ -506,7 +507,7 @@ int plan_simt(int dev, const DeviceState& ds, int wt, const Shape& s, const Sche
                 const double eff = static_cast<double>(units) / static_cast<double>(waves * ctas);
                 const double warps_sm = static_cast<double>(ctas) / ds.sms * g;
                 const double gf = static_cast<double>(g) / (g + 1);
-                double score = std::min(warps_sm, 8.0) * layout_weight(wt, static_cast<int>(s.m), nr0, h) *
+                double score = std::min(warps_sm, 8.0) * layout_weight(wt, km, nr0, h) *
                                (d == 1 ? 0.7 : 1.0) * gf * gf * (1.0 - 0.2 * std::max(0, d - 2)) * eff;
                 if (score > best) {
                     best = score;
@@ -521,7 +522,7 @@ int plan_simt(int dev, const DeviceState& ds, int wt, const Shape& s, const Sche
         }
     }
     if (best < 0) {
-        if (sc.layout >= 0 && !mv_kernel(wt, static_cast<int>(s.m), sc.layout))
+        if (sc.layout >= 0 && !mv_kernel(wt, km, sc.layout))
             return fail(REM_ELAUNCH, "rem_matvec: lane layout %d has no %s kernel for m = %u", sc.layout,
                         wt_name(wt), s.m);
         if (last_cap)
@@ -552,7 +553,7 @@ int plan_simt(int dev, const DeviceState& ds, int wt, const Shape& s, const Sche
 // is raised until no more CTAs than that fit on one SM.
 int plan_tc(int dev, const DeviceState& ds, int wt, const Shape& s, Plan& p) {
     const uint32_t S = p.S;
-    p.mp = s.m <= 8 ? 8 : 16;
+    p.mp = s.m <= 8 ? 8 : s.m <= 16 ? 16 : 32;
     p.fn = tc_kernel(wt, p.mp);
     if (!p.fn || p.mp > tc_max_mp(wt))
         return fail(REM_ELAUNCH, "rem_matvec: no %s tensor-core kernel for m = %u", wt_name(wt), s.m);
@@ -834,8 +835,7 @@ int launch_many(const void* W, int wt, const float* x, float* y, const Shape& al
     int rc = validate_args(W, wt, x, y, all, sc.split, sc.rows_per_cta, 0);
     if (rc != REM_OK) return rc;
     const int engine = sc.engine >= 0 ? sc.engine : auto_engine(wt, static_cast<uint64_t>(all.batch) * all.n, all.k);
-    const uint32_t per = (engine == REM_ENGINE_TC && tc_format(wt)) ? engine_rows(engine, wt)
-                                                                     : static_cast<uint32_t>(kMaxRows);
+    const uint32_t per = engine_rows(engine, wt);
     for (uint32_t j0 = 0; j0 < all.m; j0 += per) {
         const Shape g{std::min<uint32_t>(per, all.m - j0), all.n, all.k, all.batch, all.xrs, all.xbs, all.yrs,
                       all.ybs};

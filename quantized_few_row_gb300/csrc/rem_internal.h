@@ -167,10 +167,17 @@ inline uint32_t mv_smem_bytes(int wt, int nr0, int h, int warps, int stages, int
 
 // The tensor-core kernel rem_tc_kernel<wt, mp> (rem_tc.cuh) serves the
 // block-scaled formats Q8_0, Q5_0 and Q6_K for up to mp input rows per
-// launch, mp in {8, 16}.  A CTA owns 128 weight rows.
+// launch, mp in {8, 16, 32} (Q6_K: {8, 16}).  A CTA owns 128 weight rows.
+// (Q4_K's weights d*sc*q - dmin*mn have no exact bfloat16 code, and the
+// split a*sum(q*x) - b*sum(x) misses the tolerance where the two terms
+// cancel and turns an infinite input into NaN, so Q4_K stays on the
+// lanes-over-rows kernel, which dequantizes each weight exactly.)
 constexpr int kTcRows = 128;
 __host__ __device__ constexpr bool tc_format(int wt) { return wt == kQ8_0 || wt == kQ5_0 || wt == kQ6_K; }
-__host__ __device__ constexpr int tc_max_mp(int) { return 16; }
+// Q6_K's 16-value sub-blocks take twice the accumulator columns per unit, so
+// its widest tile is 16 input rows; the formats with 32-value scale blocks go
+// to 32.
+__host__ __device__ constexpr int tc_max_mp(int wt) { return wt == kQ6_K ? 16 : 32; }
 // K-steps (16 values) per scale block: Q6_K sub-blocks of 16, Q8_0 / Q5_0 blocks of 32.
 __host__ __device__ constexpr int tc_kpb(int wt) { return wt == kQ6_K ? 1 : 2; }
 // K-steps of a 64-value unit each consumer warp decodes: two (8 consumer

@@ -895,6 +895,21 @@ __device__ __forceinline__ void stage_x_plain(float* dst, const float* xb, uint3
     }
 }
 
+// Plain input staging for runtime m (the tensor-core kernel, whose tile is
+// wider than the launch's m): the [m][CV] slice of chunk cc, zero past k.
+template <int CV>
+__device__ __forceinline__ void stage_x_plain_m(float* dst, const float* xb, uint32_t xrs, uint32_t m, uint32_t cc,
+                                                uint32_t k, int lane) {
+    constexpr int Q = CV / 4;
+    for (int idx = lane; idx < static_cast<int>(m) * Q; idx += 32) {
+        const int j = idx / Q, q = idx - (idx / Q) * Q;
+        const uint32_t col = cc * CV + 4u * q;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < k) v = ldg4(xb + static_cast<uint64_t>(j) * xrs + col);
+        *reinterpret_cast<float4*>(dst + j * CV + 4 * q) = v;
+    }
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_rank() {

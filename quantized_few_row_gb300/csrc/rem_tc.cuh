@@ -437,21 +437,6 @@ __device__ __forceinline__ void tc_convert_x(const float* xs, uint8_t* bt, uint3
     }
 }
 
-// Plain input staging for runtime m (the TMA path needs 16-byte aligned
-// weight rows): the [m][CV] slice of chunk cc, zero past k.
-template <int CV>
-__device__ __forceinline__ void stage_x_plain_m(float* dst, const float* xb, uint32_t xrs, uint32_t m, uint32_t cc,
-                                                uint32_t k, int lane) {
-    constexpr int Q = CV / 4;
-    for (int idx = lane; idx < static_cast<int>(m) * Q; idx += 32) {
-        const int j = idx / Q, q = idx - (idx / Q) * Q;
-        const uint32_t col = cc * CV + 4u * q;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (col < k) v = ldg4(xb + static_cast<uint64_t>(j) * xrs + col);
-        *reinterpret_cast<float4*>(dst + j * CV + 4 * q) = v;
-    }
-}
-
 // 8*KPW columns of the warp's 32 lanes.
 template <int KPW>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[8 * KPW]) {
@@ -888,6 +873,7 @@ inline const void* tc_kernel_ptr() {
 #define REM_TC_INSTANTIATE(WT, NAME)                                    \
     namespace rem {                                                     \
     const void* NAME(int mp) {                                          \
-        return mp == 8 ? tc_kernel_ptr<WT, 8>() : mp == 16 ? tc_kernel_ptr<WT, 16>() : nullptr; \
+        return mp == 8 ? tc_kernel_ptr<WT, 8>() : mp == 16 ? tc_kernel_ptr<WT, 16>()                 \
+               : mp == 32 ? tc_kernel_ptr<WT, 32>() : nullptr;                                        \
     }                                                                   \
     }

@@ -35,6 +35,8 @@ pytestmark = pytest.mark.gpu
 
 FMTS = ["f16", "bf16", "f32", "q8_0", "q5_0", "q4_K", "q6_K"]
 TC = ("q8_0", "q5_0", "q6_K")
+# tensor-core tile widths: 32 input rows where a scale block is 32 values, 16 for Q6_K
+TC_MAX = {"q8_0": 32, "q5_0": 32, "q6_K": 16}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -161,7 +163,7 @@ def test_exact_arithmetic_is_bitwise(fmt, engine, lit):
     n = 150                                          # two tiles of 128 rows with a ragged tail
     k = {"f16": 520, "bf16": 520, "f32": 520}.get(fmt, 512)
     w, xmax = exact_weights(fmt, n, k, 700 + FMTS.index(fmt) + (50 if lit else 0), lit)
-    ms = [1, 3, 8] + ([12, 16, 23] if engine == rem.ENGINE_TC else [])
+    ms = [1, 3, 8] + ([12, 16, 23] + ([29] if TC_MAX[fmt] == 32 else []) if engine == rem.ENGINE_TC else [])
     mmax = max(ms)
     x = inputs.small_ints((mmax, k), 701, -xmax, xmax)
     y_ref, _ = oracle.matvec(w, fmt, n, k, 1, x, mmax, k, 0)
@@ -235,7 +237,8 @@ def test_q4k_cancelling_mins_match_oracle():
         for layout in (0, 1, 2):
             if layout == 2 and m < 2:
                 continue
-            y = H.run_sched(w, "q4_K", n, k, 1, x[:m], m, k, 0, n, 0, m * n, rem.Schedule(layout=layout))
+            y = H.run_sched(w, "q4_K", n, k, 1, x[:m], m, k, 0, n, 0, m * n,
+                            rem.Schedule(layout=layout, engine=rem.ENGINE_SIMT))
             H.assert_close_to_oracle(y.reshape(1, m, n), y_ref[:, :m], a_ref[:, :m], f"q4_K cancel m={m} l={layout}")
 
 
@@ -291,15 +294,16 @@ def test_infinite_input_stays_in_its_row(fmt, engine):
 @pytest.mark.parametrize("fmt", TC)
 def test_tc_rows_bitwise_equal_for_every_m(fmt):
     """On the tensor-core engine row j is the same bits for every m, including
-    launches of 9..16 input rows (the wider tile) and calls of more rows (two
-    launches), and equal to the oracle within tolerance."""
+    launches of 9..16 and 17..32 input rows (the wider tiles) and calls of
+    more rows than one launch takes, and equal to the oracle within
+    tolerance."""
     n, k = 200, 1024
-    mmax = 24
+    mmax = 40
     w, x = H.contiguous(fmt, n, k, mmax, 760, 761)
     y_ref, a_ref = oracle.matvec(w, fmt, n, k, 1, x, mmax, k, 0)
     tc = rem.Schedule(engine=rem.ENGINE_TC)
     alone = [H.run_sched(w, fmt, n, k, 1, x[j:j + 1], 1, k, 0, n, 0, n, tc) for j in range(mmax)]
-    for m in (1, 2, 3, 5, 8, 9, 12, 16, 17, 24):
+    for m in (1, 2, 3, 5, 8, 9, 12, 16, 17, 24, 31, 32, 40):
         y = H.run_sched(w, fmt, n, k, 1, x[:m], m, k, 0, n, 0, m * n, tc).reshape(m, n)
         H.assert_close_to_oracle(y[None], y_ref[:, :m], a_ref[:, :m], f"{fmt} m={m}")
         for j in range(m):
