@@ -390,10 +390,15 @@ struct TcGeom {
     static constexpr int DCOLS = tc_regions(WT, MP) * NCOL; // D columns per slot
     static constexpr int TCOLS = tc_tmem_cols(WT, MP);      // tensor memory allocated
     static constexpr int THREADS = tc_threads(MP);
+    // units a consumer warp takes per step (their slot waits, tensor-memory
+    // stores and loads and hand-overs issued together): two where the ring
+    // holds two steps and the accumulators of two units fit in registers
+    static constexpr int BATCH = (NS >= 4 && RPW * NCOL <= 32) ? 2 : 1;
     static_assert(F::kUPC == tc_units_per_chunk(WT), "units per chunk");
     static_assert(F::kUPC % NS == 0, "units per chunk must be a multiple of the slots");
     static_assert(KPW == 2 && RK == F::kRK && RPW * RK == KPW, "two K-steps per warp and unit, kRK per region");
     static_assert(NS * (ACOLS + DCOLS) <= TCOLS, "slots exceed the tensor memory");
+    static_assert(F::kUPC % BATCH == 0 && NS % BATCH == 0, "steps of whole units");
 };
 
 // Consumer-side conversion of one chunk's inputs ([m][CV] binary32 at xs) into
@@ -728,9 +733,30 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     // ---------------------------------------------------- consumers
     const int quarter = warp & 3, grp = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;  // this warp's TMEM lanes
+    constexpr int BATCH = G::BATCH;
+    // the words of unit b of a step come from Regs R[b] where every unit loads
+    // its own, else all from R[0] (loaded once per chunk)
+    constexpr bool kPerUnit = F::kLoad(1);
+    constexpr int kOpenAt = 1;
     bool failed = false;
-    uint32_t i = 0;   // stages consumed
+    int st = 0;       // stage of the current chunk
+    uint32_t ph = 0;  // its full-barrier parity
     uint32_t gc = 0;  // chunks over all tiles
+    // wait for stage `sq`, convert its inputs into B tile buffer `bsel`, and
+    // load unit 0's words of chunk q of the K range into r
+    auto open_chunk = [&](int sq, uint32_t phase, int q, uint32_t bsel, typename F::Regs& r) {
+        if (!failed && !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * sq, phase, a.wait_ns))) {
+            failed = true;
+            if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
+        }
+        if (failed) return;
+        const uint8_t* sp = smem + sq * STAGE;
+        tc_convert_x<WT, MP>(reinterpret_cast<const float*>(sp + WSTAGE), btiles + bsel * G::BCHUNK, m,
+                             static_cast<int>(threadIdx.x));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        F::template load<0>(sp + (quarter * 32 + lane) * BOX, Stage<WT>::sofs(c0 + static_cast<uint32_t>(q)), grp,
+                            r);
+    };
     for (uint32_t rb = cid, t = 0; rb < nblocks; rb += ncl, ++t) {
         uint32_t b, row0;
         block_origin(rb, b, row0);
@@ -759,62 +785,87 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                                                                            (KPW * grp / RK) * G::NCOL),
                                    d);
         };
-        for (int q = 0; q < nck; ++q, ++i, ++gc) {
-            const int st = static_cast<int>(i % D);
-            if (!failed &&
-                !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, static_cast<uint32_t>((i / D) & 1), a.wait_ns))) {
-                failed = true;
-                if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
-            }
-            if (failed) continue;
-            const uint8_t* sp = smem + st * STAGE;
-            // this chunk's inputs -> B tiles (the MMAs of the chunk two back,
-            // which read this buffer, were all observed complete: every unit
-            // of that chunk has had its epilogue)
-            tc_convert_x<WT, MP>(reinterpret_cast<const float*>(sp + WSTAGE), btiles + (gc & 1u) * G::BCHUNK, m,
-                                 static_cast<int>(threadIdx.x));
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            const uint8_t* row = sp + (quarter * 32 + lane) * BOX;
+        typename F::Regs R[kPerUnit ? BATCH : 1];
+        // the first chunk of the tile; each later one is opened during the
+        // last step of the one before, while that step's tensor-memory loads
+        // are in flight
+        if (nck > 0) open_chunk(st, ph, 0, gc & 1u, R[0]);
+        for (int q = 0; q < nck; ++q, ++gc) {
+            if (failed) break;
+            const uint8_t* row = smem + st * STAGE + (quarter * 32 + lane) * BOX;
             const int o = Stage<WT>::sofs(c0 + static_cast<uint32_t>(q));
-            typename F::Regs R;
-            static_for<0, UPC>([&](auto u_) {
-                constexpr int U = decltype(u_)::value, SL = U % NS;
+            const bool more = q + 1 < nck;
+            const int st1 = st + 1 == D ? 0 : st + 1;
+            const uint32_t ph1 = st + 1 == D ? ph ^ 1u : ph;
+            static_for<0, UPC / BATCH>([&](auto p_) {
+                constexpr int U0 = BATCH * decltype(p_)::value;
+                constexpr bool kLast = U0 + BATCH == UPC;
                 if (failed) return;
-                if constexpr (F::kLoad(U)) F::template load<U>(row, o, grp, R);
-                if constexpr (U == F::kLastLoad) {
+                static_for<0, BATCH>([&](auto b_) {
+                    constexpr int U = U0 + decltype(b_)::value;
+                    if constexpr (U > 0 && F::kLoad(U)) F::template load<U>(row, o, grp, R[kPerUnit ? U - U0 : 0]);
+                });
+                if constexpr (U0 <= F::kLastLoad && F::kLastLoad < U0 + BATCH) {
                     // the staged weights and inputs of this chunk are all read
                     __syncwarp();
                     if (lane == 0) mbar_arrive(eb + 8 * st);
                 }
-                const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(U / NS);
-                const bool pending = q > 0 || U >= NS;  // slot SL holds an earlier unit of this tile
-                // The unit's codes are decoded into registers while the
-                // slot's previous MMAs may still run (the pin keeps the
-                // decode from moving ahead of the previous unit), then the
-                // slot is taken over: its old D read out and scaled, the new
-                // codes stored and the slot handed to the MMA warps.
-                uint32_t av[8 * KPW];
-                float nsc[RPW];
-                F::pin(R);
-                F::template decode<U>(R, av, nsc);
+                const uint32_t use0 = gc * (UPC / NS) + static_cast<uint32_t>(U0 / NS);
+                const bool pending = q > 0 || U0 >= NS;  // the step's slots hold earlier units of this tile
+                // The units' codes are decoded into registers while the
+                // slots' previous MMAs may still run (the pin keeps the
+                // decode from moving ahead of the previous step), then the
+                // slots are taken over: their old D read out and scaled, the
+                // new codes stored and the slots handed to the MMA warps.
+                uint32_t av[BATCH][8 * KPW];
+                float nsc[BATCH][RPW];
+#pragma unroll
+                for (int bb = 0; bb < (kPerUnit ? BATCH : 1); ++bb) F::pin(R[bb]);
+                static_for<0, BATCH>([&](auto b_) {
+                    constexpr int BI = decltype(b_)::value;
+                    F::template decode<U0 + BI>(R[kPerUnit ? BI : 0], av[BI], nsc[BI]);
+                });
                 if (pending) {
-                    wait_d(SL, use - 1u);
+#pragma unroll
+                    for (int bb = 0; bb < BATCH; ++bb) wait_d((U0 + bb) % NS, use0 - 1u);
                     if (failed) return;
                 }
-                tmem_st_cols<KPW>(tmem + lane_base + static_cast<uint32_t>(SL * G::ACOLS + 8 * KPW * grp), av);
+#pragma unroll
+                for (int bb = 0; bb < BATCH; ++bb)
+                    tmem_st_cols<KPW>(tmem + lane_base + static_cast<uint32_t>(((U0 + bb) % NS) * G::ACOLS + 8 * KPW * grp),
+                                      av[bb]);
+                uint32_t d[BATCH][RPW * G::NCOL];
                 if (pending) {
-                    uint32_t d[RPW * G::NCOL];
-                    load_d(SL, d);
+#pragma unroll
+                    for (int bb = 0; bb < BATCH; ++bb) load_d((U0 + bb) % NS, d[bb]);
+                }
+                if constexpr (kLast && kOpenAt == 0) {
+                    // every MMA of the chunk before this one has been seen
+                    // complete, so its B tile buffer takes the next chunk's
+                    if (more) open_chunk(st1, ph1, q + 1, (gc + 1u) & 1u, R[0]);
+                }
+                if (pending) {
                     tmem_ld_wait();
-                    tc_scale<MP, RPW>(d, psc[SL], m, acc);
+#pragma unroll
+                    for (int bb = 0; bb < BATCH; ++bb) tc_scale<MP, RPW>(d[bb], psc[(U0 + bb) % NS], m, acc);
                 }
 #pragma unroll
-                for (int bb = 0; bb < RPW; ++bb) psc[SL][bb] = nsc[bb];
+                for (int bb = 0; bb < BATCH; ++bb)
+#pragma unroll
+                    for (int r = 0; r < RPW; ++r) psc[(U0 + bb) % NS][r] = nsc[bb][r];
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(ab + 8 * SL);
+                if (lane == 0) {
+#pragma unroll
+                    for (int bb = 0; bb < BATCH; ++bb) mbar_arrive(ab + 8 * ((U0 + bb) % NS));
+                }
+                if constexpr (kLast && kOpenAt == 1) {
+                    if (more) open_chunk(st1, ph1, q + 1, (gc + 1u) & 1u, R[0]);
+                }
             });
+            st = st1;
+            ph = ph1;
         }
         // drain: the last unit of every slot
         if (nck > 0) {
