@@ -399,6 +399,11 @@ struct TcGeom {
     static_assert(KPW == 2 && RK == F::kRK && RPW * RK == KPW, "two K-steps per warp and unit, kRK per region");
     static_assert(NS * (ACOLS + DCOLS) <= TCOLS, "slots exceed the tensor memory");
     static_assert(F::kUPC % BATCH == 0 && NS % BATCH == 0, "steps of whole units");
+    // step slots: the BATCH consecutive slots of a step share one A-ready and
+    // one D-ready barrier, and one MMA warp issues the step's MMAs
+    static constexpr int NSS = NS / BATCH;
+    static constexpr int SPC = F::kUPC / BATCH;  // steps per chunk
+    static_assert(SPC % NSS == 0, "steps per chunk must be a multiple of the step slots");
 };
 
 // Consumer-side conversion of one chunk's inputs ([m][CV] binary32 at xs) into
@@ -503,7 +508,8 @@ __device__ __forceinline__ void tc_scale(const uint32_t (&d)[RPW * 2 * MP], cons
 // lane quarter) and, as warp group g = w/4, the K-steps kstep(u, 2g) and
 // kstep(u, 2g+1) of every unit u with their accumulator regions.  Warp CW is
 // the producer (TMA or plain staging of weights and inputs); warps CW+1 and
-// CW+2 issue the MMAs of the even and the odd slots, and warp CW+1 owns the
+// CW+2 issue the MMAs of the even and the odd step slots (a step is the
+// one or two units the consumers hand over together), and warp CW+1 owns the
 // tensor memory.  The warps of one lane quarter accumulate separately; at the
 // end of a tile their partials are added in warp-group order.
 template <int WT, int MP>
@@ -514,7 +520,8 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     constexpr int NS = G::NS, UPC = F::kUPC, KPW = G::KPW, RK = G::RK, RPW = G::RPW;
     constexpr int CV = G::CV, BOX = G::BOX, ROWS = 128;
     constexpr int CW = G::CW, PRODUCER = CW, ISSUER = CW + 1, ISSUER2 = CW + 2;
-    static_assert(NS % 2 == 0, "the two MMA warps take alternate slots");
+    constexpr int NSS = G::NSS, SPC = G::SPC, BATCH = G::BATCH;
+    static_assert(NSS % 2 == 0, "the two MMA warps take alternate step slots");
     constexpr uint32_t XPAD = (MP * CV * 4 + 127u) & ~127u;
     constexpr uint32_t WSTAGE = ROWS * BOX;
     constexpr uint32_t STAGE = WSTAGE + XPAD;
@@ -562,7 +569,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             mbar_init(fb + 8 * t, a.aligned ? 1u : 32u);
             mbar_init(eb + 8 * t, static_cast<uint32_t>(CW));
         }
-        for (int t = 0; t < NS; ++t) {
+        for (int t = 0; t < NSS; ++t) {
             mbar_init(ab + 8 * t, static_cast<uint32_t>(CW));
             mbar_init(db + 8 * t, 1u);
         }
@@ -669,11 +676,11 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 
     if (warp == ISSUER || warp == ISSUER2) {
         // ------------------------------------------------ MMA issuers
-        // Two warps issue the MMAs, the first for the even slots, the second
-        // for the odd ones: a commit and the wait on it before a slot is
-        // reused hold up only the units of that warp, so the other warp's
+        // Two warps issue the MMAs, the first for the even step slots, the
+        // second for the odd ones: a commit and the wait on it before a slot
+        // is reused hold up only the steps of that warp, so the other warp's
         // MMAs keep the tensor pipe busy meanwhile.  Each warp walks all the
-        // units, so every operand is warp-uniform (the descriptors are a base
+        // steps, so every operand is warp-uniform (the descriptors are a base
         // plus compile-time steps); its lane 0 issues.
         const int par = warp - ISSUER;
         bool failed = false;
@@ -685,25 +692,28 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         for (uint32_t rb = cid; rb < nblocks; rb += ncl, ++t) {
             for (int q = 0; q < nck && !failed; ++q, ++gc) {
                 const uint64_t bchunk = bdesc0 + static_cast<uint64_t>(((gc & 1u) * G::BCHUNK) >> 4);
-                static_for<0, UPC>([&](auto u_) {
-                    constexpr int U = decltype(u_)::value, SL = U % NS;
-                    if (SL % 2 != par || failed) return;
-                    const uint32_t use = gc * (UPC / NS) + static_cast<uint32_t>(U / NS);
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(ab + 8 * SL, use & 1u, a.wait_ns))) {
+                static_for<0, SPC>([&](auto p_) {
+                    constexpr int P = decltype(p_)::value, SS = P % NSS;
+                    if (SS % 2 != par || failed) return;
+                    const uint32_t use = gc * (SPC / NSS) + static_cast<uint32_t>(P / NSS);
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(ab + 8 * SS, use & 1u, a.wait_ns))) {
                         if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
                         failed = true;
                         return;
                     }
                     tc_fence_after();
-                    const uint32_t ac = tmem + static_cast<uint32_t>(SL * G::ACOLS);
-                    const uint32_t dc = tmem + static_cast<uint32_t>(NS * G::ACOLS + SL * G::DCOLS);
                     if (lane == 0) {
+                        static_for<0, BATCH>([&](auto b_) {
+                            constexpr int U = P * BATCH + decltype(b_)::value, SL = U % NS;
+                            const uint32_t ac = tmem + static_cast<uint32_t>(SL * G::ACOLS);
+                            const uint32_t dc = tmem + static_cast<uint32_t>(NS * G::ACOLS + SL * G::DCOLS);
 #pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            tc_mma(dc + static_cast<uint32_t>((k4 / RK) * G::NCOL), ac + 8u * k4,
-                                   bchunk + static_cast<uint64_t>((F::kstep(U, k4) * G::BKSTEP) >> 4), idesc,
-                                   (k4 % RK) != 0);
-                        tc_commit(db + 8 * SL);
+                            for (int k4 = 0; k4 < 4; ++k4)
+                                tc_mma(dc + static_cast<uint32_t>((k4 / RK) * G::NCOL), ac + 8u * k4,
+                                       bchunk + static_cast<uint64_t>((F::kstep(U, k4) * G::BKSTEP) >> 4), idesc,
+                                       (k4 % RK) != 0);
+                        });
+                        tc_commit(db + 8 * SS);
                     }
                     __syncwarp();
                     issued_any = true;
@@ -733,7 +743,6 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     // ---------------------------------------------------- consumers
     const int quarter = warp & 3, grp = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;  // this warp's TMEM lanes
-    constexpr int BATCH = G::BATCH;
     // the words of unit b of a step come from Regs R[b] where every unit loads
     // its own, else all from R[0] (loaded once per chunk)
     constexpr bool kPerUnit = F::kLoad(1);
@@ -769,10 +778,11 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         for (int j = 0; j < NS; ++j)
 #pragma unroll
             for (int b = 0; b < RPW; ++b) psc[j][b] = 0.0f;
-        // the slot's MMAs (use number `use`) have completed: its D is ready, its A is free
-        auto wait_d = [&](int sl, uint32_t use) {
+        // the step slot's MMAs (use number `use`) have completed: its D is
+        // ready, its A is free
+        auto wait_d = [&](int ss, uint32_t use) {
             if (failed) return;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(db + 8 * sl, use & 1u, a.wait_ns))) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(db + 8 * ss, use & 1u, a.wait_ns))) {
                 failed = true;
                 if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
                 return;
@@ -797,8 +807,8 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             const bool more = q + 1 < nck;
             const int st1 = st + 1 == D ? 0 : st + 1;
             const uint32_t ph1 = st + 1 == D ? ph ^ 1u : ph;
-            static_for<0, UPC / BATCH>([&](auto p_) {
-                constexpr int U0 = BATCH * decltype(p_)::value;
+            static_for<0, SPC>([&](auto p_) {
+                constexpr int P = decltype(p_)::value, SS = P % NSS, U0 = BATCH * P;
                 constexpr bool kLast = U0 + BATCH == UPC;
                 if (failed) return;
                 static_for<0, BATCH>([&](auto b_) {
@@ -810,8 +820,8 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     __syncwarp();
                     if (lane == 0) mbar_arrive(eb + 8 * st);
                 }
-                const uint32_t use0 = gc * (UPC / NS) + static_cast<uint32_t>(U0 / NS);
-                const bool pending = q > 0 || U0 >= NS;  // the step's slots hold earlier units of this tile
+                const uint32_t use = gc * (SPC / NSS) + static_cast<uint32_t>(P / NSS);
+                const bool pending = q > 0 || P >= NSS;  // the step's slots hold earlier units of this tile
                 // The units' codes are decoded into registers while the
                 // slots' previous MMAs may still run (the pin keeps the
                 // decode from moving ahead of the previous step), then the
@@ -826,8 +836,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     F::template decode<U0 + BI>(R[kPerUnit ? BI : 0], av[BI], nsc[BI]);
                 });
                 if (pending) {
-#pragma unroll
-                    for (int bb = 0; bb < BATCH; ++bb) wait_d((U0 + bb) % NS, use0 - 1u);
+                    wait_d(SS, use - 1u);
                     if (failed) return;
                 }
 #pragma unroll
@@ -856,10 +865,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-#pragma unroll
-                    for (int bb = 0; bb < BATCH; ++bb) mbar_arrive(ab + 8 * ((U0 + bb) % NS));
-                }
+                if (lane == 0) mbar_arrive(ab + 8 * SS);
                 if constexpr (kLast && kOpenAt == 1) {
                     if (more) open_chunk(st1, ph1, q + 1, (gc + 1u) & 1u, R[0]);
                 }
@@ -867,16 +873,19 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             st = st1;
             ph = ph1;
         }
-        // drain: the last unit of every slot
+        // drain: the last step of every step slot, in unit order
         if (nck > 0) {
-            static_for<0, NS>([&](auto s_) {
-                constexpr int SL = decltype(s_)::value;
-                wait_d(SL, (gc - 1u) * (UPC / NS) + static_cast<uint32_t>((UPC - NS + SL) / NS));
+            static_for<0, NSS>([&](auto s_) {
+                constexpr int SS = decltype(s_)::value;
+                wait_d(SS, (gc - 1u) * (SPC / NSS) + static_cast<uint32_t>((SPC - NSS + SS) / NSS));
                 if (failed) return;
-                uint32_t d[RPW * G::NCOL];
-                load_d(SL, d);
-                tmem_ld_wait();
-                tc_scale<MP, RPW>(d, psc[SL], m, acc);
+                static_for<0, BATCH>([&](auto b_) {
+                    constexpr int SL = SS * BATCH + decltype(b_)::value;
+                    uint32_t d[RPW * G::NCOL];
+                    load_d(SL, d);
+                    tmem_ld_wait();
+                    tc_scale<MP, RPW>(d, psc[SL], m, acc);
+                });
             });
         }
         // the other warp groups' partials join group 0's, in group order
