@@ -179,9 +179,11 @@ int device_state(DeviceState** out, int* dev_out) {
                     st.max_threads[wt][m][l] = fa.maxThreadsPerBlock;
                 }
             if (tc_format(wt))
-                for (int mp = 8; mp <= tc_max_mp(wt); mp *= 2) {
-                    const void* fn = tc_kernel(wt, mp);
-                    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                for (int mp = 8; mp <= tc_max_mp(wt); mp *= 2)
+                    for (int cm = 0; cm < 2; ++cm) {
+                    const void* fn = tc_kernel(wt, mp, cm != 0);
+                    if (!fn) continue;  // not every width takes both conversion modes
+                    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                     st.smem_optin) != cudaSuccess) {
                         cudaGetLastError();
                         return fail(REM_ECUDA, "rem_matvec: cannot prepare the %s tensor-core kernels on device %d",
@@ -413,6 +415,7 @@ struct Plan {
     int nr0 = 1, h = 1, warps = 4, stages = 2, smem = 0, threads = 0, mp = 8;
     uint32_t S = 1, cpb = 0, grid = 0, nchunk = 0;
     bool aligned = false, pdl = false, x_bm = false;
+    bool cm = false;     // tensor-core engine: the MMA warps convert the inputs (tc_conv_mma)
     char note[96] = "";  // planner diagnostics (tensor-core engine: CTAs per SM for each ring depth)
 };
 
@@ -554,7 +557,8 @@ int plan_simt(int dev, const DeviceState& ds, int wt, const Shape& s, const Sche
 int plan_tc(int dev, const DeviceState& ds, int wt, const Shape& s, Plan& p) {
     const uint32_t S = p.S;
     p.mp = s.m <= 8 ? 8 : s.m <= 16 ? 16 : 32;
-    p.fn = tc_kernel(wt, p.mp);
+    p.cm = tc_conv_mma(wt, s.m);
+    p.fn = tc_kernel(wt, p.mp, p.cm);
     if (!p.fn || p.mp > tc_max_mp(wt))
         return fail(REM_ELAUNCH, "rem_matvec: no %s tensor-core kernel for m = %u", wt_name(wt), s.m);
     p.threads = tc_threads(p.mp);
@@ -756,10 +760,10 @@ int launch_matvec(const void* W, int wt, const float* x, float* y, const Shape& 
         aligned = encode_map(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), gdim, gstride, box);
     }
     snprintf(g_plan, sizeof(g_plan),
-             "%s engine=%s m=%u n=%u k=%u batch=%u split=%u nr0=%d h=%d warps=%d mp=%d stages=%d smem=%d grid=%u "
+             "%s engine=%s m=%u n=%u k=%u batch=%u split=%u nr0=%d h=%d warps=%d mp=%d%s stages=%d smem=%d grid=%u "
              "row_blocks=%llu tma=%d pdl=%d occ=[%s ]",
              wt_name(wt), p.engine == REM_ENGINE_TC ? "tc" : "simt", s.m, s.n, s.k, s.batch, p.S, p.nr0, p.h, p.warps,
-             p.mp, p.stages, p.smem, p.grid, static_cast<unsigned long long>(p.cpb) * s.batch,
+             p.mp, p.engine == REM_ENGINE_TC ? (p.cm ? " xconv=mma" : " xconv=consumers") : "", p.stages, p.smem, p.grid, static_cast<unsigned long long>(p.cpb) * s.batch,
              static_cast<int>(aligned), static_cast<int>(p.pdl), p.note);
 
     MvArgs a{};
@@ -902,11 +906,11 @@ const void* mv_kernel(int wt, int m, int layout) {
     }
 }
 
-const void* tc_kernel(int wt, int mp) {
+const void* tc_kernel(int wt, int mp, bool cm) {
     switch (wt) {
-    case kQ8_0: return tc_kernel_q8_0(mp);
-    case kQ5_0: return tc_kernel_q5_0(mp);
-    case kQ6_K: return tc_kernel_q6_k(mp);
+    case kQ8_0: return tc_kernel_q8_0(mp, cm);
+    case kQ5_0: return tc_kernel_q5_0(mp, cm);
+    case kQ6_K: return tc_kernel_q6_k(mp, cm);
     default: return nullptr;
     }
 }

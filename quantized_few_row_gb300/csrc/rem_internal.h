@@ -195,6 +195,14 @@ __host__ __device__ constexpr int tc_region_ksteps(int wt, int mp) {
 __host__ __device__ constexpr int tc_regions(int wt, int mp) { return 4 / tc_region_ksteps(wt, mp); }
 // Units of 64 values per staged chunk: Q8_0 2 (a chunk is 4 blocks), Q5_0 and Q6_K 4.
 __host__ __device__ constexpr int tc_units_per_chunk(int wt) { return wt == kQ8_0 ? 2 : 4; }
+// Whether the two MMA warps convert a chunk's inputs into its B tile (each
+// the K-steps of its own units; 4 * units-per-chunk 16-byte items per input
+// row between them) or the consumer warps do: the MMA warps while the items
+// stay few enough for them, measured per format.  The conversion is the same
+// arithmetic either way.
+__host__ __device__ constexpr bool tc_conv_mma(int wt, uint32_t m) {
+    return m * 4u * static_cast<uint32_t>(tc_units_per_chunk(wt)) <= (wt == kQ6_K ? 80u : 128u);
+}
 // Tensor-memory columns of one A/D slot: 32 columns of A (a unit as bf16
 // pairs) and one 2*mp-column accumulator per region of the unit.
 __host__ __device__ constexpr int tc_slot_cols(int wt, int mp) { return 32 + tc_regions(wt, mp) * 2 * mp; }
@@ -226,13 +234,14 @@ inline uint32_t tc_smem_bytes(int wt, int mp, int stages, int split) {
     const uint32_t groups = (uint32_t)tc_consumer_warps(mp) / 4u;
     const uint32_t pbuf = 2u * (groups - 1u) * 4u * (uint32_t)mp * 32u * 4u;
     (void)split;
-    // mbarriers: full and empty per stage, A full and D full per slot (4 + 4), a drain per MMA warp
-    return (uint32_t)stages * stage + btiles + pbuf + 8u * (4 * kMaxStages + 2) + 16u + 128u;
+    // mbarriers: full and empty per stage, A full and D full per step slot (4 + 4), a drain per
+    // MMA warp, a B-buffer release per MMA warp and buffer (2 x 2)
+    return (uint32_t)stages * stage + btiles + pbuf + 8u * (2 * kMaxStages + 4 + 4 + 2 + 4) + 16u + 128u;
 }
-const void* tc_kernel(int wt, int mp);
-const void* tc_kernel_q8_0(int mp);
-const void* tc_kernel_q5_0(int mp);
-const void* tc_kernel_q6_k(int mp);
+const void* tc_kernel(int wt, int mp, bool cm);
+const void* tc_kernel_q8_0(int mp, bool cm);
+const void* tc_kernel_q5_0(int mp, bool cm);
+const void* tc_kernel_q6_k(int mp, bool cm);
 
 // Auxiliary kernels (dequantize / quantize), rem_aux.cu.
 int launch_dequantize(const uint8_t* w, int wt, uint64_t rows, uint32_t k, uint64_t row_bytes,

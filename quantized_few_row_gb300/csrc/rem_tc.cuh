@@ -406,12 +406,12 @@ struct TcGeom {
     static_assert(SPC % NSS == 0, "steps per chunk must be a multiple of the step slots");
 };
 
-// Consumer-side conversion of one chunk's inputs ([m][CV] binary32 at xs) into
-// the B tiles at bt: K-step s, logical value v (A column order) of input row
-// j -> x_hi at tile row j, x_lo at tile row MP + j.  Work item = one 16-byte
-// row of a core matrix (8 logical values of one input row): items of input
-// row j are 32*j .. 32*j + 2*KSTEPS - 1, spread over the consumer warps.
-// Rows m..MP-1 stay zero.
+// Conversion of one chunk's inputs ([m][CV] binary32 at xs) into the B tiles
+// at bt by the consumer warps: K-step s, logical value v (A column order) of
+// input row j -> x_hi at tile row j, x_lo at tile row MP + j.  Work item =
+// one 16-byte row of a core matrix (8 logical values of one input row):
+// items of input row j are 32*j .. 32*j + 2*KSTEPS - 1, spread over the
+// consumer warps.  Rows m..MP-1 stay zero.
 template <int WT, int MP>
 __device__ __forceinline__ void tc_convert_x(const float* xs, uint8_t* bt, uint32_t m, int tid) {
     using G = TcGeom<WT, MP>;
@@ -439,6 +439,49 @@ __device__ __forceinline__ void tc_convert_x(const float* xs, uint8_t* bt, uint3
             // x_lo = bf16_rn(x - x_hi); zero where x is not finite (x_hi keeps inf / NaN)
             const float r0 = (b0 & 0x7F800000u) == 0x7F800000u ? 0.0f : __fsub_rn(e[2 * p], __uint_as_float(b0 & 0xFFFF0000u));
             const float r1 = (b1 & 0x7F800000u) == 0x7F800000u ? 0.0f : __fsub_rn(e[2 * p + 1], __uint_as_float(b1 & 0xFFFF0000u));
+            lo[p] = bf16x2_rn(r0, r1);
+        }
+        uint8_t* dst = bt + s * G::BKSTEP + (j >> 3) * 256 + kh * 128 + (j & 7) * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(dst + (MP / 8) * 256) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// One MMA warp's share of a chunk's inputs ([m][CV] binary32 at xs) in the B
+// tiles at bt: the K-steps of the units that warp issues (its step slots),
+// so no other warp's MMAs read what it writes.  K-step s, logical value v (A
+// column order) of input row j -> x_hi at tile row j, x_lo at tile row MP +
+// j.  Work item = one 16-byte row of a core matrix (8 logical values of one
+// input row); rows m..MP-1 stay zero.
+template <int WT, int MP>
+__device__ __forceinline__ void tc_convert_x_part(const float* xs, uint8_t* bt, uint32_t m, int lane, int par) {
+    using G = TcGeom<WT, MP>;
+    using F = TcFmt<WT>;
+    constexpr int NU = F::kUPC / 2;                         // units of one MMA warp per chunk
+    constexpr int PER = 8 * NU;                             // items per input row: 4 K-steps x 2 halves per unit
+    static_assert((PER & (PER - 1)) == 0, "items per row a power of two");
+    for (int it = lane; it < static_cast<int>(m) * PER; it += kLanes) {
+        const int j = it / PER, e = it % PER;
+        const int ui = e >> 3, k4 = (e >> 1) & 3, kh = e & 1;
+        // the warp's steps are those of parity par (the step slots alternate)
+        const int u = (2 * (ui / G::BATCH) + par) * G::BATCH + ui % G::BATCH;
+        const int s = F::kstep(u, k4);
+        const float* src = xs + j * G::CV + 16 * s + 8 * kh;
+        const float4 a4 = ldx4(src), b4 = ldx4(src + 4);
+        float x[8];
+        if constexpr (F::kPerm == 1) {
+            x[0] = a4.x; x[1] = a4.z; x[2] = a4.y; x[3] = a4.w; x[4] = b4.x; x[5] = b4.z; x[6] = b4.y; x[7] = b4.w;
+        } else {
+            x[0] = a4.x; x[1] = a4.y; x[2] = a4.z; x[3] = a4.w; x[4] = b4.x; x[5] = b4.y; x[6] = b4.z; x[7] = b4.w;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t b0 = __float_as_uint(x[2 * p]), b1 = __float_as_uint(x[2 * p + 1]);
+            hi[p] = __byte_perm(b0, b1, 0x7632);     // upper halves: x_hi of both values
+            // x_lo = bf16_rn(x - x_hi); zero where x is not finite (x_hi keeps inf / NaN)
+            const float r0 = (b0 & 0x7F800000u) == 0x7F800000u ? 0.0f : __fsub_rn(x[2 * p], __uint_as_float(b0 & 0xFFFF0000u));
+            const float r1 = (b1 & 0x7F800000u) == 0x7F800000u ? 0.0f : __fsub_rn(x[2 * p + 1], __uint_as_float(b1 & 0xFFFF0000u));
             lo[p] = bf16x2_rn(r0, r1);
         }
         uint8_t* dst = bt + s * G::BKSTEP + (j >> 3) * 256 + kh * 128 + (j & 7) * 16;
@@ -512,7 +555,7 @@ __device__ __forceinline__ void tc_scale(const uint32_t (&d)[RPW * 2 * MP], cons
 // one or two units the consumers hand over together), and warp CW+1 owns the
 // tensor memory.  The warps of one lane quarter accumulate separately; at the
 // end of a tile their partials are added in warp-group order.
-template <int WT, int MP>
+template <int WT, int MP, bool CM>
 __global__ void __launch_bounds__(TcGeom<WT, MP>::THREADS, 1)
 rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, const MvArgs a) {
     using G = TcGeom<WT, MP>;
@@ -521,6 +564,12 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     constexpr int CV = G::CV, BOX = G::BOX, ROWS = 128;
     constexpr int CW = G::CW, PRODUCER = CW, ISSUER = CW + 1, ISSUER2 = CW + 2;
     constexpr int NSS = G::NSS, SPC = G::SPC, BATCH = G::BATCH;
+    // who converts a chunk's inputs into its B tile (CM, chosen by the host
+    // from the number of input rows, tc_conv_mma): the two MMA warps, each
+    // the K-steps of its own units between its steps, off the consumers'
+    // path; or, for more rows, the consumer warps, where the work spreads
+    // over all four SM sub-partitions
+
     static_assert(NSS % 2 == 0, "the two MMA warps take alternate step slots");
     constexpr uint32_t XPAD = (MP * CV * 4 + 127u) & ~127u;
     constexpr uint32_t WSTAGE = ROWS * BOX;
@@ -552,7 +601,10 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     uint64_t* afull = empty + kMaxStages;
     uint64_t* dfull = afull + 4;
     uint64_t* drain = dfull + 4;   // [2], one per MMA warp
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 2);
+    // [2][2]: MMA warp p's MMAs of the chunks of parity b have completed (the
+    // readers of B tile buffer b, for that warp's K-steps)
+    uint64_t* bfree = drain + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bfree + 4);
     const uint32_t c0 = static_cast<uint32_t>((static_cast<uint64_t>(s) * a.nchunk) / S);
     const uint32_t c1 = static_cast<uint32_t>((static_cast<uint64_t>(s + 1) * a.nchunk) / S);
     const int nck = static_cast<int>(c1 - c0);
@@ -567,7 +619,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int t = 0; t < D; ++t) {
             mbar_init(fb + 8 * t, a.aligned ? 1u : 32u);
-            mbar_init(eb + 8 * t, static_cast<uint32_t>(CW));
+            mbar_init(eb + 8 * t, static_cast<uint32_t>(CW + 2));  // consumers and the two MMA warps
         }
         for (int t = 0; t < NSS; ++t) {
             mbar_init(ab + 8 * t, static_cast<uint32_t>(CW));
@@ -575,6 +627,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         }
         mbar_init(smem_u32(drain), 1u);
         mbar_init(smem_u32(drain + 1), 1u);
+        for (int t = 0; t < 4; ++t) mbar_init(smem_u32(bfree + t), 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // the B tiles' rows m..MP-1 stay zero for the whole launch
@@ -689,9 +742,34 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         uint32_t t = 0;
         constexpr uint32_t idesc = tc_idesc(G::NCOL);
         const uint64_t bdesc0 = tc_bdesc(__shfl_sync(0xFFFFFFFFu, smem_u32(btiles), 0));
+        int st = 0;       // stage of the current chunk
+        uint32_t ph = 0;  // its full-barrier parity
         for (uint32_t rb = cid; rb < nblocks; rb += ncl, ++t) {
             for (int q = 0; q < nck && !failed; ++q, ++gc) {
                 const uint64_t bchunk = bdesc0 + static_cast<uint64_t>(((gc & 1u) * G::BCHUNK) >> 4);
+                // where the MMA warps convert: this warp's K-steps of the
+                // chunk's inputs -> B tile buffer gc & 1, once the chunk is
+                // staged and this warp's MMAs of chunk gc - 2 (the buffer's
+                // last readers of those K-steps) have completed
+                const uint32_t bf = smem_u32(bfree + 2 * par + static_cast<int>(gc & 1u));
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, ph, a.wait_ns)) ||
+                    (CM && gc >= 2u &&
+                     !__all_sync(0xFFFFFFFFu, mbar_wait(bf, ((gc >> 1) - 1u) & 1u, a.wait_ns)))) {
+                    if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
+                    failed = true;
+                    break;
+                }
+                if constexpr (CM) {
+                    tc_convert_x_part<WT, MP>(reinterpret_cast<const float*>(smem + st * STAGE + WSTAGE),
+                                              btiles + (gc & 1u) * G::BCHUNK, m, lane, par);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(eb + 8 * st);  // this warp has read the staged inputs
+                if (++st == D) {
+                    st = 0;
+                    ph ^= 1u;
+                }
                 static_for<0, SPC>([&](auto p_) {
                     constexpr int P = decltype(p_)::value, SS = P % NSS;
                     if (SS % 2 != par || failed) return;
@@ -718,6 +796,8 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     __syncwarp();
                     issued_any = true;
                 });
+                if (!failed && lane == 0) tc_commit(bf);
+                __syncwarp();
             }
             if (S > 1) {
                 if (t > 0) cluster_wait();
@@ -751,8 +831,9 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     int st = 0;       // stage of the current chunk
     uint32_t ph = 0;  // its full-barrier parity
     uint32_t gc = 0;  // chunks over all tiles
-    // wait for stage `sq`, convert its inputs into B tile buffer `bsel`, and
-    // load unit 0's words of chunk q of the K range into r
+    // wait for stage `sq`, convert its inputs into B tile buffer `bsel` where
+    // the consumers do that, and load unit 0's words of chunk q of the K
+    // range into r
     auto open_chunk = [&](int sq, uint32_t phase, int q, uint32_t bsel, typename F::Regs& r) {
         if (!failed && !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * sq, phase, a.wait_ns))) {
             failed = true;
@@ -760,9 +841,11 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         }
         if (failed) return;
         const uint8_t* sp = smem + sq * STAGE;
-        tc_convert_x<WT, MP>(reinterpret_cast<const float*>(sp + WSTAGE), btiles + bsel * G::BCHUNK, m,
-                             static_cast<int>(threadIdx.x));
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if constexpr (!CM) {
+            tc_convert_x<WT, MP>(reinterpret_cast<const float*>(sp + WSTAGE), btiles + bsel * G::BCHUNK, m,
+                                 static_cast<int>(threadIdx.x));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
         F::template load<0>(sp + (quarter * 32 + lane) * BOX, Stage<WT>::sofs(c0 + static_cast<uint32_t>(q)), grp,
                             r);
     };
@@ -849,8 +932,6 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     for (int bb = 0; bb < BATCH; ++bb) load_d((U0 + bb) % NS, d[bb]);
                 }
                 if constexpr (kLast && kOpenAt == 0) {
-                    // every MMA of the chunk before this one has been seen
-                    // complete, so its B tile buffer takes the next chunk's
                     if (more) open_chunk(st1, ph1, q + 1, (gc + 1u) & 1u, R[0]);
                 }
                 if (pending) {
@@ -917,23 +998,27 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 }  // namespace dev
 }  // namespace rem
 
-// Kernel pointer of rem_tc_kernel<WT, MP>, or nullptr where MP exceeds the
-// format's limit (tc_max_mp).
+// Kernel pointer of rem_tc_kernel<WT, MP, CM>, or nullptr where MP exceeds
+// the format's limit or no m of the width MP takes that conversion mode
+// (tc_conv_mma).
 namespace rem {
-template <int WT, int MP>
+template <int WT, int MP, bool CM>
 inline const void* tc_kernel_ptr() {
-    if constexpr (MP > tc_max_mp(WT)) {
+    constexpr uint32_t mlo = MP == 8 ? 1u : static_cast<uint32_t>(MP / 2 + 1), mhi = static_cast<uint32_t>(MP);
+    if constexpr (MP > tc_max_mp(WT) || (CM && !tc_conv_mma(WT, mlo)) || (!CM && tc_conv_mma(WT, mhi))) {
         return nullptr;
     } else {
-        return reinterpret_cast<const void*>(&dev::rem_tc_kernel<WT, MP>);
+        return reinterpret_cast<const void*>(&dev::rem_tc_kernel<WT, MP, CM>);
     }
 }
 }  // namespace rem
 
-#define REM_TC_INSTANTIATE(WT, NAME)                                    \
-    namespace rem {                                                     \
-    const void* NAME(int mp) {                                          \
-        return mp == 8 ? tc_kernel_ptr<WT, 8>() : mp == 16 ? tc_kernel_ptr<WT, 16>()                 \
-               : mp == 32 ? tc_kernel_ptr<WT, 32>() : nullptr;                                        \
-    }                                                                   \
+#define REM_TC_INSTANTIATE(WT, NAME)                                                              \
+    namespace rem {                                                                               \
+    const void* NAME(int mp, bool cm) {                                                           \
+        if (cm) return mp == 8 ? tc_kernel_ptr<WT, 8, true>() : mp == 16 ? tc_kernel_ptr<WT, 16, true>() \
+                       : mp == 32 ? tc_kernel_ptr<WT, 32, true>() : nullptr;                       \
+        return mp == 8 ? tc_kernel_ptr<WT, 8, false>() : mp == 16 ? tc_kernel_ptr<WT, 16, false>()  \
+               : mp == 32 ? tc_kernel_ptr<WT, 32, false>() : nullptr;                              \
+    }                                                                                             \
     }
