@@ -179,7 +179,7 @@ int device_state(DeviceState** out, int* dev_out) {
                     st.max_threads[wt][m][l] = fa.maxThreadsPerBlock;
                 }
             if (tc_format(wt))
-                for (int mp = 8; mp <= tc_max_mp(wt); mp *= 2)
+                for (int mp = 1; mp <= tc_max_mp(wt); mp *= 2)
                     for (int cm = 0; cm < 2; ++cm) {
                     const void* fn = tc_kernel(wt, mp, cm != 0);
                     if (!fn) continue;  // not every width takes both conversion modes
@@ -556,7 +556,7 @@ int plan_simt(int dev, const DeviceState& ds, int wt, const Shape& s, const Sche
 // is raised until no more CTAs than that fit on one SM.
 int plan_tc(int dev, const DeviceState& ds, int wt, const Shape& s, Plan& p) {
     const uint32_t S = p.S;
-    p.mp = s.m <= 8 ? 8 : s.m <= 16 ? 16 : 32;
+    p.mp = tc_tile_mp(s.m);
     p.cm = tc_conv_mma(wt, s.m);
     p.fn = tc_kernel(wt, p.mp, p.cm);
     if (!p.fn || p.mp > tc_max_mp(wt))

@@ -165,9 +165,11 @@ inline uint32_t mv_smem_bytes(int wt, int nr0, int h, int warps, int stages, int
 
 // ---------------------------------------------------------------- tensor-core engine
 
-// The tensor-core kernel rem_tc_kernel<wt, mp> (rem_tc.cuh) serves the
+// The tensor-core kernel rem_tc_kernel<wt, mp, cm> (rem_tc.cuh) serves the
 // block-scaled formats Q8_0, Q5_0 and Q6_K for up to mp input rows per
-// launch, mp in {8, 16, 32} (Q6_K: {8, 16}).  A CTA owns 128 weight rows.
+// launch, mp in {1, 2, 4, 8, 16, 32} (Q6_K: up to 16): a launch takes the
+// smallest mp >= m, so the scaling of the accumulators handles exactly mp
+// columns with no branch on m.  A CTA owns 128 weight rows.
 // (Q4_K's weights d*sc*q - dmin*mn have no exact bfloat16 code, and the
 // split a*sum(q*x) - b*sum(x) misses the tolerance where the two terms
 // cancel and turns an infinite input into NaN, so Q4_K stays on the
@@ -178,6 +180,13 @@ __host__ __device__ constexpr bool tc_format(int wt) { return wt == kQ8_0 || wt 
 // its widest tile is 16 input rows; the formats with 32-value scale blocks go
 // to 32.
 __host__ __device__ constexpr int tc_max_mp(int wt) { return wt == kQ6_K ? 16 : 32; }
+// MMA N: 2*mp columns (x_hi rows, x_lo rows), at least 16 (the rest of a
+// narrow tile's B rows stay zero).
+__host__ __device__ constexpr int tc_ncol(int mp) { return mp < 8 ? 16 : 2 * mp; }
+// The tile width a launch of m input rows takes.
+__host__ __device__ constexpr int tc_tile_mp(uint32_t m) {
+    return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : m <= 16 ? 16 : 32;
+}
 // K-steps (16 values) per scale block: Q6_K sub-blocks of 16, Q8_0 / Q5_0 blocks of 32.
 __host__ __device__ constexpr int tc_kpb(int wt) { return wt == kQ6_K ? 1 : 2; }
 // K-steps of a 64-value unit each consumer warp decodes: two (8 consumer
@@ -204,8 +213,8 @@ __host__ __device__ constexpr bool tc_conv_mma(int wt, uint32_t m) {
     return m * 4u * static_cast<uint32_t>(tc_units_per_chunk(wt)) <= (wt == kQ6_K ? 80u : 128u);
 }
 // Tensor-memory columns of one A/D slot: 32 columns of A (a unit as bf16
-// pairs) and one 2*mp-column accumulator per region of the unit.
-__host__ __device__ constexpr int tc_slot_cols(int wt, int mp) { return 32 + tc_regions(wt, mp) * 2 * mp; }
+// pairs) and one N-column accumulator per region of the unit.
+__host__ __device__ constexpr int tc_slot_cols(int wt, int mp) { return 32 + tc_regions(wt, mp) * tc_ncol(mp); }
 // A/D slots in tensor memory: the deepest ring (4, 2 or 1 slots) that divides
 // the units of a chunk and fits the SM's 512 columns (a tensor-core CTA runs
 // alone on its SM).
@@ -223,14 +232,14 @@ __host__ __device__ constexpr int tc_tmem_cols(int wt, int mp) {
 }
 // Dynamic shared memory of one tensor-core CTA: stages x [weight box (128 rows
 // x box) | input box (mp x chunk floats, padded to 128 B)], two B tiles of a
-// chunk (bf16, 2*mp rows x chunk values), two buffers of partials (the warp
+// chunk (bf16, N rows x chunk values), two buffers of partials (the warp
 // groups past the first of each lane quarter, x 4 quarters x mp x 32 floats;
 // the cross-range partials reuse them), the mbarriers and the tensor-memory
 // address, plus slack to align the base to 128 bytes.
 inline uint32_t tc_smem_bytes(int wt, int mp, int stages, int split) {
     const uint32_t xpad = ((uint32_t)mp * chunk_values(wt) * 4u + 127u) & ~127u;
     const uint32_t stage = (uint32_t)kTcRows * chunk_box(wt) + xpad;
-    const uint32_t btiles = 2u * (uint32_t)(chunk_values(wt) / 16) * 64u * (uint32_t)mp;
+    const uint32_t btiles = 2u * (uint32_t)(chunk_values(wt) / 16) * 32u * (uint32_t)tc_ncol(mp);
     const uint32_t groups = (uint32_t)tc_consumer_warps(mp) / 4u;
     const uint32_t pbuf = 2u * (groups - 1u) * 4u * (uint32_t)mp * 32u * 4u;
     (void)split;

@@ -376,7 +376,7 @@ struct TcGeom {
     using F = TcFmt<WT>;
     static constexpr int CV = Stage<WT>::kValues;           // values per chunk
     static constexpr int BOX = Stage<WT>::kBox;             // staged bytes per row
-    static constexpr int NCOL = 2 * MP;                     // MMA N: x_hi rows, then x_lo rows
+    static constexpr int NCOL = tc_ncol(MP);                // MMA N: x_hi rows, then x_lo rows (>= 16)
     static constexpr int KSTEPS = CV / 16;                  // K-steps per chunk
     static constexpr int BKSTEP = 32 * NCOL;                // B bytes per K-step (NCOL rows x 32 bytes)
     static constexpr int BCHUNK = KSTEPS * BKSTEP;          // B bytes per chunk
@@ -441,9 +441,11 @@ __device__ __forceinline__ void tc_convert_x(const float* xs, uint8_t* bt, uint3
             const float r1 = (b1 & 0x7F800000u) == 0x7F800000u ? 0.0f : __fsub_rn(e[2 * p + 1], __uint_as_float(b1 & 0xFFFF0000u));
             lo[p] = bf16x2_rn(r0, r1);
         }
-        uint8_t* dst = bt + s * G::BKSTEP + (j >> 3) * 256 + kh * 128 + (j & 7) * 16;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(dst + (MP / 8) * 256) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        // tile rows: x_hi at j, x_lo at MP + j
+        uint8_t* bs = bt + s * G::BKSTEP + kh * 128;
+        const int rl = MP + j;
+        *reinterpret_cast<uint4*>(bs + (j >> 3) * 256 + (j & 7) * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(bs + (rl >> 3) * 256 + (rl & 7) * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
 }
 
@@ -484,9 +486,11 @@ __device__ __forceinline__ void tc_convert_x_part(const float* xs, uint8_t* bt, 
             const float r1 = (b1 & 0x7F800000u) == 0x7F800000u ? 0.0f : __fsub_rn(x[2 * p + 1], __uint_as_float(b1 & 0xFFFF0000u));
             lo[p] = bf16x2_rn(r0, r1);
         }
-        uint8_t* dst = bt + s * G::BKSTEP + (j >> 3) * 256 + kh * 128 + (j & 7) * 16;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(dst + (MP / 8) * 256) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        // tile rows: x_hi at j, x_lo at MP + j
+        uint8_t* bs = bt + s * G::BKSTEP + kh * 128;
+        const int rl = MP + j;
+        *reinterpret_cast<uint4*>(bs + (j >> 3) * 256 + (j & 7) * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(bs + (rl >> 3) * 256 + (rl & 7) * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
 }
 
@@ -508,41 +512,33 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
 }
 
 // The RPW accumulator regions of a warp, their D columns loaded into d
-// (region b at columns b*2*MP on): c = D_hi + D_lo for input rows 0..NJ-1
-// (NJ >= m; the rest of acc stays zero and is never stored) and acc =
-// fma(scale_b, c, acc), region by region.  Columns go in pairs through the
-// f32x2 add and fma, which round each lane as the binary32 ops do; each
-// column is computed on its own, so skipping the columns past m changes no
-// bit of the others.
-template <int MP, int RPW, int NJ>
-__device__ __forceinline__ void tc_scale_cols(const uint32_t (&d)[RPW * 2 * MP], const float (&sc)[RPW],
-                                              float (&acc)[MP]) {
+// (region b at columns b*N on: x_hi of input rows 0..MP-1, then x_lo): c =
+// D_hi + D_lo for each of the tile's MP input rows (rows past m hold zeros
+// and are never stored) and acc = fma(scale_b, c, acc), region by region.
+// Columns go in pairs through the f32x2 add and fma, which round each lane
+// as the binary32 ops do; each column is computed on its own, so the tile
+// width changes no bit of an output.
+template <int MP, int RPW>
+__device__ __forceinline__ void tc_scale(const uint32_t (&d)[RPW * tc_ncol(MP)], const float (&sc)[RPW],
+                                         float (&acc)[MP]) {
+    constexpr int NC = tc_ncol(MP);
 #pragma unroll
     for (int b = 0; b < RPW; ++b) {
         const float2 s2 = make_float2(sc[b], sc[b]);
 #pragma unroll
-        for (int j = 0; j + 1 < NJ; j += 2) {
-            const float2 c = add2(make_float2(__uint_as_float(d[b * 2 * MP + j]), __uint_as_float(d[b * 2 * MP + j + 1])),
-                                  make_float2(__uint_as_float(d[b * 2 * MP + MP + j]),
-                                              __uint_as_float(d[b * 2 * MP + MP + j + 1])));
+        for (int j = 0; j + 1 < MP; j += 2) {
+            const float2 c = add2(make_float2(__uint_as_float(d[b * NC + j]), __uint_as_float(d[b * NC + j + 1])),
+                                  make_float2(__uint_as_float(d[b * NC + MP + j]),
+                                              __uint_as_float(d[b * NC + MP + j + 1])));
             const float2 r = fma2(s2, c, make_float2(acc[j], acc[j + 1]));
             acc[j] = r.x;
             acc[j + 1] = r.y;
         }
-        if constexpr (NJ & 1)
-            acc[NJ - 1] = __fmaf_rn(sc[b], __fadd_rn(__uint_as_float(d[b * 2 * MP + NJ - 1]),
-                                                     __uint_as_float(d[b * 2 * MP + MP + NJ - 1])),
-                                    acc[NJ - 1]);
+        if constexpr (MP & 1)
+            acc[MP - 1] = __fmaf_rn(sc[b], __fadd_rn(__uint_as_float(d[b * NC + MP - 1]),
+                                                     __uint_as_float(d[b * NC + 2 * MP - 1])),
+                                    acc[MP - 1]);
     }
-}
-template <int MP, int RPW>
-__device__ __forceinline__ void tc_scale(const uint32_t (&d)[RPW * 2 * MP], const float (&sc)[RPW], uint32_t m,
-                                         float (&acc)[MP]) {
-    if (m <= 1) tc_scale_cols<MP, RPW, 1>(d, sc, acc);
-    else if (m <= 2) tc_scale_cols<MP, RPW, 2>(d, sc, acc);
-    else if (m <= 4) tc_scale_cols<MP, RPW, 4>(d, sc, acc);
-    else if (MP == 8 || m <= 8) tc_scale_cols<MP, RPW, (MP < 8 ? MP : 8)>(d, sc, acc);
-    else tc_scale_cols<MP, RPW, MP>(d, sc, acc);
 }
 
 // Persistent kernel: clusters of `split` CTAs walk the 128-row tiles; CTA
@@ -937,7 +933,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 if (pending) {
                     tmem_ld_wait();
 #pragma unroll
-                    for (int bb = 0; bb < BATCH; ++bb) tc_scale<MP, RPW>(d[bb], psc[(U0 + bb) % NS], m, acc);
+                    for (int bb = 0; bb < BATCH; ++bb) tc_scale<MP, RPW>(d[bb], psc[(U0 + bb) % NS], acc);
                 }
 #pragma unroll
                 for (int bb = 0; bb < BATCH; ++bb)
@@ -965,7 +961,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     uint32_t d[RPW * G::NCOL];
                     load_d(SL, d);
                     tmem_ld_wait();
-                    tc_scale<MP, RPW>(d, psc[SL], m, acc);
+                    tc_scale<MP, RPW>(d, psc[SL], acc);
                 });
             });
         }
@@ -1004,7 +1000,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
 namespace rem {
 template <int WT, int MP, bool CM>
 inline const void* tc_kernel_ptr() {
-    constexpr uint32_t mlo = MP == 8 ? 1u : static_cast<uint32_t>(MP / 2 + 1), mhi = static_cast<uint32_t>(MP);
+    constexpr uint32_t mlo = static_cast<uint32_t>(MP / 2 + 1), mhi = static_cast<uint32_t>(MP);
     if constexpr (MP > tc_max_mp(WT) || (CM && !tc_conv_mma(WT, mlo)) || (!CM && tc_conv_mma(WT, mhi))) {
         return nullptr;
     } else {
@@ -1015,10 +1011,17 @@ inline const void* tc_kernel_ptr() {
 
 #define REM_TC_INSTANTIATE(WT, NAME)                                                              \
     namespace rem {                                                                               \
-    const void* NAME(int mp, bool cm) {                                                           \
-        if (cm) return mp == 8 ? tc_kernel_ptr<WT, 8, true>() : mp == 16 ? tc_kernel_ptr<WT, 16, true>() \
-                       : mp == 32 ? tc_kernel_ptr<WT, 32, true>() : nullptr;                       \
-        return mp == 8 ? tc_kernel_ptr<WT, 8, false>() : mp == 16 ? tc_kernel_ptr<WT, 16, false>()  \
-               : mp == 32 ? tc_kernel_ptr<WT, 32, false>() : nullptr;                              \
+    template <bool CM>                                                                            \
+    static const void* NAME##_cm(int mp) {                                                        \
+        switch (mp) {                                                                             \
+        case 1: return tc_kernel_ptr<WT, 1, CM>();                                                \
+        case 2: return tc_kernel_ptr<WT, 2, CM>();                                                \
+        case 4: return tc_kernel_ptr<WT, 4, CM>();                                                \
+        case 8: return tc_kernel_ptr<WT, 8, CM>();                                                \
+        case 16: return tc_kernel_ptr<WT, 16, CM>();                                              \
+        case 32: return tc_kernel_ptr<WT, 32, CM>();                                              \
+        default: return nullptr;                                                                  \
+        }                                                                                         \
     }                                                                                             \
+    const void* NAME(int mp, bool cm) { return cm ? NAME##_cm<true>(mp) : NAME##_cm<false>(mp); } \
     }

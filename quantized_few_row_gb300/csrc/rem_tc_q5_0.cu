@@ -1,4 +1,4 @@
-// Instantiates rem_tc_kernel<kQ5_0, MP> for MP = 8, 16, 32.
+// Instantiates rem_tc_kernel<kQ5_0, MP, CM> for the tile widths MP = 1, 2, 4, 8, 16, 32.
 #include "rem_tc.cuh"
 
 REM_TC_INSTANTIATE(rem::kQ5_0, tc_kernel_q5_0)
