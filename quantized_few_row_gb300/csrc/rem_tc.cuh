@@ -894,11 +894,6 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     constexpr int U = U0 + decltype(b_)::value;
                     if constexpr (U > 0 && F::kLoad(U)) F::template load<U>(row, o, grp, R[kPerUnit ? U - U0 : 0]);
                 });
-                if constexpr (U0 <= F::kLastLoad && F::kLastLoad < U0 + BATCH) {
-                    // the staged weights and inputs of this chunk are all read
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(eb + 8 * st);
-                }
                 const uint32_t use = gc * (SPC / NSS) + static_cast<uint32_t>(P / NSS);
                 const bool pending = q > 0 || P >= NSS;  // the step's slots hold earlier units of this tile
                 // The units' codes are decoded into registers while the
@@ -914,6 +909,13 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     constexpr int BI = decltype(b_)::value;
                     F::template decode<U0 + BI>(R[kPerUnit ? BI : 0], av[BI], nsc[BI]);
                 });
+                if constexpr (U0 <= F::kLastLoad && F::kLastLoad < U0 + BATCH) {
+                    // the staged weights and inputs of this chunk are all
+                    // read, and the words decoded (the release has no load
+                    // left to wait for)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(eb + 8 * st);
+                }
                 if (pending) {
                     wait_d(SS, use - 1u);
                     if (failed) return;
