@@ -58,6 +58,10 @@ WORKLOADS = {
     "q8_0_n4096_k4096_m1-8_bias": ("q8_0", 4096, 4096, 1, list(range(1, 9)), False, 10),
     # profiling size of the Q6_K path: 215 MB of weights (above the L2), for ncu captures
     "q6_K_n65536_k4096_m1,8": ("q6_K", 65536, 4096, 1, [1, 8], False, 16),
+    # the tensor-core engine on request (rem_matvec_sched) where the default is the lanes-over-rows one
+    "q5_0_grouped_b16_n1024_k4096_m1-8_tc": ("q5_0", 1024, 4096, 16, list(range(1, 9)), True, 4, "tc"),
+    "q5_0_n28672_k4096_m1-8_tc": ("q5_0", 28672, 4096, 1, list(range(1, 9)), False, 17, "tc"),
+    "q8_0_n28672_k4096_m1-8_tc": ("q8_0", 28672, 4096, 1, list(range(1, 9)), False, 18, "tc"),
 }
 # workloads that run the epilogue alpha * W.x + beta * c with c a bias vector
 EPILOGUE = {"q8_0_n4096_k4096_m1-8_bias": (1.0, 1.0)}
@@ -67,7 +71,8 @@ DEFAULT = "q6_K_n128256_k4096_m1,4,8"
 EXTRA = ["f16_n256_k512_m1", "q8_0_n4096_k4096_m1-8", "q4_K_n14336_k4096_m1-8", "q5_0_grouped_b16_n1024_k4096_m8",
          "f16_n8192_k4096_m1-8", "q8_0_n16384_k4096_m1-8", "q4_K_n28672_k4096_m1-8", "q5_0_grouped_b32_n1024_k4096_m8",
          "q4_K_n14336_k4096_m16,32", "q8_0_n16384_k4096_m16,32", "q6_K_n128256_k4096_m16",
-         "bf16_n8192_k4096_m1-8", "f32_n4096_k4096_m1-8", "a4_g64_n14336_k4096_m1-8", "q8_0_n4096_k4096_m1-8_bias"]
+         "bf16_n8192_k4096_m1-8", "f32_n4096_k4096_m1-8", "a4_g64_n14336_k4096_m1-8", "q8_0_n4096_k4096_m1-8_bias",
+         "q5_0_grouped_b16_n1024_k4096_m1-8_tc", "q5_0_n28672_k4096_m1-8_tc", "q8_0_n28672_k4096_m1-8_tc"]
 METRIC = "achieved HBM GB/s (% of GB300 peak) and us/call, m=1..8 quantized mat-vec"
 
 
@@ -204,7 +209,10 @@ class Workload:
 
     def __init__(self, name, dev, rem, inputs, l2):
         import torch
-        fmt, n, k, batch, ms, grouped, ci = WORKLOADS[name]
+        fmt, n, k, batch, ms, grouped, ci = WORKLOADS[name][:7]
+        # an engine requested explicitly (the tensor cores for Q8_0 / Q5_0), else the library's choice
+        forced = WORKLOADS[name][7] if len(WORKLOADS[name]) > 7 else None
+        self.sched = rem.Schedule(engine=1 if forced == "tc" else 0) if forced else None
         self.name, self.fmt, self.n, self.k, self.batch, self.ms, self.grouped = name, fmt, n, k, batch, ms, grouped
         self.rem = rem
         self.rb = rem.rem_row_bytes(fmt, k)
@@ -243,7 +251,7 @@ class Workload:
             self.xbs, self.ybs = mmax * k, mmax * n
         self.epi = EPILOGUE.get(name)
         self.bias = inputs.torch_normal((batch, n), 3000 + ci, inputs.X_STD, dev) if self.epi else None
-        self.engine = rem.rem_engine_of(fmt, batch * n, k)
+        self.engine = self.sched.engine if self.sched is not None else rem.rem_engine_of(fmt, batch * n, k)
         torch.cuda.synchronize()
 
     def call(self, slot, m, stream=None, xv=None, yv=None):
@@ -263,6 +271,9 @@ class Workload:
         if self.epi:
             return rem.rem_matvec_axpby(w, fmt, n, k, batch, xs, m, k, xb, ys, n, yb, self.epi[0], self.epi[1],
                                         self.bias, 0, n, stream)
+        if self.sched is not None:
+            xrs, yrs = (batch * k, batch * n) if self.grouped else (k, n)
+            return rem.rem_matvec_sched(w, fmt, n, k, batch, xs, m, xrs, xb, ys, yrs, yb, self.sched, stream)
         if m > 8:
             xrs, yrs = (batch * k, batch * n) if self.grouped else (k, n)
             return rem.rem_matvec_many(w, fmt, n, k, batch, xs, m, xrs, xb, ys, yrs, yb, 0, stream)
@@ -583,7 +594,7 @@ def oracle_sample(fmt, n, k, batch, ms, grouped, ci, seconds: float):
 def oracle_sample_one_core(workload: str, seconds: float):
     """oracle_sample on one host thread (a child process with OMP_NUM_THREADS=1)."""
     env = dict(os.environ, OMP_NUM_THREADS="1")
-    code = ("import json, bench; fmt, n, k, batch, ms, g, ci = bench.WORKLOADS[%r]; "
+    code = ("import json, bench; fmt, n, k, batch, ms, g, ci = bench.WORKLOADS[%r][:7]; "
             "print(json.dumps(bench.oracle_sample(fmt, n, k, batch, ms, g, ci, %r)))" % (workload, seconds))
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=int(20 * seconds) + 300)
@@ -594,7 +605,7 @@ def oracle_sample_one_core(workload: str, seconds: float):
 
 
 def run_reference(args):
-    fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload]
+    fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload][:7]
     per_step = max(0.2, 60.0 / max(1, args.steps + args.warmup))
     vals = []
     for s in range(args.warmup + args.steps):
@@ -646,7 +657,7 @@ def main():
         if args.no_cpu_baseline:
             res["cpu_baseline"] = None
         else:
-            fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload]
+            fmt, n, k, batch, ms, grouped, ci = WORKLOADS[args.workload][:7]
             v, cores, desc = oracle_sample(fmt, n, k, batch, ms, grouped, ci, args.cpu_seconds)
             res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                    "sample": desc}
