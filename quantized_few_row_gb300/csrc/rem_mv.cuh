@@ -146,6 +146,20 @@ __device__ __forceinline__ uint64_t global_ns() {
 // has not completed `limit_ns` nanoseconds (of the global timer) after the
 // first unsuccessful try.  The poll count is capped as well, so the wait
 // ends even if the timer were not to advance.
+// One non-blocking test of the phase of `parity` (mbarrier.test_wait, acquire
+// when it reports the phase complete).  Issued ahead of the point where the
+// answer is needed, its latency overlaps other work.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = global_ns();

@@ -822,16 +822,16 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     // the words of unit b of a step come from Regs R[b] where every unit loads
     // its own, else all from R[0] (loaded once per chunk)
     constexpr bool kPerUnit = F::kLoad(1);
-    constexpr int kOpenAt = 1;
     bool failed = false;
     int st = 0;       // stage of the current chunk
     uint32_t ph = 0;  // its full-barrier parity
     uint32_t gc = 0;  // chunks over all tiles
-    // wait for stage `sq`, convert its inputs into B tile buffer `bsel` where
-    // the consumers do that, and load unit 0's words of chunk q of the K
-    // range into r
-    auto open_chunk = [&](int sq, uint32_t phase, int q, uint32_t bsel, typename F::Regs& r) {
-        if (!failed && !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * sq, phase, a.wait_ns))) {
+    // wait for stage `sq` (unless an earlier poll, `seen`, found it full),
+    // convert its inputs into B tile buffer `bsel` where the consumers do
+    // that, and load unit 0's words of chunk q of the K range into r
+    auto open_chunk = [&](int sq, uint32_t phase, int q, uint32_t bsel, typename F::Regs& r, bool seen = false) {
+        if (!failed && !__all_sync(0xFFFFFFFFu, seen) &&
+            !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * sq, phase, a.wait_ns))) {
             failed = true;
             if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
         }
@@ -875,9 +875,12 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                                    d);
         };
         typename F::Regs R[kPerUnit ? BATCH : 1];
-        // the first chunk of the tile; each later one is opened during the
-        // last step of the one before, while that step's tensor-memory loads
-        // are in flight
+        // polls issued a step ahead: the next step's slot barrier (dseen) and,
+        // from the chunk's first step, the next chunk's stage (fseen); the
+        // blocking wait runs only where a poll found the phase incomplete
+        bool dseen = false, fseen = false;
+        // the first chunk of the tile; each later one is opened at the end of
+        // the last step of the one before
         if (nck > 0) open_chunk(st, ph, 0, gc & 1u, R[0]);
         for (int q = 0; q < nck; ++q, ++gc) {
             if (failed) break;
@@ -917,9 +920,11 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                     if (lane == 0) mbar_arrive(eb + 8 * st);
                 }
                 if (pending) {
-                    wait_d(SS, use - 1u);
+                    if (__all_sync(0xFFFFFFFFu, dseen)) tc_fence_after();
+                    else wait_d(SS, use - 1u);
                     if (failed) return;
                 }
+                if constexpr (P == 0) fseen = more && mbar_test(fb + 8 * st1, ph1);
 #pragma unroll
                 for (int bb = 0; bb < BATCH; ++bb)
                     tmem_st_cols<KPW>(tmem + lane_base + static_cast<uint32_t>(((U0 + bb) % NS) * G::ACOLS + 8 * KPW * grp),
@@ -928,9 +933,6 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 if (pending) {
 #pragma unroll
                     for (int bb = 0; bb < BATCH; ++bb) load_d((U0 + bb) % NS, d[bb]);
-                }
-                if constexpr (kLast && kOpenAt == 0) {
-                    if (more) open_chunk(st1, ph1, q + 1, (gc + 1u) & 1u, R[0]);
                 }
                 if (pending) {
                     tmem_ld_wait();
@@ -945,8 +947,19 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ab + 8 * SS);
-                if constexpr (kLast && kOpenAt == 1) {
-                    if (more) open_chunk(st1, ph1, q + 1, (gc + 1u) & 1u, R[0]);
+                // poll the next step's slot barrier now (its previous use was
+                // handed over a step ago); the wait there uses the answer
+                if constexpr (!kLast) {
+                    constexpr int P1 = P + 1;
+                    const uint32_t use1 = gc * (SPC / NSS) + static_cast<uint32_t>(P1 / NSS);
+                    const bool pend1 = q > 0 || P1 >= NSS;
+                    dseen = pend1 && mbar_test(db + 8 * (P1 % NSS), (use1 - 1u) & 1u);
+                } else {
+                    const uint32_t use1 = (gc + 1u) * (SPC / NSS);
+                    dseen = more && mbar_test(db + 8 * 0, (use1 - 1u) & 1u);
+                }
+                if constexpr (kLast) {
+                    if (more) open_chunk(st1, ph1, q + 1, (gc + 1u) & 1u, R[0], fseen);
                 }
             });
             st = st1;
