@@ -89,6 +89,29 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// C consecutive 32-bit columns of the warp's 32 lanes into r[0..C-1] (C = 2,
+// 4 or 8; the rest of r is left as it is).
+template <int C, int N>
+__device__ __forceinline__ void tmem_ld_narrow(uint32_t taddr, uint32_t* r) {
+    static_assert(C <= N, "columns");
+    if constexpr (C == 2) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr)
+                     : "memory");
+    } else if constexpr (C == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr)
+                     : "memory");
+    } else {
+        static_assert(C == 8, "2, 4 or 8 columns");
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7])
+                     : "r"(taddr)
+                     : "memory");
+    }
+}
+
 // N consecutive 32-bit columns of the warp's 32 lanes (N = 16, 32, 64).
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
@@ -869,10 +892,19 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
             tc_fence_after();
         };
         // the warp's RPW regions of slot sl: regions KPW*grp/RK on, contiguous
+        // (the 1- and 2-row tiles read only their 2*MP used columns of each
+        // region -- tc_scale reads no other; from 4 rows one wide load per
+        // unit measured faster)
         auto load_d = [&](int sl, uint32_t (&d)[RPW * G::NCOL]) {
-            tmem_ld<RPW * G::NCOL>(tmem + lane_base + static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS +
-                                                                           (KPW * grp / RK) * G::NCOL),
-                                   d);
+            const uint32_t ta = tmem + lane_base + static_cast<uint32_t>(NS * G::ACOLS + sl * G::DCOLS +
+                                                                         (KPW * grp / RK) * G::NCOL);
+            if constexpr (MP <= 2) {
+#pragma unroll
+                for (int r = 0; r < RPW; ++r)
+                    tmem_ld_narrow<2 * MP, G::NCOL>(ta + static_cast<uint32_t>(r * G::NCOL), d + r * G::NCOL);
+            } else {
+                tmem_ld<RPW * G::NCOL>(ta, d);
+            }
         };
         typename F::Regs R[kPerUnit ? BATCH : 1];
         // polls issued a step ahead: the next step's slot barrier (dseen) and,
