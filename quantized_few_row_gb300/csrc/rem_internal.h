@@ -210,7 +210,7 @@ __host__ __device__ constexpr int tc_units_per_chunk(int wt) { return wt == kQ8_
 // stay few enough for them, measured per format.  The conversion is the same
 // arithmetic either way.
 __host__ __device__ constexpr bool tc_conv_mma(int wt, uint32_t m) {
-    return m * 4u * static_cast<uint32_t>(tc_units_per_chunk(wt)) <= (wt == kQ6_K ? 80u : 128u);
+    return m * 4u * static_cast<uint32_t>(tc_units_per_chunk(wt)) <= (wt == kQ6_K ? 64u : 128u);
 }
 // Tensor-memory columns of one A/D slot: 32 columns of A (a unit as bf16
 // pairs) and one N-column accumulator per region of the unit.
