@@ -911,6 +911,15 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         // from the chunk's first step, the next chunk's stage (fseen); the
         // blocking wait runs only where a poll found the phase incomplete
         bool dseen = false, fseen = false;
+        // 1- and 2-row tiles of the formats that load a chunk's words once
+        // (Q6_K): when the poll found the next step's slots complete, their
+        // accumulators are read right away into dn (a few registers there),
+        // so the read-back latency passes during the next step's decode;
+        // dn_ok says it was done.  (Q8_0 and Q5_0, which load per unit,
+        // measured slower with it.)
+        constexpr bool kEarlyD = MP <= 2 && !kPerUnit;
+        uint32_t dn[kEarlyD ? BATCH : 1][RPW * G::NCOL];
+        bool dn_ok = false;
         // the first chunk of the tile; each later one is opened at the end of
         // the last step of the one before
         if (nck > 0) open_chunk(st, ph, 0, gc & 1u, R[0]);
@@ -961,15 +970,26 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 for (int bb = 0; bb < BATCH; ++bb)
                     tmem_st_cols<KPW>(tmem + lane_base + static_cast<uint32_t>(((U0 + bb) % NS) * G::ACOLS + 8 * KPW * grp),
                                       av[bb]);
-                uint32_t d[BATCH][RPW * G::NCOL];
-                if (pending) {
+                if constexpr (kEarlyD) {
+                    if (pending) {
+                        if (!dn_ok) {
 #pragma unroll
-                    for (int bb = 0; bb < BATCH; ++bb) load_d((U0 + bb) % NS, d[bb]);
-                }
-                if (pending) {
-                    tmem_ld_wait();
+                            for (int bb = 0; bb < BATCH; ++bb) load_d((U0 + bb) % NS, dn[kEarlyD ? bb : 0]);
+                        }
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int bb = 0; bb < BATCH; ++bb) tc_scale<MP, RPW>(d[bb], psc[(U0 + bb) % NS], acc);
+                        for (int bb = 0; bb < BATCH; ++bb)
+                            tc_scale<MP, RPW>(dn[kEarlyD ? bb : 0], psc[(U0 + bb) % NS], acc);
+                    }
+                } else {
+                    uint32_t d[BATCH][RPW * G::NCOL];
+                    if (pending) {
+#pragma unroll
+                        for (int bb = 0; bb < BATCH; ++bb) load_d((U0 + bb) % NS, d[bb]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int bb = 0; bb < BATCH; ++bb) tc_scale<MP, RPW>(d[bb], psc[(U0 + bb) % NS], acc);
+                    }
                 }
 #pragma unroll
                 for (int bb = 0; bb < BATCH; ++bb)
@@ -989,6 +1009,16 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                 } else {
                     const uint32_t use1 = (gc + 1u) * (SPC / NSS);
                     dseen = more && mbar_test(db + 8 * 0, (use1 - 1u) & 1u);
+                }
+                if constexpr (kEarlyD) {
+                    // the next step's slots: (BATCH * P1 + bb) % NS, or the next chunk's first step's
+                    constexpr int N0 = kLast ? 0 : BATCH * (P + 1);
+                    dn_ok = __all_sync(0xFFFFFFFFu, dseen);
+                    if (dn_ok) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int bb = 0; bb < BATCH; ++bb) load_d((N0 + bb) % NS, dn[kEarlyD ? bb : 0]);
+                    }
                 }
                 if constexpr (kLast) {
                     if (more) open_chunk(st1, ph1, q + 1, (gc + 1u) & 1u, R[0], fseen);
@@ -1034,6 +1064,7 @@ rem_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
                                     pair_floats, [&](int j) { return static_cast<uint32_t>(j) < m; }, grp == 0);
     }
     if (S > 1) cluster_sync();
+    tmem_ld_wait();  // no read of tensor memory outlives the warp (an early read after a failed wait)
     tc_fence_before();
     asm volatile("bar.sync 1, %0;" ::"n"((CW + 2) * 32) : "memory");
 }
