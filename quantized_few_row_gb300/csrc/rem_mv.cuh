@@ -1258,7 +1258,9 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
     }
 
     bool failed = false;
-    uint32_t i = 0;
+    int st = 0;          // stage of the current chunk
+    uint32_t ph = 0;     // its full-barrier parity
+    bool seen = false;   // a poll during the previous chunk found this stage full
     for (uint32_t rb = cid, t = 0; rb < nblocks; rb += ncl, ++t) {
         uint32_t b, row0;
         block_origin(rb, b, row0);
@@ -1269,19 +1271,29 @@ rem_mv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ 
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int j = 0; j < MH; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
-        for (int q = 0; q < nck; ++q, ++i) {
-            const int st = static_cast<int>(i % D);
-            if (!failed &&
-                !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, static_cast<uint32_t>((i / D) & 1), a.wait_ns))) {
+        for (int q = 0; q < nck; ++q) {
+            const int st1 = st + 1 == D ? 0 : st + 1;
+            const uint32_t ph1 = st + 1 == D ? ph ^ 1u : ph;
+            if (!failed && !__all_sync(0xFFFFFFFFu, seen) &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait(fb + 8 * st, ph, a.wait_ns))) {
                 failed = true;
                 if (lane == 0) report_timeout(a.status, kStatusWaitTimeout);
             }
-            if (failed) continue;  // keep walking so every barrier below is still reached
+            // poll the next stage now; the answer is used a chunk later (the
+            // blocking wait runs only where it found the stage not yet full)
+            seen = !failed && mbar_test(fb + 8 * st1, ph1);
+            if (failed) {  // keep walking so every barrier below is still reached
+                st = st1;
+                ph = ph1;
+                continue;
+            }
             if (wactive)
                 mv_chunk<WT, M, NR0, H>(smem + st * stage_bytes, wstage, warp, lane, c0 + static_cast<uint32_t>(q),
                                         acc, a, b, wrow0);
             __syncwarp();
             if (lane == 0) mbar_arrive(eb + 8 * st);
+            st = st1;
+            ph = ph1;
         }
         mv_finish<M, NR0, H>(acc, failed, a, b, wrow0, wactive, lane, warp, s, S, t, parts, part_floats);
     }
