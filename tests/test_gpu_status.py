@@ -31,15 +31,20 @@ def _lib():
     torch.cuda.init()
 
 
-CASES = [("q8_0", rem.ENGINE_SIMT), ("q8_0", rem.ENGINE_TC), ("q6_K", rem.ENGINE_TC), ("f16", rem.ENGINE_SIMT),
-         ("q4_K", rem.ENGINE_SIMT)]
+# (format, engine, m): on the tensor cores m picks the tile width and who
+# converts the inputs -- 1 (MP 1, the MMA warps, the early accumulator read),
+# 3 (MP 4, the MMA warps), 8 (MP 8, the consumer warps), 16 (MP 16, the
+# consumer warps)
+CASES = [("q8_0", rem.ENGINE_SIMT, 3), ("q8_0", rem.ENGINE_TC, 3), ("q6_K", rem.ENGINE_TC, 3), ("f16", rem.ENGINE_SIMT, 3),
+         ("q4_K", rem.ENGINE_SIMT, 3), ("q6_K", rem.ENGINE_TC, 1), ("q6_K", rem.ENGINE_TC, 8),
+         ("q5_0", rem.ENGINE_TC, 16)]
 
 
-@pytest.mark.parametrize("fmt,engine", CASES, ids=[f"{f}-{'tc' if e else 'simt'}" for f, e in CASES])
-def test_wait_that_runs_out_is_reported(fmt, engine):
+@pytest.mark.parametrize("fmt,engine,m", CASES, ids=[f"{f}-{'tc' if e else 'simt'}-m{m}" for f, e, m in CASES])
+def test_wait_that_runs_out_is_reported(fmt, engine, m):
     assert rem.rem_device_status(True) in (rem.REM_OK, rem.REM_ECUDA)   # start clean
     assert rem.rem_device_status(False) == rem.REM_OK
-    n, k, m = 300, 2048, 3
+    n, k = 300, 2048
     w, x = H.contiguous(fmt, n, k, m, 770, 771)
     hook = rem.Schedule(engine=engine, wait_ns=2_000_000, test_flags=rem.TEST_SKIP_FIRST_STAGE)
     y = H.run_sched(w, fmt, n, k, 1, x, m, k, 0, n, 0, m * n, hook)
