@@ -10,31 +10,37 @@
 // The integer codes q - offset are exact in bfloat16, and each input value is
 // split into bfloat16 parts x = x_hi + x_lo + r with x_hi the upper half of
 // its binary32 bits and x_lo = bf16_rn(x - x_hi), so |r| <= 2^-16 |x|.  One
-// tcgen05.mma (M = 128 weight rows, K = 16 values, N = 2*MP columns: the MP
-// x_hi rows of the inputs, then the MP x_lo rows) gives, per block, the exact
-// products (q - offset)*x_hi and (q - offset)*x_lo summed in binary32 in
-// tensor memory; the consumer warps then form c = D_hi + D_lo and
-// acc = fma(a_u, c, acc) per output, in block order.  The error against the
-// exact sum is below 2^-15 * sum |w*x| plus the binary32 rounding of the
-// sums, well inside the required 1e-4 * sum |w*x|.
+// tcgen05.mma (M = 128 weight rows, K = 16 values, N = max(16, 2*MP)
+// columns: the MP x_hi rows of the inputs, then the MP x_lo rows, then zero
+// rows) gives, per block, the exact products (q - offset)*x_hi and
+// (q - offset)*x_lo summed in binary32 in tensor memory; the consumer warps
+// then form c = D_hi + D_lo and acc = fma(a_u, c, acc) per output, in block
+// order.  The error against the exact sum is below 2^-15 * sum |w*x| plus the
+// binary32 rounding of the sums, well inside the required 1e-4 * sum |w*x|.
 //
 // Row exactness.  Output (i, j) depends only on weight row i (lane i of the
-// tile), the bits of input row j (column j and MP + j of every B tile), and
+// tile), the bits of input row j (columns j and MP + j of every B tile), and
 // the fixed order of blocks and K ranges; the tensor core computes each
-// output column on its own, so neither m (the launch pads its inputs to MP
-// rows with zeros) nor anything else of the launch changes it.
+// output column on its own, so neither m nor the tile width MP a launch
+// takes (1, 2, 4, 8, 16 or 32 rows, the inputs padded with zeros) nor
+// anything else of the launch changes it.
 //
-// Work mapping.  A CTA owns a tile of 128 consecutive weight rows (lane l of
-// consumer warp w holds row 32w + l = TMEM lane 32w + l) and one K range
-// (`split` CTAs of a cluster share a tile, as in the lanes-over-rows kernel).
-// Warps: 4 consumers, 1 TMA producer, 1 MMA issuer (which also owns the
-// tensor memory).  Per staged chunk of K the consumers convert the chunk's
-// inputs to the B tiles (shared memory, canonical K-major layout without
-// swizzle), then per unit of 64 values they decode their rows' codes into 32
-// columns of bf16 pairs and store them to the unit's A slot in tensor memory;
-// the MMA warp issues the unit's 4 MMAs into the slot's D columns and commits
-// to the slot's mbarrier; the consumers read D back and scale it.  NS slots
-// of A and D rotate, so decoding the next units overlaps the MMAs.
+// Work mapping.  A CTA owns a tile of 128 consecutive weight rows (TMEM lane
+// 32*(w%4) + l holds row 32*(w%4) + l for lane l of consumer warp w) and one
+// K range (`split` CTAs of a cluster share a tile, as in the lanes-over-rows
+// kernel).  Warps: 8 consumers (two per lane quarter, each decoding two of a
+// unit's four K-steps), one TMA producer, two MMA warps (the first owns the
+// tensor memory).  A staged chunk's inputs become its B tile (shared memory,
+// canonical K-major layout without swizzle), converted by the MMA warps for
+// a few input rows and by the consumers for more.  Per unit of 64 values the
+// consumers decode their rows' codes into bf16 pairs and store them to the
+// unit's A slot in tensor memory; units are handed to the MMA warps in steps
+// of one or two, each step slot with one A-ready and one D-ready mbarrier;
+// an MMA warp issues the step's MMAs into the slots' D columns and commits;
+// the consumers read D back and scale it when they take the slot again.
+// Waits whose phase has long completed are polled a step ahead, so they cost
+// nothing on the consumers' path.  The slots rotate, so decoding the next
+// units overlaps the MMAs.
 #pragma once
 #include "rem_mv.cuh"
 
