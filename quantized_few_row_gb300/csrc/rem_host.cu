@@ -332,10 +332,12 @@ uint32_t auto_split(int wt, uint64_t rows, uint32_t k) {
 // The engine (and with it the arithmetic) of a weight shape: the tensor-core
 // kernel for Q6_K, the lanes-over-rows kernel otherwise.  Q6_K's sub-block
 // decode is what limits the lanes-over-rows kernel from m = 2 up (at 128256 x
-// 4096 it takes 107, 271 and 512 us at m = 1, 4 and 8 against 192, 202 and
-// 214 us on the tensor cores); for Q8_0 and Q5_0 the lanes-over-rows kernel
-// is as fast or faster at m = 8 and well ahead at m = 1.  Like the split, it
-// depends on (wtype, rows, k) only.
+// 4096 it takes 108, 271 and 512 us at m = 1, 4 and 8 against 127, 150 and
+// 161 us on the tensor cores); for Q8_0 and Q5_0 the lanes-over-rows kernel
+// is well ahead at m <= 2 and the tensor cores pull ahead only from m = 4
+// (Q5_0 16384 x 4096: 21 against 29 us at m = 1, 50 against 36 at m = 8), so
+// they keep the lanes-over-rows kernel.  Like the split, it depends on
+// (wtype, rows, k) only.
 int auto_engine(int wt, uint64_t rows, uint32_t k) {
     (void)rows;
     (void)k;
