@@ -427,23 +427,30 @@ struct TcGeom {
 
 // Conversion of one chunk's inputs ([m][CV] binary32 at xs) into the B tiles
 // at bt by the consumer warps: K-step s, logical value v (A column order) of
-// input row j -> x_hi at tile row j, x_lo at tile row MP + j.  Work item =
-// one 16-byte row of a core matrix (8 logical values of one input row):
-// items of input row j are 32*j .. 32*j + 2*KSTEPS - 1, spread over the
-// consumer warps.  Rows m..MP-1 stay zero.
+// input row j -> x_hi at tile row j, x_lo at tile row MP + j.  Work item r of
+// input row j = one 16-byte row of a core matrix (logical values 8r .. 8r+7 of
+// K-step r/2, half r%2), read as 32 contiguous bytes of the staged row.  Input
+// rows lie a multiple of 128 bytes apart, so the bank of a read depends on r
+// alone and the bank of a tile store on j alone: lane i of each quarter warp
+// takes row 8*pass + i and item (b + i) mod 32, b = 4*warp + quarter, and
+// lanes 4..7 read their second 16 bytes first, so the eight 16-byte reads and
+// the eight stores of a quarter warp each fall in eight different banks.
+// Rows m..MP-1 stay zero.
 template <int WT, int MP>
 __device__ __forceinline__ void tc_convert_x(const float* xs, uint8_t* bt, uint32_t m, int tid) {
     using G = TcGeom<WT, MP>;
     constexpr int PER = 2 * G::KSTEPS;                      // items per input row (32 or 16)
-    constexpr int NT = G::CW * kLanes;
-    // thread t takes items it = t', t' + NT, ... of the interleaved order t' = (t % CW) * 32 + t / CW
-    const int tt = (tid % G::CW) * kLanes + tid / G::CW;
-    for (int it = tt; it < static_cast<int>(m) * 32; it += NT) {
-        const int j = it >> 5, r = it & 31;
-        if (r >= PER) continue;
-        const int s = r >> 1, kh = r & 1;
-        const float* src = xs + j * G::CV + 16 * s + 8 * kh;
-        const float4 u = ldx4(src), v = ldx4(src + 4);
+    static_assert(G::CW == 8 && PER <= 32, "8 consumer warps x 4 quarters cover the 32 item slots of a row");
+    const int lane = tid & 31, i = lane & 7;
+    const int r = ((tid >> 5) * 4 + (lane >> 3) + i) & 31;  // the same for every pass
+    const int sw = i >> 2;                                  // second half first
+    if (r >= PER) return;
+    const int s = r >> 1, kh = r & 1;
+    uint8_t* bs = bt + s * G::BKSTEP + kh * 128;
+    for (int j = i; j < static_cast<int>(m); j += 8) {
+        const float* src = xs + j * G::CV + 8 * r;
+        const float4 f0 = ldx4(src + 4 * sw), f1 = ldx4(src + 4 * (sw ^ 1));
+        const float4 u = sw ? f1 : f0, v = sw ? f0 : f1;
         float e[8];
         if constexpr (TcFmt<WT>::kPerm == 1) {
             e[0] = u.x; e[1] = u.z; e[2] = u.y; e[3] = u.w; e[4] = v.x; e[5] = v.z; e[6] = v.y; e[7] = v.w;
@@ -461,7 +468,6 @@ __device__ __forceinline__ void tc_convert_x(const float* xs, uint8_t* bt, uint3
             lo[p] = bf16x2_rn(r0, r1);
         }
         // tile rows: x_hi at j, x_lo at MP + j
-        uint8_t* bs = bt + s * G::BKSTEP + kh * 128;
         const int rl = MP + j;
         *reinterpret_cast<uint4*>(bs + (j >> 3) * 256 + (j & 7) * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(bs + (rl >> 3) * 256 + (rl & 7) * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
